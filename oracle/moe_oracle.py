@@ -1,0 +1,321 @@
+"""Plain fp64 CPU oracle for the sparse top-k routed MoE layer forward.
+
+TEST INFRASTRUCTURE ONLY.  Only tests/, __graft_entry__.smoke() and bench.py's CPU
+baseline leg may import or call this module.  It shares no code with the CUDA path and
+imports nothing from the library package: it takes numpy arrays and returns numpy
+arrays.
+
+Every function writes out the plain definition the pages give, in float64, with no
+blocking, fusion or reordering beyond what the definition states.  Library primitives
+used as steps: numpy matmul (a dot product over the hidden axis), numpy stable argsort,
+numpy exp.  Inputs that arrive as bf16/fp32 widen to float64 exactly.
+
+Sources (page title and section):
+  [KM]  AI Knowledge Map, "MoE: each token activates only a few FFNs" - router in four
+        steps (score, softmax, top-k hard selection, renormalise and combine); capacity
+        C = ceil(c*N*k/E) with the 6-token / 4-expert / top-2 worked example; overflow
+        handling (drop, reroute, larger c); load CV = std/mean.
+  [LI]  LLM Internals §14.2 "Mixture of experts" - §14.2.1 six steps and shapes
+        (input, router scoring, top-k + normalisation, dispatch permutation, grouped
+        GEMM, combine + shared expert); §14.2.2 parameter accounting; §14.2.3 balance
+        loss L = alpha*N*sum f_i p_i with worked example, bias-adjusted selection
+        (tech-report eq. 16), capacity factor with worked example; §14.2.4 shared
+        expert.
+  [SN]  "Mixture of Experts (MoE)" study notes, Case 1: top-k pseudo-code (softmax over
+        the k chosen values).
+
+Readings where the pages are silent (each is listed in the design doc):
+  * ties in top-k go to the lower expert index; the chosen set is written in ascending
+    expert order (the pages define S as a set);
+  * capacity keeps the lowest token indices of each expert;
+  * a dropped slot contributes nothing; the other gates are not renormalised;
+  * f_i counts router choices before capacity, f_i = m_i / (T*k);
+  * for sigmoid scoring, p_i averages the row-normalised affinities s / sum_e s;
+  * SwiGLU expert: h = SiLU(x W_gate) * (x W_up), y = h W_down, SiLU(z) = z*sigmoid(z),
+    no biases.
+
+Parity is pinned for every function here (tests/test_oracle_pins.py); none is unpinned.
+"""
+
+from __future__ import annotations
+
+from fractions import Fraction
+from typing import Callable, Dict, Optional, Sequence, Tuple
+
+import numpy as np
+
+f64 = np.float64
+
+
+# ---------------------------------------------------------------------------
+# Step 2: router scoring                                          [LI §14.2.1 step 2]
+# ---------------------------------------------------------------------------
+
+def router_logits(X: np.ndarray, Wg: np.ndarray,
+                  logit_bias: Optional[np.ndarray] = None) -> np.ndarray:
+    """l[t, e] = sum_h X[t, h] * W_g[h, e]  (+ a fixed per-expert logit offset).
+
+    [LI §14.2.1 step 2]: X[T, H] x W_g[H, E] -> s[T, E].  [KM] step one: W_r x.
+    Products of a bf16 or fp32 value by an fp32 value are exact in float64.
+    """
+    l = np.asarray(X, dtype=f64) @ np.asarray(Wg, dtype=f64)
+    if logit_bias is not None:
+        l = l + np.asarray(logit_bias, dtype=f64)[None, :]
+    return l
+
+
+def softmax_rows(l: np.ndarray) -> np.ndarray:
+    """g_e = exp(l_e) / sum_j exp(l_j) per row  [KM step two].
+
+    The row maximum is subtracted first; that leaves the quotient unchanged.
+    """
+    m = l.max(axis=1, keepdims=True)
+    z = np.exp(l - m)
+    return z / z.sum(axis=1, keepdims=True)
+
+
+def sigmoid(l: np.ndarray) -> np.ndarray:
+    """Per-cell affinity s = 1 / (1 + exp(-l))  [LI §14.2.1 step 2, DeepSeek-V3]."""
+    with np.errstate(over="ignore"):
+        return 1.0 / (1.0 + np.exp(-l))
+
+
+def selection_keys(l: np.ndarray, score: str,
+                   bias: Optional[np.ndarray] = None) -> np.ndarray:
+    """The value the top-k compares.
+
+    softmax: the logit itself (softmax is strictly increasing in each logit of a row,
+    so top-k on logits equals top-k on probabilities - [SN] Case 1 takes top-k on the
+    raw router scores, [KM] on the probabilities).
+    sigmoid: s + b, the bias taking part in selection only  [LI §14.2.3, eq. 16].
+    """
+    if score == "softmax":
+        return l.copy()
+    if score == "sigmoid":
+        s = sigmoid(l)
+        return s + (0.0 if bias is None else np.asarray(bias, dtype=f64)[None, :])
+    raise ValueError(score)
+
+
+# ---------------------------------------------------------------------------
+# Step 3: top-k hard selection and renormalisation     [LI §14.2.1 step 3; KM steps 3-4]
+# ---------------------------------------------------------------------------
+
+def select_topk(key: np.ndarray, k: int) -> Tuple[np.ndarray, np.ndarray]:
+    """The k largest keys of each row.
+
+    Returns idx[T, k] (the chosen experts, ascending expert index) and gap[T] =
+    key_(k) - key_(k+1), the margin between the k-th and (k+1)-th largest key
+    (+inf when k == E).  Ties go to the lower expert index (stable sort).
+    """
+    T, E = key.shape
+    order = np.argsort(-key, axis=1, kind="stable")
+    rows = np.arange(T)
+    if k < E:
+        gap = key[rows, order[:, k - 1]] - key[rows, order[:, k]]
+    else:
+        gap = np.full(T, np.inf)
+    idx = np.sort(order[:, :k], axis=1)
+    return idx.astype(np.int64), gap
+
+
+def gates_for(l: np.ndarray, idx: np.ndarray, score: str, renorm: bool) -> np.ndarray:
+    """Gate weights of the chosen experts.
+
+    softmax: g_e = softmax(l)_e; with renorm, g_e / sum_{e' in S} g_{e'}  [KM step four].
+    sigmoid: s_e = sigmoid(l_e) of the UNBIASED logit; with renorm, s_e / sum_S s
+             [LI §14.2.3 eq. 16: the gate keeps the original affinity; §14.2.1 step 3
+             normalises among the k chosen].
+    """
+    rows = np.arange(l.shape[0])[:, None]
+    if score == "softmax":
+        g = softmax_rows(l)[rows, idx]
+    elif score == "sigmoid":
+        g = sigmoid(l)[rows, idx]
+    else:
+        raise ValueError(score)
+    if renorm:
+        g = g / g.sum(axis=1, keepdims=True)
+    return g
+
+
+def row_probabilities(l: np.ndarray, score: str) -> np.ndarray:
+    """p[t, e] used by the balance statistics: the softmax row, or for sigmoid scoring
+    the affinities normalised over the row (an extension: the pages define p_i only as
+    "the router's mean probability for expert i")."""
+    if score == "softmax":
+        return softmax_rows(l)
+    s = sigmoid(l)
+    return s / s.sum(axis=1, keepdims=True)
+
+
+# ---------------------------------------------------------------------------
+# Capacity and step 4: dispatch permutation                  [KM capacity; LI §14.2.1]
+# ---------------------------------------------------------------------------
+
+def capacity(c: float, T: int, k: int, E: int) -> int:
+    """C = ceil(c * N * k / E) with N the token count  [KM capacity formula].
+
+    Evaluated exactly: the float c is the dyadic rational it stores.
+    """
+    q = Fraction(c) * T * k / E
+    return int(-((-q.numerator) // q.denominator))
+
+
+def dispatch(idx: np.ndarray, E: int, C: Optional[int] = None) -> Dict[str, np.ndarray]:
+    """Group the (token, choice) slots by expert  [LI §14.2.1 step 4].
+
+    Slot s = t*k + j is the j-th choice of token t.  m_e counts the slots routed to e
+    (before capacity).  With a capacity C, expert e keeps its C slots of lowest token
+    index and drops the rest  [KM overflow: drop].  Rows of the permuted batch are
+    ordered by (expert ascending, token ascending); offsets[e] is the first row of e.
+    row_of_slot[s] = permuted row of slot s, or -1 when the slot was dropped;
+    slot_of_row is its inverse on the kept rows.
+    """
+    T, k = idx.shape
+    flat = idx.reshape(-1)
+    counts = np.bincount(flat, minlength=E).astype(np.int64)
+    kept = counts.copy() if C is None else np.minimum(counts, C)
+    offsets = np.zeros(E + 1, dtype=np.int64)
+    offsets[1:] = np.cumsum(kept)
+    R = int(offsets[-1])
+    row_of_slot = np.full(T * k, -1, dtype=np.int64)
+    slot_of_row = np.full(R, -1, dtype=np.int64)
+    for e in range(E):
+        # a token routes to e at most once, so ascending slot = ascending token
+        slots = np.nonzero(flat == e)[0]
+        keep = slots[: kept[e]]
+        rows = offsets[e] + np.arange(keep.size)
+        row_of_slot[keep] = rows
+        slot_of_row[rows] = keep
+    return dict(counts=counts, kept=kept, offsets=offsets,
+                row_of_slot=row_of_slot, slot_of_row=slot_of_row)
+
+
+# ---------------------------------------------------------------------------
+# Step 5: one SwiGLU expert                                  [LI §14.2.1 step 5, §14.2.2]
+# ---------------------------------------------------------------------------
+
+def swiglu_expert(x: np.ndarray, W_gate: np.ndarray, W_up: np.ndarray,
+                  W_down: np.ndarray) -> np.ndarray:
+    """y = (SiLU(x W_gate^T) * (x W_up^T)) W_down^T for a batch of rows x[m, H].
+
+    Weights are stored output-major: W_gate, W_up [I, H]; W_down [H, I].  The expert is
+    the three-matrix SwiGLU of [LI §14.2.2]; [LI §14.2.1 step 5] projects [m, H] to
+    [m, I] and back to H.
+    """
+    x = np.asarray(x, dtype=f64)
+    a = x @ np.asarray(W_gate, dtype=f64).T
+    u = x @ np.asarray(W_up, dtype=f64).T
+    h = a * sigmoid(a) * u
+    return h @ np.asarray(W_down, dtype=f64).T
+
+
+# ---------------------------------------------------------------------------
+# Balance statistics                             [LI §14.2.3; KM monitoring, CV]
+# ---------------------------------------------------------------------------
+
+def balance_loss(f: Sequence[float], p: Sequence[float], alpha: float) -> float:
+    """L = alpha * N * sum_i f_i p_i with N the number of experts  [LI §14.2.3]."""
+    f = np.asarray(f, dtype=f64)
+    p = np.asarray(p, dtype=f64)
+    return float(alpha * f.size * np.sum(f * p))
+
+
+def balance_stats(counts: np.ndarray, prob_colsum: np.ndarray, T: int, k: int,
+                  n_kept: int, alpha: float) -> Dict[str, object]:
+    """f_i = m_i/(T k) (router choices before capacity), p_i = mean_t p[t, i],
+    loss = alpha*E*sum f p, drop rate = dropped slots / (T k),
+    CV = population std / mean of m_i  [KM monitoring], routing entropy -sum f ln f
+    [LI §14.2.3 monitoring: routing entropy, per-expert load, drop rate]."""
+    counts = np.asarray(counts, dtype=f64)
+    E = counts.size
+    f = counts / (T * k)
+    p = np.asarray(prob_colsum, dtype=f64) / T
+    loss = balance_loss(f, p, alpha)
+    drop_rate = (T * k - n_kept) / (T * k)
+    mean = counts.mean()
+    cv = float(np.sqrt(np.mean((counts - mean) ** 2)) / mean) if mean > 0 else 0.0
+    nz = f[f > 0]
+    entropy = float(-np.sum(nz * np.log(nz)))
+    return dict(f=f, p=p, loss=loss, drop_rate=drop_rate, cv=cv, entropy=entropy)
+
+
+# ---------------------------------------------------------------------------
+# The whole layer                                  [LI §14.2.1 steps 1-6; KM combine]
+# ---------------------------------------------------------------------------
+
+def route(X, Wg, k: int, score: str, renorm: bool, bias=None, logit_bias=None,
+          C: Optional[int] = None) -> Dict[str, np.ndarray]:
+    """Steps 2-4 on every token (capacity is a property of the whole batch)."""
+    l = router_logits(X, Wg, logit_bias)
+    key = selection_keys(l, score, bias)
+    idx, gap = select_topk(key, k)
+    g = gates_for(l, idx, score, renorm)
+    d = dispatch(idx, Wg.shape[1], C)
+    d.update(logits=l, key=key, idx=idx, gap=gap, gate=g,
+             prob_colsum=row_probabilities(l, score).sum(axis=0))
+    return d
+
+
+ExpertFn = Callable[[int], Tuple[np.ndarray, np.ndarray, np.ndarray]]
+
+
+def combine_subset(X, routing: Dict[str, np.ndarray], expert: ExpertFn, tokens,
+                   shared: Optional[Tuple[np.ndarray, np.ndarray, np.ndarray]] = None
+                   ) -> np.ndarray:
+    """Steps 5-6 for the given tokens: Y[t] = sum over kept j of g_j * E_{idx_j}(x_t)
+    plus the shared expert's output  [LI §14.2.1 step 6; KM final weighted sum].
+
+    `expert(e)` returns (W_gate[e], W_up[e], W_down[e]); experts are fetched one at a
+    time, and only those that a kept slot of the given tokens uses.
+    """
+    tokens = np.asarray(tokens, dtype=np.int64)
+    X = np.asarray(X)
+    idx, gate, ros = routing["idx"], routing["gate"], routing["row_of_slot"]
+    T, k = idx.shape
+    H = X.shape[1]
+    Y = np.zeros((tokens.size, H), dtype=f64)
+    uses: Dict[int, list] = {}
+    for n, t in enumerate(tokens):
+        for j in range(k):
+            if ros[t * k + j] >= 0:
+                uses.setdefault(int(idx[t, j]), []).append((n, j))
+    for e in sorted(uses):
+        Wgt, Wup, Wdn = expert(e)
+        sel = np.asarray(uses[e], dtype=np.int64)
+        sel_t, sel_j = sel[:, 0], sel[:, 1]
+        o = swiglu_expert(X[tokens[sel_t]], Wgt, Wup, Wdn)
+        Y[sel_t] += gate[tokens[sel_t], sel_j][:, None] * o
+    if shared is not None:
+        Y += swiglu_expert(X[tokens], *shared)
+    return Y
+
+
+def moe_layer(X, Wg, W_gate, W_up, W_down, k: int, score: str, renorm: bool,
+              bias=None, logit_bias=None, C: Optional[int] = None,
+              shared=None, tokens=None) -> Tuple[np.ndarray, Dict[str, np.ndarray]]:
+    """The full forward on in-memory weights (small workloads)."""
+    routing = route(X, Wg, k, score, renorm, bias, logit_bias, C)
+    if tokens is None:
+        tokens = np.arange(np.asarray(X).shape[0])
+    Y = combine_subset(X, routing, lambda e: (W_gate[e], W_up[e], W_down[e]), tokens,
+                       shared)
+    return Y, routing
+
+
+# ---------------------------------------------------------------------------
+# Parameter accounting                                           [LI §14.2.2]
+# ---------------------------------------------------------------------------
+
+def expert_params(H: int, I: int) -> int:
+    """One SwiGLU expert is three [H, I] matrices: 3*H*I parameters."""
+    return 3 * H * I
+
+
+def layer_params(H: int, I: int, routed: int, shared: int) -> int:
+    return (routed + shared) * expert_params(H, I)
+
+
+def active_params(H: int, I: int, k: int, shared: int) -> int:
+    return (k + shared) * expert_params(H, I)

@@ -1,0 +1,342 @@
+"""Pins of the fp64 oracle to what the pages and the mathematics fix (CPU only).
+
+Each test checks the oracle against something other than itself: a value printed in a
+worked example of the pages (fixtures under tests/golden/, each naming its source), a
+closed form, brute force on tiny inputs, or an invariant the definition implies.
+"""
+
+import itertools
+import math
+
+import numpy as np
+import pytest
+
+from oracle import moe_oracle as O
+
+
+# ---------------------------------------------------------------- parameter accounting
+
+def test_param_accounting(golden):
+    g = golden("param_accounting.json")
+    H, I = g["hidden_size"], g["moe_intermediate_size"]
+    pe = O.expert_params(H, I)
+    assert pe == g["params_per_expert"] == 44_040_192
+    layer = O.layer_params(H, I, g["routed"], g["shared"])
+    assert round(layer / 1e9, 2) == g["layer_params_approx_B"]
+    assert round(g["moe_layers"] * layer / 1e9, 1) == g["all_moe_layers_approx_B"]
+    act = O.active_params(H, I, g["top_k"], g["shared"])
+    assert round(act / 1e6, 1) == g["active_per_token_layer_approx_M"]
+    assert round(g["moe_layers"] * act / 1e9, 2) == g["active_all_layers_approx_B"]
+    assert round(100 * act / layer, 1) == g["active_fraction_percent_approx"]
+    assert math.comb(256, 8) == g["comb_256_8"]
+    assert math.comb(8, 2) == g["comb_8_2"]
+    assert abs(g["comb_256_8"] / g["comb_8_2"] / g["comb_ratio_approx"] - 1) < 0.05
+
+
+# ---------------------------------------------------------------- balance loss
+
+def test_balance_loss_worked_example(golden):
+    g = golden("balance_loss_example.json")
+    f, p = np.array(g["f"]), np.array(g["p"])
+    np.testing.assert_allclose(f * p, g["f_times_p"], atol=1e-15)
+    assert abs(O.balance_loss(f, p, 1.0) / g["N_experts"] - g["sum_f_p"]) < 1e-15
+    assert abs(O.balance_loss(f, p, 1.0) - g["N_sum_f_p"]) < 1e-14
+    b = g["balanced"]
+    assert abs(O.balance_loss(b["f"], b["p"], 1.0) - b["N_sum_f_p"]) < 1e-15
+    one_hot = [1.0, 0.0, 0.0, 0.0]
+    assert abs(O.balance_loss(one_hot, one_hot, 1.0) - g["collapsed_N_sum_f_p"]) < 1e-15
+    # alpha scales linearly
+    assert abs(O.balance_loss(f, p, 0.01) - 0.01 * g["N_sum_f_p"]) < 1e-15
+
+
+def test_balance_stats_from_counts(golden):
+    g = golden("balance_loss_example.json")
+    # 10 tokens, top-1: counts 7,1,1,1 give f = [.7,.1,.1,.1]; column sums of p give p
+    counts = np.array([7, 1, 1, 1])
+    colsum = np.array(g["p"]) * 10
+    s = O.balance_stats(counts, colsum, T=10, k=1, n_kept=10, alpha=1.0)
+    np.testing.assert_allclose(s["f"], g["f"], atol=1e-15)
+    assert abs(s["loss"] - g["N_sum_f_p"]) < 1e-14
+    assert s["drop_rate"] == 0.0
+    # CV = population std / mean of [7,1,1,1]: mean 2.5, var = (20.25+3*2.25)/4 = 6.75
+    assert abs(s["cv"] - math.sqrt(6.75) / 2.5) < 1e-15
+    ent = -(0.7 * math.log(0.7) + 3 * 0.1 * math.log(0.1))
+    assert abs(s["entropy"] - ent) < 1e-15
+    # uniform load: CV 0, entropy ln E, loss alpha
+    s = O.balance_stats(np.array([5, 5, 5, 5]), np.full(4, 5.0), T=20, k=1, n_kept=15,
+                        alpha=0.01)
+    assert s["cv"] == 0.0 and abs(s["entropy"] - math.log(4)) < 1e-15
+    assert abs(s["loss"] - 0.01) < 1e-17 and s["drop_rate"] == 0.25
+
+
+# ---------------------------------------------------------------- capacity
+
+def test_capacity_worked_examples(golden):
+    g = golden("capacity_examples.json")
+    km = g["knowledge_map"]
+    assert km["T"] * km["k"] == km["requests"]
+    assert O.capacity(1.0, km["T"], km["k"], km["E"]) == km["C_at_c_1.0"]
+    assert O.capacity(2.0, km["T"], km["k"], km["E"]) == km["C_at_c_2.0"]
+    li = g["llm_internals"]
+    C = O.capacity(li["capacity_factor"], li["T"], li["k"], li["E"])
+    assert C == li["slots_per_expert"]
+    assert li["T"] * li["k"] // li["E"] == li["average_per_expert"]
+    assert li["hot_expert_received"] - C == li["hot_expert_dropped"]
+    assert li["E"] * C == li["total_slots"]
+    assert li["E"] * C - li["T"] * li["k"] == li["idle_slots_if_uniform"]
+    # ceil, not floor or round: 7 requests over 2 experts at c=1 -> 4
+    assert O.capacity(1.0, 7, 1, 2) == 4
+    assert O.capacity(1.0, 6, 1, 4) == 2
+    assert O.capacity(0.0, 6, 2, 4) == 0
+    # the Switch workload: T=16384, E=64, top-1
+    assert O.capacity(1.0, 16384, 1, 64) == 256
+    assert O.capacity(1.25, 16384, 1, 64) == 320
+
+
+@pytest.mark.parametrize("c", ["c_1.0", "c_2.0"])
+def test_dispatch_six_token_example(golden, c):
+    g = golden("six_token_routing.json")
+    idx = np.array(g["idx"])
+    exp = g[c]
+    d = O.dispatch(idx, g["E"], exp["C"])
+    assert d["counts"].tolist() == g["counts"]
+    assert d["kept"].tolist() == exp["kept"]
+    assert d["offsets"].tolist() == exp["offsets"]
+    assert d["row_of_slot"].tolist() == exp["row_of_slot"]
+    assert d["slot_of_row"].tolist() == exp["slot_of_row"]
+    assert np.nonzero(d["row_of_slot"] < 0)[0].tolist() == exp["dropped_slots"]
+
+
+def test_dispatch_invariants():
+    rng = np.random.default_rng(3)
+    T, E, k = 50, 7, 3
+    idx = np.sort(np.stack([rng.choice(E, k, replace=False) for _ in range(T)]), 1)
+    for C in (None, 0, 5, 21, 1000):
+        d = O.dispatch(idx, E, C)
+        ros, sor, off = d["row_of_slot"], d["slot_of_row"], d["offsets"]
+        kept = ros >= 0
+        # mutual inverses
+        assert np.all(sor[ros[kept]] == np.nonzero(kept)[0])
+        assert np.all(ros[sor] == np.arange(sor.size))
+        # rows sorted by (expert, token) and grouped at offsets
+        ex = idx.reshape(-1)[sor]
+        tok = sor // k
+        assert np.all(np.diff(ex) >= 0)
+        for e in range(E):
+            seg = slice(off[e], off[e + 1])
+            assert np.all(ex[seg] == e)
+            assert np.all(np.diff(tok[seg]) > 0)
+        # capacity keeps the lowest token indices, sum kept = sum min(m, C)
+        cap = np.inf if C is None else C
+        assert off[-1] == sum(min(m, cap) for m in d["counts"])
+        for e in range(E):
+            toks = np.nonzero((idx == e).any(1))[0]
+            kept_toks = tok[off[e]:off[e + 1]]
+            assert kept_toks.tolist() == toks[: len(kept_toks)].tolist()
+        # dropless reproduces the counts
+        if C is None:
+            assert np.all(d["kept"] == d["counts"]) and kept.all()
+    # gather by slot_of_row then scatter by row_of_slot returns the kept rows unchanged
+    X = rng.standard_normal((T, 4))
+    d = O.dispatch(idx, E, 5)
+    Xperm = X[d["slot_of_row"] // k]
+    back = np.zeros((T * k, 4))
+    back[d["slot_of_row"]] = Xperm
+    kept = d["row_of_slot"] >= 0
+    assert np.array_equal(back[kept], X[np.nonzero(kept)[0] // k])
+
+
+# ---------------------------------------------------------------- scoring and top-k
+
+def test_router_logits_one_hot_and_offset():
+    rng = np.random.default_rng(0)
+    H, E = 5, 3
+    Wg = rng.standard_normal((H, E))
+    X = np.eye(H)[[2, 0, 4]]            # one-hot rows pick rows of W_g
+    l = O.router_logits(X, Wg)
+    assert np.array_equal(l, Wg[[2, 0, 4]])
+    off = np.array([0.5, -1.0, 0.0])
+    assert np.array_equal(O.router_logits(X, Wg, off), Wg[[2, 0, 4]] + off)
+    # a wrong orientation (W_g^T) would not even have these shapes
+    assert l.shape == (3, E)
+
+
+def test_softmax_two_experts_closed_form():
+    l = np.array([[0.3, -1.2], [5.0, 5.0], [-40.0, 2.0]])
+    p = O.softmax_rows(l)
+    for r in range(3):
+        d = l[r, 0] - l[r, 1]
+        assert abs(p[r, 0] - 1.0 / (1.0 + math.exp(-d))) < 1e-15
+    np.testing.assert_allclose(p.sum(1), 1.0, atol=1e-15)
+    # shift invariance and strict monotonicity
+    assert np.allclose(O.softmax_rows(l + 7.0), p, atol=1e-15)
+
+
+def test_sigmoid_closed_form():
+    l = np.array([[0.0, math.log(3.0), -math.log(3.0)]])
+    np.testing.assert_allclose(O.sigmoid(l), [[0.5, 0.75, 0.25]], atol=1e-15)
+    assert O.sigmoid(np.array([[-1000.0]]))[0, 0] == 0.0
+
+
+def test_topk_brute_force():
+    rng = np.random.default_rng(7)
+    for E in (2, 3, 5, 8):
+        for k in range(1, E + 1):
+            key = rng.standard_normal((12, E))
+            idx, gap = O.select_topk(key, k)
+            for t in range(12):
+                best = max(itertools.combinations(range(E), k),
+                           key=lambda S: sum(key[t, list(S)]))
+                assert idx[t].tolist() == sorted(best)
+                srt = sorted(key[t], reverse=True)
+                want_gap = srt[k - 1] - srt[k] if k < E else math.inf
+                assert gap[t] == want_gap
+
+
+def test_topk_ties_lower_index():
+    key = np.array([[1.0, 2.0, 2.0, 2.0, 0.0]])
+    idx, gap = O.select_topk(key, 2)
+    assert idx.tolist() == [[1, 2]] and gap[0] == 0.0
+
+
+def test_renorm_two_page_forms_agree():
+    """[KM] renormalises the full softmax over S; [SN] takes softmax of the k chosen
+    scores.  The full denominator cancels, so the two must agree."""
+    rng = np.random.default_rng(1)
+    l = rng.standard_normal((20, 8)) * 2
+    for k in (1, 2, 3, 8):
+        idx, _ = O.select_topk(l, k)
+        g = O.gates_for(l, idx, "softmax", True)
+        chosen = np.take_along_axis(l, idx, 1)
+        z = np.exp(chosen - chosen.max(1, keepdims=True))
+        np.testing.assert_allclose(g, z / z.sum(1, keepdims=True), rtol=1e-14, atol=1e-16)
+        np.testing.assert_allclose(g.sum(1), 1.0, atol=1e-14)
+        if k == 8:
+            np.testing.assert_allclose(g, O.softmax_rows(l), rtol=1e-14)
+    # without renorm, the gate is the plain probability and gates sum to < 1
+    idx, _ = O.select_topk(l, 2)
+    g = O.gates_for(l, idx, "softmax", False)
+    assert np.all(g.sum(1) < 1.0)
+    np.testing.assert_allclose(g, np.take_along_axis(O.softmax_rows(l), idx, 1))
+
+
+def test_sigmoid_bias_selects_but_does_not_weigh():
+    """[LI §14.2.3 eq. 16]: the bias enters the top-k comparison only."""
+    l = np.array([[0.0, math.log(3.0), -math.log(3.0)]])   # s = .5, .75, .25
+    bias = np.array([0.0, 0.0, 0.6])                        # keys .5, .75, .85
+    key = O.selection_keys(l, "sigmoid", bias)
+    idx, gap = O.select_topk(key, 2)
+    assert idx.tolist() == [[1, 2]]
+    assert abs(gap[0] - (0.75 - 0.5)) < 1e-15
+    g = O.gates_for(l, idx, "sigmoid", True)
+    np.testing.assert_allclose(g, [[0.75, 0.25]], atol=1e-15)
+    idx0, _ = O.select_topk(O.selection_keys(l, "sigmoid", None), 2)
+    assert idx0.tolist() == [[0, 1]]
+    np.testing.assert_allclose(O.gates_for(l, idx0, "sigmoid", True), [[0.4, 0.6]],
+                               atol=1e-15)
+
+
+# ---------------------------------------------------------------- expert and layer
+
+def _silu(z):
+    return z / (1.0 + math.exp(-z))
+
+
+def test_swiglu_scalar_closed_form():
+    # H = I = 1: y = w_d * silu(w_g x) * (w_u x)
+    y = O.swiglu_expert(np.array([[1.0]]), np.array([[2.0]]), np.array([[3.0]]),
+                        np.array([[5.0]]))
+    assert abs(y[0, 0] - 5.0 * _silu(2.0) * 3.0) < 1e-13
+    # swapping gate and up gives a different value: the pin catches a swap
+    assert abs(5.0 * _silu(3.0) * 2.0 - 5.0 * _silu(2.0) * 3.0) > 1.0
+    assert O.swiglu_expert(np.zeros((1, 1)), np.ones((1, 1)), np.ones((1, 1)),
+                           np.ones((1, 1)))[0, 0] == 0.0
+
+
+def test_swiglu_one_hot_orientation():
+    """Non-square weights with one-hot inputs: each output is a scalar expression."""
+    rng = np.random.default_rng(5)
+    H, I = 3, 4
+    Wg, Wu, Wd = rng.standard_normal((I, H)), rng.standard_normal((I, H)), \
+        rng.standard_normal((H, I))
+    for hsel in range(H):
+        x = np.zeros((1, H))
+        x[0, hsel] = 1.0
+        y = O.swiglu_expert(x, Wg, Wu, Wd)[0]
+        for o in range(H):
+            want = sum(Wd[o, i] * _silu(Wg[i, hsel]) * Wu[i, hsel] for i in range(I))
+            assert abs(y[o] - want) < 1e-13
+
+
+def test_layer_single_expert_is_dense_swiglu():
+    """E = 1, k = 1: the gate is 1 and the layer is the one expert."""
+    X = np.array([[1.0], [-0.5]])
+    Wg = np.array([[0.3]])
+    Y, r = O.moe_layer(X, Wg, np.array([[[2.0]]]), np.array([[[3.0]]]),
+                       np.array([[[5.0]]]), k=1, score="softmax", renorm=True)
+    assert r["gate"].tolist() == [[1.0], [1.0]]
+    for t, x in enumerate([1.0, -0.5]):
+        assert abs(Y[t, 0] - 5.0 * _silu(2.0 * x) * 3.0 * x) < 1e-13
+
+
+def test_layer_combine_weights_and_shared():
+    """Two scalar experts, top-2 softmax renorm: Y = g0*E0(x) + g1*E1(x) + shared(x)."""
+    X = np.array([[1.0]])
+    Wg = np.array([[0.0, math.log(3.0)]])          # logits 0, ln3 -> gates 1/4, 3/4
+    Wgt = np.array([[[2.0]], [[1.0]]])
+    Wup = np.array([[[3.0]], [[1.0]]])
+    Wdn = np.array([[[5.0]], [[4.0]]])
+    sh = (np.array([[1.0]]), np.array([[2.0]]), np.array([[-1.0]]))
+    Y, r = O.moe_layer(X, Wg, Wgt, Wup, Wdn, k=2, score="softmax", renorm=True,
+                       shared=sh)
+    np.testing.assert_allclose(r["gate"], [[0.25, 0.75]], atol=1e-15)
+    e0 = 5.0 * _silu(2.0) * 3.0
+    e1 = 4.0 * _silu(1.0) * 1.0
+    s = -1.0 * _silu(1.0) * 2.0
+    assert abs(Y[0, 0] - (0.25 * e0 + 0.75 * e1 + s)) < 1e-13
+
+
+def test_layer_drop_contributes_nothing():
+    """Capacity 0 drops every slot: only the shared expert remains; with capacity 1 the
+    second token loses its slot and its gate is not renormalised onto anything."""
+    X = np.array([[1.0], [2.0]])
+    Wg = np.array([[1.0]])
+    W = np.array([[[1.0]]])
+    sh = (np.array([[1.0]]), np.array([[1.0]]), np.array([[1.0]]))
+    Y, r = O.moe_layer(X, Wg, W, W, W, k=1, score="softmax", renorm=True, C=0,
+                       shared=sh)
+    for t, x in enumerate([1.0, 2.0]):
+        assert abs(Y[t, 0] - _silu(x) * x) < 1e-13
+    Y, r = O.moe_layer(X, Wg, W, W, W, k=1, score="softmax", renorm=True, C=1)
+    assert r["row_of_slot"].tolist() == [0, -1]
+    assert abs(Y[0, 0] - _silu(1.0)) < 1e-13 and Y[1, 0] == 0.0
+
+
+def test_identity_experts_round_trip():
+    """Dispatch then combine with identity experts and renormalised gates returns X:
+    the gates of a token sum to 1 [KM], and the permutation pair is inverse [LI 14.2.1]."""
+    rng = np.random.default_rng(11)
+    T, H, E, k = 30, 6, 5, 3
+    X = rng.standard_normal((T, H))
+    l = rng.standard_normal((T, E))
+    idx, _ = O.select_topk(l, k)
+    g = O.gates_for(l, idx, "softmax", True)
+    d = O.dispatch(idx, E)
+    Xperm = X[d["slot_of_row"] // k]            # step 4: gather
+    Operm = Xperm.copy()                        # identity experts
+    Y = np.zeros_like(X)
+    for s in range(T * k):                      # step 6: weighted scatter back
+        Y[s // k] += g[s // k, s % k] * Operm[d["row_of_slot"][s]]
+    np.testing.assert_allclose(Y, X, atol=1e-14)
+
+
+def test_route_probabilities_and_gap():
+    rng = np.random.default_rng(2)
+    X = rng.standard_normal((10, 6))
+    Wg = rng.standard_normal((6, 4)) * 0.5
+    r = O.route(X, Wg, 2, "softmax", True)
+    np.testing.assert_allclose(r["prob_colsum"].sum(), 10.0, atol=1e-12)
+    srt = -np.sort(-r["logits"], 1)
+    np.testing.assert_allclose(r["gap"], srt[:, 1] - srt[:, 2], atol=0)
+    r = O.route(X, Wg, 2, "sigmoid", True, bias=np.zeros(4))
+    np.testing.assert_allclose(r["prob_colsum"].sum(), 10.0, atol=1e-12)

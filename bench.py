@@ -1,0 +1,347 @@
+#!/usr/bin/env python3
+"""Benchmark of the MoE layer forward on B300: tokens/s of one full forward (router,
+dispatch, grouped SwiGLU experts, combine, balance statistics) through the C ABI.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl reference]
+
+One JSON line on stdout (rank 0).  With --gpus N > 1 (launched by torch.distributed.run)
+every rank runs an independent replica of the workload on its own GPU (weak scaling; the
+forward has no cross-GPU exchange) and the time is the maximum over ranks.
+
+--impl reference times the fp64 CPU oracle on a bounded sample of the same workload
+(rank 0 only), the slow program the kernels are checked against.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from sparse_top_routing_router_b300 import configs as K  # noqa: E402
+from sparse_top_routing_router_b300.inputs import make_inputs, token_subset  # noqa: E402
+
+METRIC = "MoE-layer fwd tokens/s on 1 B300; % of bf16 tensor peak / % of HBM roofline"
+DEFAULT_CONFIG = K.MIXTRAL.name
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "expert_gate_up_traffic.json")
+KERNEL_SRC = os.path.join(ROOT, "sparse_top_routing_router_b300", "csrc", "expert_tc.cu")
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def workload_config(cfg: K.MoEConfig, cf) -> dict:
+    d = {"workload": cfg.name, "T": cfg.T, "H": cfg.H, "E": cfg.E, "I": cfg.I, "k": cfg.k,
+         "score": cfg.score, "renorm": cfg.renorm, "shared_expert": cfg.shared,
+         "capacity_factor": cf, "router": "fp32", "experts": cfg.dtype}
+    return d
+
+
+def peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as fh:
+            j = json.load(fh)
+        return {"hbm_gbs": j["hbm_gbs"], "bf16_tflops": j["bf16_tflops"],
+                "bf16_tflops_sustained": j.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0,
+            "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi sampled every 200 ms while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def traffic_from_profile():
+    """dram bytes per launch of expert_gate_up from the committed ncu summary, if the
+    kernel source has not changed since it was captured."""
+    if not os.path.exists(PROFILE_TRAFFIC):
+        return None
+    with open(PROFILE_TRAFFIC) as fh:
+        j = json.load(fh)
+    with open(KERNEL_SRC, "rb") as fh:
+        h = hashlib.sha256(fh.read()).hexdigest()[:16]
+    if j.get("kernel_sha") != h:
+        return None
+    return j
+
+
+# --------------------------------------------------------------------------- CPU oracle
+
+def oracle_sample(cfg, d, cf, n_tokens: int, seed: int):
+    """Time the fp64 oracle: routing of all T tokens (capacity is a batch property), then
+    experts + combine for a seeded sample of n_tokens.  Expert weights of the sample are
+    staged in host memory before the clock starts."""
+    import numpy as np
+    from threadpoolctl import threadpool_info
+
+    from oracle import moe_oracle as O
+
+    def host(t):
+        return t.detach().to("cpu").float().numpy()
+
+    X = host(d["X"])
+    Wg = host(d["Wg"])
+    bias = host(d["bias"]) if "bias" in d else None
+    lb = host(d["logit_bias"]) if "logit_bias" in d else None
+    C = None if cf is None else O.capacity(cf, cfg.T, cfg.k, cfg.E)
+    t0 = time.perf_counter()
+    r = O.route(X, Wg, cfg.k, cfg.score, cfg.renorm, bias, lb, C)
+    t_route = time.perf_counter() - t0
+    tokens = token_subset(cfg.T, n_tokens, seed).numpy()
+    need = sorted({int(e) for e in r["idx"][tokens].reshape(-1)})
+    W = {e: (host(d["W_gate"][e]), host(d["W_up"][e]), host(d["W_down"][e])) for e in need}
+    shared = (host(d["Ws_gate"]), host(d["Ws_up"]), host(d["Ws_down"])) if cfg.shared else None
+    t0 = time.perf_counter()
+    O.combine_subset(X, r, lambda e: W[e], tokens, shared)
+    t_ffn = time.perf_counter() - t0
+    threads = max([i.get("num_threads", 1) for i in threadpool_info()] or [1])
+    return t_route, t_ffn, int(tokens.size), threads
+
+
+def run_reference(args, cfg, cf):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    d = make_inputs(cfg, device="cpu")
+    n_tok = args.ref_tokens
+    times = []
+    threads = 1
+    for i in range(args.warmup + args.steps):
+        tr, tf, n, threads = oracle_sample(cfg, d, cf, n_tok, seed=1 + i)
+        if i >= args.warmup:
+            times.append(cfg.T / (tr + tf * cfg.T / n))
+        log(f"reference step {i}: route {tr:.2f}s ffn({n} tok) {tf:.2f}s")
+    v = statistics.mean(times)
+    sample = (f"routing of all {cfg.T} tokens + experts/combine of {n_tok} seeded tokens "
+              f"per step, throughput extrapolated to {cfg.T} tokens")
+    line = {"metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * cfg.T / v,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f64", "data": "synthetic", "impl": "reference",
+            "config": workload_config(cfg, cf),
+            "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": threads,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------------------- GPU arm
+
+def run_gpu(args, cfg, cf):
+    from sparse_top_routing_router_b300.layer import MoELayer
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+    d = make_inputs(cfg, device=dev, seed=cfg.seed + rank)
+    layer = MoELayer(cfg, d, device=local, capacity_factor=cf)
+    X = d["X"]
+    stream = torch.cuda.current_stream()
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    for _ in range(args.warmup):
+        layer.forward(X)
+    torch.cuda.synchronize()
+    st = layer.device_status()
+    if st != 0:
+        raise RuntimeError(f"device status {st} after warm-up")
+    R = int(layer.offsets[-1].item())
+
+    # ---- timed region: K forwards, inputs resident in HBM
+    layer.ctx.set_tracing(True)
+    layer.ctx.trace_read()
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    barrier()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        layer.forward(X)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    clk = clocks.stop()
+    ms = ev0.elapsed_time(ev1)
+    kern = layer.ctx.trace_read()
+    layer.ctx.set_tracing(False)
+    if dist is not None:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    ms_step = ms / args.steps
+    value = world * cfg.T * args.steps / (ms / 1e3)
+
+    # ---- end to end: pinned host X -> device, forward, device Y -> pinned host
+    Xh = torch.empty(X.shape, dtype=X.dtype, pin_memory=True)
+    Xh.copy_(X)
+    Yh = torch.empty(layer.Y.shape, dtype=layer.Y.dtype, pin_memory=True)
+    Xd = torch.empty_like(X)
+    for _ in range(2):
+        layer.forward_host(Xh, Yh, Xd)
+    torch.cuda.synchronize()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        layer.forward_host(Xh, Yh, Xd)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    ms_e2e = e0.elapsed_time(e1)
+    if dist is not None:
+        t = torch.tensor([ms_e2e], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_e2e = float(t.item())
+    st = layer.device_status()
+    if st != 0:
+        raise RuntimeError(f"device status {st} after the timed region")
+
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return
+
+    pk = peaks()
+    n_gu, ms_gu = kern["expert_gate_up"]
+    gu_ms = ms_gu / max(n_gu, 1)
+    gu_flops = 2.0 * (R + (cfg.T if cfg.shared else 0)) * cfg.H * 2 * cfg.I
+    achieved = gu_flops / (gu_ms / 1e3) / 1e12
+    prof = traffic_from_profile()
+    roofline = {"kernel": "expert_gate_up", "bound": "tensor", "achieved": achieved,
+                "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": achieved / pk["bf16_tflops"],
+                "peak_source": pk["source"] + " bf16 burst (MEASURED_PEAKS.json)"
+                if pk["source"] == "measured" else "fallback bf16 burst",
+                "traffic": prof["dram_bytes_per_launch"] if prof else None,
+                "algorithmic_flops_per_launch": gu_flops, "avg_launch_ms": gu_ms}
+    launches = sum(n for n, _ in kern.values())
+    layer_flops = cfg.flops(R)
+    kernels = {k: {"launches": n, "ms_per_step": t / args.steps,
+                   "share": t / max(sum(x for _, x in kern.values()), 1e-9)}
+               for k, (n, t) in kern.items() if n}
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16"
+        if cfg.dtype == "bf16" else "f32",
+        "data": "synthetic (seeded N(0,1) tokens, N(0,0.02) random-init weights)",
+        "config": dict(workload_config(cfg, cf),
+                       l2="inputs larger than L2: all expert weights "
+                          f"({3 * cfg.E * cfg.H * cfg.I * (2 if cfg.dtype == 'bf16' else 4) / 1e9:.2f} GB)"
+                          " stream from HBM every step",
+                       kept_rows=R, parallelism=f"replicas x{world}"),
+        "tflops": layer_flops * args.steps / (ms / 1e3) / 1e12 / world * world,
+        "roofline": roofline,
+        "e2e": {"value": world * cfg.T * args.steps / (ms_e2e / 1e3), "unit": "tokens/s",
+                "h2d_bytes_per_step": X.numel() * X.element_size(),
+                "d2h_bytes_per_step": layer.Y.numel() * layer.Y.element_size()},
+        "gpu_launches": launches,
+        "kernels": kernels,
+        "clocks": clk,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        tr, tf, n, threads = oracle_sample(cfg, d, cf, args.cpu_tokens, seed=1)
+        v = cfg.T / (tr + tf * cfg.T / n)
+        line["cpu_baseline"] = {
+            "value": v, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "sample": f"fp64 oracle: routing of all {cfg.T} tokens ({tr:.2f} s) + experts and "
+                      f"combine of {n} seeded tokens ({tf:.2f} s), extrapolated to {cfg.T} tokens"}
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", default=DEFAULT_CONFIG, choices=sorted(K.BY_NAME))
+    ap.add_argument("--capacity-factor", type=float, default=None)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--cpu-tokens", type=int, default=8)
+    ap.add_argument("--ref-tokens", type=int, default=2)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)     # fewer warm-up steps give no valid number
+    cfg = K.BY_NAME[args.config]
+    cf = args.capacity_factor
+    if cf is None and cfg.capacity_factors:
+        cf = cfg.capacity_factors[0]
+    if args.impl == "reference":
+        run_reference(args, cfg, cf)
+    else:
+        run_gpu(args, cfg, cf)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,226 @@
+/*
+ * moe.h - C ABI of libmoe.so: the forward of one sparse top-k routed Mixture-of-Experts
+ * layer on one NVIDIA B300 (sm_103a).
+ *
+ * The five compute calls follow the six-step forward of "LLM Internals §14.2.1 (one MoE
+ * forward: six steps and shapes)":
+ *   step 1  input X[T, H]                                   (caller's buffer)
+ *   step 2  router scoring X x W_g -> s[T, E]                moe_router_topk
+ *   step 3  top-k per row and normalisation among the k     moe_router_topk
+ *   step 4  dispatch permutation grouping rows by expert     moe_dispatch
+ *   step 5  grouped GEMM per expert over variable m_i        moe_grouped_swiglu
+ *   step 6  gate-weighted combine through the inverse
+ *           permutation, plus the shared expert              moe_combine
+ * and the monitoring signals of §14.2.3 (balance loss, per-expert load, drop rate,
+ * routing entropy) with the load CV of "AI Knowledge Map - MoE": moe_balance_stats.
+ *
+ * Conventions for every call
+ *  - Pointers are DEVICE pointers unless stated.  The caller owns every buffer.  The
+ *    library allocates no device memory: scratch lives in a caller-provided workspace
+ *    of moe_workspace_bytes() bytes whose first 256 bytes hold a device status word and
+ *    must be zeroed once (moe_workspace_init) before first use.
+ *  - Every call is asynchronous on `stream`, performs no host synchronisation (except
+ *    moe_get_device_status and moe_ctx_trace_read, which say so) and returns an int
+ *    status: MOE_OK (0) or a negative MOE_ERR_*.  Argument checks run before anything is
+ *    enqueued; a failed check enqueues nothing.  No C++ exception crosses the ABI.
+ *  - Device-side failures (a bounded wait that timed out, an index out of range) are
+ *    recorded in the workspace status word (first error wins) and read back with
+ *    moe_get_device_status.  Kernels never trap.
+ *  - Layouts are row-major.  Expert weights are stored output-major (the transpose of
+ *    the [H, I] orientation in which §14.2.1 writes the product) so that both operands
+ *    of every expert GEMM are contiguous along their reduction axis:
+ *      W_gate, W_up : [E][I][H]     W_down : [E][H][I]
+ *      Ws_gate, Ws_up : [I][H]      Ws_down : [H][I]      (shared expert)
+ *  - Supported: 1 <= k <= min(E, 32), 1 <= E <= 512, T >= 0.  bf16 experts need
+ *    H % 64 == 0 and I % 64 == 0; fp32 experts need H % 4 == 0 and I % 4 == 0.
+ *    All pointers 16-byte aligned.
+ */
+#ifndef MOE_H_
+#define MOE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* cudaStream_t without pulling in the CUDA headers. */
+typedef struct CUstream_st* moe_stream_t;
+
+enum moe_status {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = -1, /* null pointer, bad size, misaligned pointer, small ws   */
+  MOE_ERR_UNSUPPORTED = -2, /* valid request outside what the kernels implement      */
+  MOE_ERR_CUDA = -3,        /* a CUDA runtime/driver call failed                      */
+  MOE_ERR_TIMEOUT = -4,     /* device: a bounded wait gave up                         */
+  MOE_ERR_DEVICE_INDEX = -5 /* device: an index read from memory was out of range     */
+};
+
+enum moe_score { MOE_SCORE_SOFTMAX = 0, MOE_SCORE_SIGMOID = 1 };
+enum moe_dtype { MOE_DTYPE_BF16 = 0, MOE_DTYPE_F32 = 1 };
+
+typedef struct moe_ctx moe_ctx;
+
+/* Shape and policy of the router (steps 2-3). */
+typedef struct {
+  int T, H, E, k;
+  int score;   /* MOE_SCORE_SOFTMAX: key = logit, gate from softmax(l) ("AI Knowledge
+                  Map - MoE", router steps 1-4).  MOE_SCORE_SIGMOID: s = sigmoid(l) per
+                  cell (§14.2.1 step 2), key = s + bias (§14.2.3 eq. 16). */
+  int renorm;  /* 1: gates renormalised over the k chosen (sum to 1); 0: raw softmax
+                  probability / raw affinity. */
+  int x_dtype; /* dtype of X: MOE_DTYPE_BF16 or MOE_DTYPE_F32 */
+} moe_router_desc;
+
+/* Shape of the expert stage (step 5). */
+typedef struct {
+  int T, H, E, I, k;
+  int dtype;      /* dtype of X / Xperm and all expert weights */
+  int has_shared; /* 1: one always-on shared expert of width I (§14.2.4) */
+} moe_expert_desc;
+
+/* ------------------------------------------------------------------ context */
+
+/* Create a context bound to CUDA device `device` (reads its SM count, resolves the
+ * tensor-map encoder of the driver).  *out is owned by the caller; free it with
+ * moe_ctx_destroy.  Returns MOE_ERR_CUDA if the device cannot be queried. */
+int moe_ctx_create(moe_ctx** out, int device);
+void moe_ctx_destroy(moe_ctx* ctx);
+
+/* Bytes of workspace the calls of one forward of this shape need (all five calls share
+ * one workspace).  Host-only; never fails (returns 0 for negative sizes). */
+size_t moe_workspace_bytes(int T, int H, int E, int I, int k, int dtype, int has_shared);
+
+/* Zero the workspace header (status word) on `stream`. */
+int moe_workspace_init(void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* Expert capacity C = ceil(c * T * k / E) ("AI Knowledge Map - MoE", capacity formula;
+ * the GShard form of §14.2.3), evaluated exactly on the binary value of c.  Host-only.
+ * Returns C >= 0, or MOE_ERR_INVALID_ARG for c < 0, non-finite c, T < 0, k < 1, E < 1 or
+ * a result above INT32_MAX. */
+int moe_capacity(double c, int T, int k, int E);
+
+/* ------------------------------------------------------------------ steps 2-3 */
+
+/* Router scoring, top-k and gates for all T tokens.
+ *   X          [T, H] bf16 or fp32 (d->x_dtype)
+ *   Wg         [H, E] fp32 router weight
+ *   bias       [E] fp32 selection-only bias (sigmoid scoring; nullable = 0)
+ *   logit_bias [E] fp32 offset added to every logit before scoring (nullable = 0)
+ *   topk_idx   [T, k] int32 out: the k chosen experts of each token, ascending index
+ *   topk_gate  [T, k] fp32 out: their gate weights, same order
+ *   key_gap    [T] fp32 out (nullable): key_(k) - key_(k+1) of the row (+inf if k == E)
+ *   prob_colsum[E] fp64 out (nullable): sum over tokens of p[t, e] (softmax row, or the
+ *              sigmoid affinities normalised over the row); zeroed by the call
+ * Selection is exact: logits are computed in fp32 with compensated accumulation, and
+ * any row whose k-th/(k+1)-th margin falls inside the fp32 error bound is re-decided
+ * from float64 dot products.  Ties go to the lower expert index. */
+int moe_router_topk(moe_ctx* ctx, const moe_router_desc* d, const void* X,
+                    const float* Wg, const float* bias, const float* logit_bias,
+                    int32_t* topk_idx, float* topk_gate, float* key_gap,
+                    double* prob_colsum, void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* ------------------------------------------------------------------ step 4 */
+
+/* Group the T*k (token, choice) slots by expert (§14.2.1 step 4) under an optional
+ * capacity ("AI Knowledge Map - MoE": overflow beyond C is dropped; the lowest token
+ * indices of an expert are kept).
+ *   capacity   < 0: dropless; >= 0: C (see moe_capacity)
+ *   topk_idx   [T, k] int32 from moe_router_topk
+ *   counts     [E] int32 out: m_e, slots routed to e BEFORE capacity
+ *   offsets    [E+1] int32 out: first permuted row of each expert AFTER capacity;
+ *              offsets[E] = R, the kept slot count
+ *   row_of_slot[T*k] int32 out: permuted row of slot t*k+j, or -1 if dropped
+ *   slot_of_row[T*k] int32 out: rows [0, R) hold the inverse; rows >= R untouched
+ *   X, Xperm   nullable pair: when both are given, Xperm[row] = X[slot / k] for every
+ *              kept row (x_dtype element type, Xperm has T*k rows)
+ * Rows are ordered by (expert ascending, token ascending). */
+int moe_dispatch(moe_ctx* ctx, int T, int k, int E, int H, int x_dtype, int capacity,
+                 const int32_t* topk_idx, const void* X, int32_t* counts,
+                 int32_t* offsets, int32_t* row_of_slot, int32_t* slot_of_row,
+                 void* Xperm, void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* ------------------------------------------------------------------ step 5 */
+
+/* Per-expert SwiGLU FFN over the permuted rows (§14.2.1 step 5, §14.2.2 three
+ * matrices): for the rows [offsets[e], offsets[e+1]) of expert e,
+ *   h = SiLU(x W_gate[e]^T) * (x W_up[e]^T),   o = h W_down[e]^T,
+ * and for the shared expert (has_shared) the same over all T rows of X.
+ *   X        [T, H]   (read only for the shared expert; nullable when has_shared = 0)
+ *   Xperm    [T*k, H] permuted rows from moe_dispatch
+ *   offsets  [E+1]    from moe_dispatch (read on the device; no host sync)
+ *   O        [T*k, H] fp32 out: o of each kept row; rows >= R untouched
+ *   O_shared [T, H]   fp32 out (has_shared): the shared expert's output
+ * bf16: tcgen05 tensor cores, fp32 accumulation, h rounded to bf16.  fp32: CUDA-core
+ * fp32 FMA throughout. */
+int moe_grouped_swiglu(moe_ctx* ctx, const moe_expert_desc* d, const void* X,
+                       const void* Xperm, const int32_t* offsets, const void* W_gate,
+                       const void* W_up, const void* W_down, const void* Ws_gate,
+                       const void* Ws_up, const void* Ws_down, float* O, float* O_shared,
+                       void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* ------------------------------------------------------------------ step 6 */
+
+/* Y[t] = sum over kept j of topk_gate[t, j] * O[row_of_slot[t*k+j]]  (+ O_shared[t])
+ * (§14.2.1 step 6; "AI Knowledge Map - MoE" final weighted sum).  A dropped slot adds
+ * nothing and the remaining gates are not renormalised.
+ *   O_shared nullable; Y [T, H] fp32 out; Y_bf16 [T, H] nullable bf16 copy of Y. */
+int moe_combine(moe_ctx* ctx, int T, int k, int H, const float* O, const float* O_shared,
+                const int32_t* row_of_slot, const float* topk_gate, float* Y,
+                void* Y_bf16, moe_stream_t stream);
+
+/* ------------------------------------------------------------------ balance signals */
+
+/* Load-balance statistics of one routed batch (§14.2.3 balance loss and monitoring;
+ * "AI Knowledge Map - MoE" load CV):
+ *   f[e] = counts[e] / (T k)   (router choices before capacity; sums to 1)
+ *   p[e] = prob_colsum[e] / T
+ *   out[0] = alpha * E * sum_e f[e] p[e]        (Switch balance loss)
+ *   out[1] = (T k - offsets[E]) / (T k)        (drop rate; 0 when offsets is null)
+ *   out[2] = std(counts) / mean(counts)         (population std; load CV)
+ *   out[3] = -sum_e f[e] ln f[e]                (routing entropy)
+ * f, p: [E] fp64 out; out: [4] fp64 out.  With T == 0 everything is 0. */
+int moe_balance_stats(moe_ctx* ctx, int T, int k, int E, const int32_t* counts,
+                      const int32_t* offsets, const double* prob_colsum, double alpha,
+                      double* f, double* p, double* out, moe_stream_t stream);
+
+/* ------------------------------------------------------------------ diagnostics */
+
+/* Synchronise `stream`, copy the workspace status word into *status (host pointer) and,
+ * if reset != 0, zero it.  Returns MOE_ERR_CUDA if the copy fails. */
+int moe_get_device_status(moe_ctx* ctx, void* ws, int* status, int reset,
+                          moe_stream_t stream);
+
+/* Kernel timing.  With tracing on, every kernel a call launches is bracketed by CUDA
+ * events recorded on that call's stream.  moe_ctx_trace_read synchronises those events
+ * and writes, per kernel id, the number of launches and their summed milliseconds
+ * (host arrays of n entries, n >= MOE_KERNEL_COUNT), then clears the record. */
+enum moe_kernel_id {
+  MOE_K_ROUTER_LOGITS = 0,
+  MOE_K_ROUTER_SELECT,
+  MOE_K_DISPATCH_COUNT,
+  MOE_K_DISPATCH_SCAN,
+  MOE_K_DISPATCH_SCATTER,
+  MOE_K_DISPATCH_GATHER,
+  MOE_K_EXPERT_GATE_UP,
+  MOE_K_EXPERT_DOWN,
+  MOE_K_COMBINE,
+  MOE_K_BALANCE_STATS,
+  MOE_KERNEL_COUNT
+};
+int moe_ctx_set_tracing(moe_ctx* ctx, int enable);
+int moe_ctx_trace_read(moe_ctx* ctx, int* launches, double* total_ms, int n);
+const char* moe_kernel_name(int id);
+
+const char* moe_status_string(int status);
+/* Text describing why the last call made by this thread failed ("" after a success).
+ * Host-only; the pointer stays valid until this thread's next call. */
+const char* moe_last_error_detail(void);
+int moe_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_H_ */

@@ -1,0 +1,464 @@
+// The C ABI of libmoe.so (declared in include/moe.h): argument checks, workspace
+// carving, kernel launches on the caller's stream, optional per-kernel event timing.
+// Nothing here allocates device memory and nothing here synchronises, except
+// moe_get_device_status and moe_ctx_trace_read, which are documented to.
+#include <math.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "moe_internal.h"
+
+using namespace moe;
+
+struct moe_ctx {
+  int device = 0;
+  int num_sms = 0;
+  EncodeTiledFn encode = nullptr;
+  bool tracing = false;
+  struct Rec {
+    int id;
+    cudaEvent_t a, b;
+  };
+  std::vector<Rec> recs;
+  std::vector<cudaEvent_t> pool;
+  std::mutex mu;
+};
+
+namespace {
+
+thread_local std::string g_detail;
+
+int fail(int code, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
+int fail(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_detail = buf;
+  return code;
+}
+
+int ok() {
+  g_detail.clear();
+  return MOE_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+cudaEvent_t take_event(moe_ctx* c) {
+  if (!c->pool.empty()) {
+    cudaEvent_t e = c->pool.back();
+    c->pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+  return e;
+}
+
+// Launches `fn` with optional event bracketing on `s`.
+template <typename F>
+cudaError_t traced(moe_ctx* c, int id, cudaStream_t s, F&& fn) {
+  if (!c->tracing) return fn();
+  std::lock_guard<std::mutex> lk(c->mu);
+  cudaEvent_t a = take_event(c), b = take_event(c);
+  if (a) cudaEventRecord(a, s);
+  cudaError_t e = fn();
+  if (b) cudaEventRecord(b, s);
+  if (a && b) c->recs.push_back({id, a, b});
+  return e;
+}
+
+int check_ctx(moe_ctx* c) {
+  if (!c) return fail(MOE_ERR_INVALID_ARG, "ctx is null");
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess)
+    return fail(MOE_ERR_CUDA, "cudaGetDevice failed");
+  if (dev != c->device)
+    return fail(MOE_ERR_INVALID_ARG, "current device %d is not the context's device %d", dev,
+                c->device);
+  return MOE_OK;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+  return fail(MOE_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+int check_shape(int T, int E, int k) {
+  if (T < 0) return fail(MOE_ERR_INVALID_ARG, "T = %d < 0", T);
+  if (E < 1 || E > kMaxE) return fail(MOE_ERR_UNSUPPORTED, "E = %d outside [1, %d]", E, kMaxE);
+  if (k < 1 || k > E || k > kMaxK)
+    return fail(MOE_ERR_UNSUPPORTED, "k = %d outside [1, min(E, %d)]", k, kMaxK);
+  if ((long long)T * k > 0x7fffffffLL) return fail(MOE_ERR_UNSUPPORTED, "T*k exceeds int32");
+  return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int moe_version(void) { return 10000; }
+
+const char* moe_status_string(int s) {
+  switch (s) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported configuration";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_TIMEOUT: return "device wait timed out";
+    case MOE_ERR_DEVICE_INDEX: return "device index out of range";
+    default: return "unknown status";
+  }
+}
+
+// Text describing the last failure of a call made by this thread ("" after success).
+const char* moe_last_error_detail(void) { return g_detail.c_str(); }
+
+const char* moe_kernel_name(int id) {
+  static const char* names[MOE_KERNEL_COUNT] = {
+      "router_logits",    "router_select",    "dispatch_count", "dispatch_scan",
+      "dispatch_scatter", "dispatch_gather",  "expert_gate_up", "expert_down",
+      "combine",          "balance_stats"};
+  return (id >= 0 && id < MOE_KERNEL_COUNT) ? names[id] : "unknown";
+}
+
+int moe_ctx_create(moe_ctx** out, int device) {
+  if (!out) return fail(MOE_ERR_INVALID_ARG, "out is null");
+  *out = nullptr;
+  int n = 0;
+  cudaError_t e = cudaGetDeviceCount(&n);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDeviceCount");
+  if (device < 0 || device >= n)
+    return fail(MOE_ERR_INVALID_ARG, "device %d outside [0, %d)", device, n);
+  int sms = 0, major = 0, minor = 0;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device)) != cudaSuccess)
+    return cuda_fail(e, "cudaDeviceGetAttribute");
+  cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, device);
+  cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, device);
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                       &q);
+  if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn)
+    return fail(MOE_ERR_CUDA, "cannot resolve cuTensorMapEncodeTiled");
+  moe_ctx* c = new moe_ctx();
+  c->device = device;
+  c->num_sms = sms;
+  c->encode = reinterpret_cast<EncodeTiledFn>(fn);
+  *out = c;
+  (void)major;
+  (void)minor;
+  return ok();
+}
+
+void moe_ctx_destroy(moe_ctx* c) {
+  if (!c) return;
+  for (auto& r : c->recs) {
+    cudaEventDestroy(r.a);
+    cudaEventDestroy(r.b);
+  }
+  for (auto e : c->pool) cudaEventDestroy(e);
+  delete c;
+}
+
+size_t moe_workspace_bytes(int T, int H, int E, int I, int k, int dtype, int has_shared) {
+  if (T < 0 || H < 0 || E < 0 || I < 0 || k < 0) return 0;
+  return ws_layout(T, H, E, I, k, dtype, has_shared).total;
+}
+
+int moe_workspace_init(void* ws, size_t ws_bytes, moe_stream_t stream) {
+  if (!ws || ws_bytes < kWsHeader) return fail(MOE_ERR_INVALID_ARG, "workspace too small");
+  cudaError_t e = cudaMemsetAsync(ws, 0, kWsHeader, (cudaStream_t)stream);
+  return e == cudaSuccess ? ok() : cuda_fail(e, "cudaMemsetAsync");
+}
+
+int moe_capacity(double c, int T, int k, int E) {
+  if (!isfinite(c) || c < 0.0) return fail(MOE_ERR_INVALID_ARG, "capacity factor %g", c);
+  if (T < 0 || k < 1 || E < 1) return fail(MOE_ERR_INVALID_ARG, "bad T/k/E");
+  if (c == 0.0 || T == 0) return 0;
+  // c = mant * 2^ex exactly
+  int e2 = 0;
+  const double f = frexp(c, &e2);                      // c = f * 2^e2, f in [0.5, 1)
+  const unsigned long long mant = (unsigned long long)ldexp(f, 53);
+  const int ex = e2 - 53;
+  typedef unsigned __int128 u128;
+  u128 num = (u128)mant * (u128)(unsigned)T * (u128)(unsigned)k;
+  u128 q;
+  if (ex >= 0) {
+    if (ex > 30) return fail(MOE_ERR_INVALID_ARG, "capacity overflows");
+    q = num << ex;
+  } else {
+    const int s = -ex;
+    q = (s >= 127) ? (num > 0 ? 1 : 0) : ((num + (((u128)1 << s) - 1)) >> s);   // ceil
+  }
+  const u128 C = (q + (u128)(unsigned)E - 1) / (u128)(unsigned)E;           // ceil
+  if (C > (u128)0x7fffffff) return fail(MOE_ERR_INVALID_ARG, "capacity overflows int32");
+  g_detail.clear();
+  return (int)C;
+}
+
+int moe_router_topk(moe_ctx* ctx, const moe_router_desc* d, const void* X, const float* Wg,
+                    const float* bias, const float* logit_bias, int32_t* topk_idx,
+                    float* topk_gate, float* key_gap, double* prob_colsum, void* ws,
+                    size_t ws_bytes, moe_stream_t stream) {
+  if (!d) return fail(MOE_ERR_INVALID_ARG, "desc is null");
+  int r = check_shape(d->T, d->E, d->k);
+  if (r) return r;
+  if (d->H < 1) return fail(MOE_ERR_INVALID_ARG, "H = %d", d->H);
+  if (d->score != MOE_SCORE_SOFTMAX && d->score != MOE_SCORE_SIGMOID)
+    return fail(MOE_ERR_INVALID_ARG, "score = %d", d->score);
+  if (d->x_dtype != MOE_DTYPE_BF16 && d->x_dtype != MOE_DTYPE_F32)
+    return fail(MOE_ERR_INVALID_ARG, "x_dtype = %d", d->x_dtype);
+  if (d->T > 0 && (!X || !Wg || !topk_idx || !topk_gate))
+    return fail(MOE_ERR_INVALID_ARG, "X, Wg, topk_idx and topk_gate are required");
+  if (!ws) return fail(MOE_ERR_INVALID_ARG, "workspace is null");
+  if (!aligned16(X) || !aligned16(Wg) || !aligned16(ws))
+    return fail(MOE_ERR_INVALID_ARG, "X, Wg and ws must be 16-byte aligned");
+  const WsLayout L = ws_layout(d->T, d->H, d->E, 0, d->k, d->x_dtype, 0);
+  if (ws_bytes < L.chunk_counts) return fail(MOE_ERR_INVALID_ARG, "workspace too small");
+  if ((r = check_ctx(ctx))) return r;
+  cudaStream_t s = (cudaStream_t)stream;
+  cudaError_t e;
+  if (prob_colsum && (e = cudaMemsetAsync(prob_colsum, 0, sizeof(double) * d->E, s)))
+    return cuda_fail(e, "cudaMemsetAsync");
+  if (d->T == 0) return ok();
+  RouterArgs a;
+  a.T = d->T;
+  a.H = d->H;
+  a.E = d->E;
+  a.k = d->k;
+  a.score = d->score;
+  a.renorm = d->renorm;
+  a.x_dtype = d->x_dtype;
+  a.X = X;
+  a.Wg = Wg;
+  a.bias = bias;
+  a.logit_bias = logit_bias;
+  a.logits = reinterpret_cast<float*>(static_cast<char*>(ws) + L.logits);
+  a.idx = topk_idx;
+  a.gate = topk_gate;
+  a.gap = key_gap;
+  a.colsum = prob_colsum;
+  a.status = static_cast<int*>(ws);
+  if ((e = traced(ctx, MOE_K_ROUTER_LOGITS, s, [&] { return launch_router_logits(a, s); })))
+    return cuda_fail(e, "router_logits launch");
+  if ((e = traced(ctx, MOE_K_ROUTER_SELECT, s, [&] { return launch_router_select(a, s); })))
+    return cuda_fail(e, "router_select launch");
+  return ok();
+}
+
+int moe_dispatch(moe_ctx* ctx, int T, int k, int E, int H, int x_dtype, int capacity,
+                 const int32_t* topk_idx, const void* X, int32_t* counts, int32_t* offsets,
+                 int32_t* row_of_slot, int32_t* slot_of_row, void* Xperm, void* ws,
+                 size_t ws_bytes, moe_stream_t stream) {
+  int r = check_shape(T, E, k);
+  if (r) return r;
+  if (!counts || !offsets || !ws) return fail(MOE_ERR_INVALID_ARG, "counts/offsets/ws null");
+  if (T > 0 && (!topk_idx || !row_of_slot || !slot_of_row))
+    return fail(MOE_ERR_INVALID_ARG, "topk_idx/row_of_slot/slot_of_row null");
+  if ((X == nullptr) != (Xperm == nullptr))
+    return fail(MOE_ERR_INVALID_ARG, "X and Xperm must be given together");
+  if (Xperm) {
+    if (x_dtype != MOE_DTYPE_BF16 && x_dtype != MOE_DTYPE_F32)
+      return fail(MOE_ERR_INVALID_ARG, "x_dtype = %d", x_dtype);
+    if (H < 1 || (H * (x_dtype == MOE_DTYPE_BF16 ? 2 : 4)) % 16 != 0)
+      return fail(MOE_ERR_UNSUPPORTED, "row of H = %d elements is not a multiple of 16 B", H);
+    if (!aligned16(X) || !aligned16(Xperm))
+      return fail(MOE_ERR_INVALID_ARG, "X and Xperm must be 16-byte aligned");
+  }
+  if (!aligned16(ws)) return fail(MOE_ERR_INVALID_ARG, "ws must be 16-byte aligned");
+  const WsLayout L = ws_layout(T, H, E, 0, k, MOE_DTYPE_BF16, 0);
+  if (ws_bytes < L.h) return fail(MOE_ERR_INVALID_ARG, "workspace too small");
+  if ((r = check_ctx(ctx))) return r;
+  cudaStream_t s = (cudaStream_t)stream;
+  cudaError_t e;
+  if (T == 0) {
+    if ((e = cudaMemsetAsync(counts, 0, sizeof(int32_t) * E, s)) ||
+        (e = cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (E + 1), s)))
+      return cuda_fail(e, "cudaMemsetAsync");
+    return ok();
+  }
+  DispatchArgs a;
+  a.T = T;
+  a.k = k;
+  a.E = E;
+  a.H = H;
+  a.x_dtype = x_dtype;
+  a.capacity = capacity < 0 ? -1 : capacity;
+  a.idx = topk_idx;
+  a.X = X;
+  a.counts = counts;
+  a.offsets = offsets;
+  a.row_of_slot = row_of_slot;
+  a.slot_of_row = slot_of_row;
+  a.Xperm = Xperm;
+  a.chunk_counts = reinterpret_cast<int32_t*>(static_cast<char*>(ws) + L.chunk_counts);
+  a.chunk_base = reinterpret_cast<int32_t*>(static_cast<char*>(ws) + L.chunk_base);
+  a.status = static_cast<int*>(ws);
+  if ((e = traced(ctx, MOE_K_DISPATCH_COUNT, s, [&] { return launch_dispatch_count(a, s); })))
+    return cuda_fail(e, "dispatch_count launch");
+  if ((e = traced(ctx, MOE_K_DISPATCH_SCAN, s, [&] { return launch_dispatch_scan(a, s); })))
+    return cuda_fail(e, "dispatch_scan launch");
+  if ((e = traced(ctx, MOE_K_DISPATCH_SCATTER, s,
+                  [&] { return launch_dispatch_scatter(a, s); })))
+    return cuda_fail(e, "dispatch_scatter launch");
+  if (Xperm &&
+      (e = traced(ctx, MOE_K_DISPATCH_GATHER, s, [&] { return launch_dispatch_gather(a, s); })))
+    return cuda_fail(e, "dispatch_gather launch");
+  return ok();
+}
+
+int moe_grouped_swiglu(moe_ctx* ctx, const moe_expert_desc* d, const void* X,
+                       const void* Xperm, const int32_t* offsets, const void* W_gate,
+                       const void* W_up, const void* W_down, const void* Ws_gate,
+                       const void* Ws_up, const void* Ws_down, float* O, float* O_shared,
+                       void* ws, size_t ws_bytes, moe_stream_t stream) {
+  if (!d) return fail(MOE_ERR_INVALID_ARG, "desc is null");
+  int r = check_shape(d->T, d->E, d->k);
+  if (r) return r;
+  if (d->H < 1 || d->I < 1) return fail(MOE_ERR_INVALID_ARG, "H = %d, I = %d", d->H, d->I);
+  if (d->dtype == MOE_DTYPE_BF16) {
+    if (d->H % 64 || d->I % 64)
+      return fail(MOE_ERR_UNSUPPORTED, "bf16 experts need H %% 64 == 0 and I %% 64 == 0");
+  } else if (d->dtype == MOE_DTYPE_F32) {
+    if (d->H % 4 || d->I % 4)
+      return fail(MOE_ERR_UNSUPPORTED, "fp32 experts need H %% 4 == 0 and I %% 4 == 0");
+  } else {
+    return fail(MOE_ERR_INVALID_ARG, "dtype = %d", d->dtype);
+  }
+  if (!offsets || !W_gate || !W_up || !W_down || !O || !Xperm || !ws)
+    return fail(MOE_ERR_INVALID_ARG, "offsets, weights, Xperm, O and ws are required");
+  if (d->has_shared && (!X || !Ws_gate || !Ws_up || !Ws_down || !O_shared))
+    return fail(MOE_ERR_INVALID_ARG, "the shared expert needs X, Ws_* and O_shared");
+  const void* ptrs[] = {X, Xperm, W_gate, W_up, W_down, Ws_gate, Ws_up, Ws_down, O, O_shared, ws};
+  for (const void* q : ptrs)
+    if (!aligned16(q)) return fail(MOE_ERR_INVALID_ARG, "pointers must be 16-byte aligned");
+  const WsLayout L = ws_layout(d->T, d->H, d->E, d->I, d->k, d->dtype, d->has_shared);
+  if (ws_bytes < L.total) return fail(MOE_ERR_INVALID_ARG, "workspace too small");
+  if ((r = check_ctx(ctx))) return r;
+  if (d->T == 0) return ok();
+  cudaStream_t s = (cudaStream_t)stream;
+  ExpertArgs a;
+  a.T = d->T;
+  a.H = d->H;
+  a.E = d->E;
+  a.I = d->I;
+  a.k = d->k;
+  a.has_shared = d->has_shared ? 1 : 0;
+  a.num_sms = ctx->num_sms;
+  a.X = X;
+  a.Xperm = Xperm;
+  a.offsets = offsets;
+  a.W_gate = W_gate;
+  a.W_up = W_up;
+  a.W_down = W_down;
+  a.Ws_gate = Ws_gate;
+  a.Ws_up = Ws_up;
+  a.Ws_down = Ws_down;
+  a.h = static_cast<char*>(ws) + L.h;
+  a.O = O;
+  a.O_shared = O_shared;
+  a.status = static_cast<int*>(ws);
+  cudaError_t e;
+  if (d->dtype == MOE_DTYPE_BF16) {
+    bool bad = false;
+    e = traced(ctx, MOE_K_EXPERT_GATE_UP, s,
+               [&] { return launch_expert_gate_up_tc(a, ctx->encode, &bad, s); });
+    if (bad) return fail(MOE_ERR_INVALID_ARG, "tensor map encoding failed (gate/up)");
+    if (e) return cuda_fail(e, "expert_gate_up launch");
+    e = traced(ctx, MOE_K_EXPERT_DOWN, s,
+               [&] { return launch_expert_down_tc(a, ctx->encode, &bad, s); });
+    if (bad) return fail(MOE_ERR_INVALID_ARG, "tensor map encoding failed (down)");
+    if (e) return cuda_fail(e, "expert_down launch");
+  } else {
+    if ((e = traced(ctx, MOE_K_EXPERT_GATE_UP, s,
+                    [&] { return launch_expert_gate_up_f32(a, s); })))
+      return cuda_fail(e, "expert_gate_up launch");
+    if ((e = traced(ctx, MOE_K_EXPERT_DOWN, s, [&] { return launch_expert_down_f32(a, s); })))
+      return cuda_fail(e, "expert_down launch");
+  }
+  return ok();
+}
+
+int moe_combine(moe_ctx* ctx, int T, int k, int H, const float* O, const float* O_shared,
+                const int32_t* row_of_slot, const float* topk_gate, float* Y, void* Y_bf16,
+                moe_stream_t stream) {
+  if (T < 0 || k < 1 || k > kMaxK) return fail(MOE_ERR_INVALID_ARG, "T = %d, k = %d", T, k);
+  if (H < 4 || H % 4) return fail(MOE_ERR_UNSUPPORTED, "combine needs H %% 4 == 0");
+  if (T > 0 && (!O || !row_of_slot || !topk_gate || !Y))
+    return fail(MOE_ERR_INVALID_ARG, "O, row_of_slot, topk_gate and Y are required");
+  if (!aligned16(O) || !aligned16(O_shared) || !aligned16(Y) || !aligned16(Y_bf16))
+    return fail(MOE_ERR_INVALID_ARG, "O, O_shared, Y, Y_bf16 must be 16-byte aligned");
+  int r = check_ctx(ctx);
+  if (r) return r;
+  if (T == 0) return ok();
+  cudaStream_t s = (cudaStream_t)stream;
+  CombineArgs a{T, k, H, O, O_shared, row_of_slot, topk_gate, Y, Y_bf16};
+  cudaError_t e = traced(ctx, MOE_K_COMBINE, s, [&] { return launch_combine(a, s); });
+  return e ? cuda_fail(e, "combine launch") : ok();
+}
+
+int moe_balance_stats(moe_ctx* ctx, int T, int k, int E, const int32_t* counts,
+                      const int32_t* offsets, const double* prob_colsum, double alpha,
+                      double* f, double* p, double* out, moe_stream_t stream) {
+  int r = check_shape(T, E, k);
+  if (r) return r;
+  if (!counts || !prob_colsum || !f || !p || !out)
+    return fail(MOE_ERR_INVALID_ARG, "counts, prob_colsum, f, p and out are required");
+  if ((r = check_ctx(ctx))) return r;
+  cudaStream_t s = (cudaStream_t)stream;
+  StatsArgs a{T, k, E, counts, offsets, prob_colsum, alpha, f, p, out};
+  cudaError_t e = traced(ctx, MOE_K_BALANCE_STATS, s, [&] { return launch_balance_stats(a, s); });
+  return e ? cuda_fail(e, "balance_stats launch") : ok();
+}
+
+int moe_get_device_status(moe_ctx* ctx, void* ws, int* status, int reset,
+                          moe_stream_t stream) {
+  if (!ws || !status) return fail(MOE_ERR_INVALID_ARG, "ws and status are required");
+  int r = check_ctx(ctx);
+  if (r) return r;
+  cudaStream_t s = (cudaStream_t)stream;
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e) return cuda_fail(e, "cudaStreamSynchronize");
+  if ((e = cudaMemcpy(status, ws, sizeof(int), cudaMemcpyDeviceToHost)))
+    return cuda_fail(e, "cudaMemcpy");
+  if (reset && (e = cudaMemset(ws, 0, sizeof(int)))) return cuda_fail(e, "cudaMemset");
+  return ok();
+}
+
+int moe_ctx_set_tracing(moe_ctx* ctx, int enable) {
+  if (!ctx) return fail(MOE_ERR_INVALID_ARG, "ctx is null");
+  ctx->tracing = enable != 0;
+  return ok();
+}
+
+int moe_ctx_trace_read(moe_ctx* ctx, int* launches, double* total_ms, int n) {
+  if (!ctx || !launches || !total_ms || n < MOE_KERNEL_COUNT)
+    return fail(MOE_ERR_INVALID_ARG, "bad trace buffers");
+  std::lock_guard<std::mutex> lk(ctx->mu);
+  for (int i = 0; i < n; ++i) {
+    launches[i] = 0;
+    total_ms[i] = 0.0;
+  }
+  int rc = MOE_OK;
+  for (auto& rec : ctx->recs) {
+    float ms = 0.f;
+    cudaError_t e = cudaEventSynchronize(rec.b);
+    if (e == cudaSuccess) e = cudaEventElapsedTime(&ms, rec.a, rec.b);
+    if (e != cudaSuccess) rc = cuda_fail(e, "cudaEventElapsedTime");
+    launches[rec.id] += 1;
+    total_ms[rec.id] += ms;
+    ctx->pool.push_back(rec.a);
+    ctx->pool.push_back(rec.b);
+  }
+  ctx->recs.clear();
+  return rc ? rc : ok();
+}
+
+}  // extern "C"

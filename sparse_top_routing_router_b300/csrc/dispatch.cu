@@ -1,0 +1,165 @@
+// Step 4 of the MoE forward: the dispatch permutation ("LLM Internals §14.2.1 step 4":
+// rows re-ordered by expert so that each expert's tokens are contiguous), with the
+// optional capacity of "AI Knowledge Map - MoE" (C = ceil(c*N*k/E), overflow dropped,
+// the lowest token indices kept).
+//
+// A stable counting sort of the T*k slots by expert, in four launches:
+//  count    per 256-token chunk, per-expert slot counts (shared-memory histogram)
+//  scan     per expert, exclusive scan over chunks; m_e; capacity clamp; offsets
+//  scatter  per chunk, each slot's rank inside its expert = chunk base + the number of
+//           earlier tokens of the chunk routed to the same expert (bitmap popcount);
+//           row_of_slot / slot_of_row, or -1 beyond capacity
+//  gather   one warp per token: its X row copied once to each of its kept rows, with
+//           16-byte vector moves
+#include "moe_internal.h"
+#include "ptx.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kChunk = kDispatchChunk;   // 256 tokens, one per thread
+
+__global__ void __launch_bounds__(kChunk) dispatch_count_kernel(DispatchArgs a) {
+  __shared__ int hist[kMaxE];
+  const int c = blockIdx.x;
+  for (int e = threadIdx.x; e < a.E; e += blockDim.x) hist[e] = 0;
+  __syncthreads();
+  const int t = c * kChunk + threadIdx.x;
+  if (t < a.T) {
+    for (int j = 0; j < a.k; ++j) {
+      const int e = a.idx[(size_t)t * a.k + j];
+      if (e >= 0 && e < a.E) atomicAdd(&hist[e], 1);
+      else set_status(a.status, MOE_ERR_DEVICE_INDEX);
+    }
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < a.E; e += blockDim.x)
+    a.chunk_counts[(size_t)c * a.E + e] = hist[e];
+}
+
+// One CTA of 512 threads: thread e walks the chunks of expert e.
+__global__ void __launch_bounds__(kMaxE) dispatch_scan_kernel(DispatchArgs a, int nchunks) {
+  __shared__ int s_warp[kMaxE / 32];
+  const int e = threadIdx.x;
+  int run = 0;
+  if (e < a.E) {
+    for (int c = 0; c < nchunks; ++c) {
+      const size_t i = (size_t)c * a.E + e;
+      a.chunk_base[i] = run;
+      run += a.chunk_counts[i];
+    }
+    a.counts[e] = run;
+  }
+  const int kept = (e < a.E) ? (a.capacity >= 0 ? min(run, a.capacity) : run) : 0;
+  // block exclusive scan of kept over experts
+  const int lane = e & 31, w = e >> 5;
+  int v = kept;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int n = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += n;
+  }
+  if (lane == 31) s_warp[w] = v;
+  __syncthreads();
+  if (w == 0) {
+    int x = (lane < kMaxE / 32) ? s_warp[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += n;
+    }
+    if (lane < kMaxE / 32) s_warp[lane] = x;   // inclusive warp totals
+  }
+  __syncthreads();
+  const int excl = v - kept + (w > 0 ? s_warp[w - 1] : 0);
+  if (e < a.E) a.offsets[e] = excl;
+  if (e == a.E - 1) a.offsets[a.E] = excl + kept;
+}
+
+__global__ void __launch_bounds__(kChunk) dispatch_scatter_kernel(DispatchArgs a) {
+  __shared__ uint32_t bits[kMaxE][kChunk / 32];
+  const int c = blockIdx.x, tid = threadIdx.x;
+  for (int i = tid; i < a.E * (kChunk / 32); i += blockDim.x) (&bits[0][0])[i] = 0u;
+  __syncthreads();
+  const int t = c * kChunk + tid;
+  const int wd = tid >> 5;
+  const uint32_t me = 1u << (tid & 31);
+  if (t < a.T) {
+    for (int j = 0; j < a.k; ++j) {
+      const int e = a.idx[(size_t)t * a.k + j];
+      if (e >= 0 && e < a.E) atomicOr(&bits[e][wd], me);
+    }
+  }
+  __syncthreads();
+  if (t >= a.T) return;
+  for (int j = 0; j < a.k; ++j) {
+    const size_t s = (size_t)t * a.k + j;
+    const int e = a.idx[s];
+    if (e < 0 || e >= a.E) {
+      a.row_of_slot[s] = -1;
+      continue;
+    }
+    int rank = a.chunk_base[(size_t)c * a.E + e] + __popc(bits[e][wd] & (me - 1u));
+    for (int q = 0; q < wd; ++q) rank += __popc(bits[e][q]);
+    if (a.capacity >= 0 && rank >= a.capacity) {
+      a.row_of_slot[s] = -1;
+    } else {
+      const int row = a.offsets[e] + rank;
+      a.row_of_slot[s] = row;
+      a.slot_of_row[row] = (int)s;
+    }
+  }
+}
+
+template <int VEC_BYTES>
+__global__ void __launch_bounds__(256) dispatch_gather_kernel(DispatchArgs a,
+                                                              int row_bytes) {
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (t >= a.T) return;
+  int rows[kMaxK];
+  int nk = 0;
+  for (int j = 0; j < a.k; ++j) {
+    const int r = a.row_of_slot[(size_t)t * a.k + j];
+    if (r >= 0) rows[nk++] = r;
+  }
+  if (nk == 0) return;
+  const int nvec = row_bytes / 16;
+  const uint4* src = reinterpret_cast<const uint4*>(static_cast<const char*>(a.X) +
+                                                    (size_t)t * row_bytes);
+  char* dst = static_cast<char*>(a.Xperm);
+  for (int v = lane; v < nvec; v += 32) {
+    const uint4 x = src[v];
+    for (int q = 0; q < nk; ++q)
+      reinterpret_cast<uint4*>(dst + (size_t)rows[q] * row_bytes)[v] = x;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_dispatch_count(const DispatchArgs& a, cudaStream_t s) {
+  const int nchunks = (a.T + kChunk - 1) / kChunk;
+  dispatch_count_kernel<<<nchunks, kChunk, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dispatch_scan(const DispatchArgs& a, cudaStream_t s) {
+  const int nchunks = (a.T + kChunk - 1) / kChunk;
+  dispatch_scan_kernel<<<1, kMaxE, 0, s>>>(a, nchunks);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dispatch_scatter(const DispatchArgs& a, cudaStream_t s) {
+  const int nchunks = (a.T + kChunk - 1) / kChunk;
+  dispatch_scatter_kernel<<<nchunks, kChunk, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dispatch_gather(const DispatchArgs& a, cudaStream_t s) {
+  const int elt = a.x_dtype == MOE_DTYPE_BF16 ? 2 : 4;
+  const int row_bytes = a.H * elt;
+  dispatch_gather_kernel<16><<<(a.T + 7) / 8, 256, 0, s>>>(a, row_bytes);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

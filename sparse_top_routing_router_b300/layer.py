@@ -1,0 +1,90 @@
+"""One MoE layer forward through the C ABI: the six steps of "LLM Internals §14.2.1"
+as five library calls (router, dispatch, grouped SwiGLU, combine, balance stats).
+
+`MoELayer` owns the device buffers of one batch shape; `forward` enqueues the calls on
+the current stream and returns device tensors; `forward_host` is the end-to-end call a
+host program makes (pinned host X in, host Y out).
+"""
+
+from __future__ import annotations
+
+from typing import Dict, Optional
+
+import torch
+
+from . import binding as B
+from .configs import MoEConfig
+
+
+class MoELayer:
+    def __init__(self, cfg: MoEConfig, weights: Dict[str, torch.Tensor],
+                 ctx: Optional[B.Context] = None, device: int = 0,
+                 capacity_factor: Optional[float] = None, gather: bool = True):
+        self.cfg = cfg
+        self.w = weights
+        self.dev = torch.device("cuda", device)
+        self.ctx = ctx if ctx is not None else B.Context(device)
+        self.score = B.MOE_SCORE_SIGMOID if cfg.score == "sigmoid" else B.MOE_SCORE_SOFTMAX
+        self.capacity = (-1 if capacity_factor is None
+                         else B.moe_capacity(capacity_factor, cfg.T, cfg.k, cfg.E))
+        self.dtype_code = B.MOE_DTYPE_BF16 if cfg.dtype == "bf16" else B.MOE_DTYPE_F32
+        self._alloc(cfg.T)
+
+    def _alloc(self, T: int) -> None:
+        c, dev = self.cfg, self.dev
+        i32, f32 = torch.int32, torch.float32
+        xdt = torch.bfloat16 if c.dtype == "bf16" else torch.float32
+        nbytes = B.moe_workspace_bytes(T, c.H, c.E, c.I, c.k, self.dtype_code, c.shared)
+        self.ws = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=dev)
+        B.moe_workspace_init(self.ws)
+        self.idx = torch.empty(T, c.k, dtype=i32, device=dev)
+        self.gate = torch.empty(T, c.k, dtype=f32, device=dev)
+        self.gap = torch.empty(T, dtype=f32, device=dev)
+        self.colsum = torch.empty(c.E, dtype=torch.float64, device=dev)
+        self.counts = torch.empty(c.E, dtype=i32, device=dev)
+        self.offsets = torch.empty(c.E + 1, dtype=i32, device=dev)
+        self.row_of_slot = torch.empty(T * c.k, dtype=i32, device=dev)
+        self.slot_of_row = torch.empty(T * c.k, dtype=i32, device=dev)
+        self.Xperm = torch.empty(T * c.k, c.H, dtype=xdt, device=dev)
+        self.O = torch.empty(T * c.k, c.H, dtype=f32, device=dev)
+        self.O_shared = torch.empty(T, c.H, dtype=f32, device=dev) if c.shared else None
+        self.Y = torch.empty(T, c.H, dtype=f32, device=dev)
+        self.f = torch.empty(c.E, dtype=torch.float64, device=dev)
+        self.p = torch.empty(c.E, dtype=torch.float64, device=dev)
+        self.stats = torch.empty(4, dtype=torch.float64, device=dev)
+        self.T = T
+
+    def forward(self, X: torch.Tensor, stats: bool = True, stream=None) -> torch.Tensor:
+        c, w = self.cfg, self.w
+        assert X.shape == (self.T, c.H)
+        B.moe_router_topk(self.ctx, X, w["Wg"], c.k, self.score, c.renorm, self.idx,
+                          self.gate, self.ws, bias=w.get("bias"),
+                          logit_bias=w.get("logit_bias"), key_gap=self.gap,
+                          prob_colsum=self.colsum, stream=stream)
+        B.moe_dispatch(self.ctx, self.idx, c.E, self.capacity, self.counts, self.offsets,
+                       self.row_of_slot, self.slot_of_row, self.ws, X=X, Xperm=self.Xperm,
+                       stream=stream)
+        B.moe_grouped_swiglu(self.ctx, X, self.Xperm, self.offsets, w["W_gate"], w["W_up"],
+                             w["W_down"], self.O, self.ws, c.k, Ws_gate=w.get("Ws_gate"),
+                             Ws_up=w.get("Ws_up"), Ws_down=w.get("Ws_down"),
+                             O_shared=self.O_shared, stream=stream)
+        B.moe_combine(self.ctx, self.O, self.row_of_slot, self.gate, self.Y,
+                      O_shared=self.O_shared, stream=stream)
+        if stats:
+            B.moe_balance_stats(self.ctx, self.T, c.k, self.counts, self.colsum, c.alpha,
+                                self.f, self.p, self.stats, offsets=self.offsets,
+                                stream=stream)
+        return self.Y
+
+    def forward_host(self, X_host: torch.Tensor, Y_host: torch.Tensor,
+                     X_dev: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+        """Host X (pinned) -> device, forward, device Y -> host Y (pinned)."""
+        if X_dev is None:
+            X_dev = torch.empty_like(X_host, device=self.dev)
+        X_dev.copy_(X_host, non_blocking=True)
+        Y = self.forward(X_dev, stream=stream)
+        Y_host.copy_(Y, non_blocking=True)
+        return Y_host
+
+    def device_status(self) -> int:
+        return B.moe_get_device_status(self.ctx, self.ws, reset=True)

@@ -1,0 +1,115 @@
+"""Host-side checks of the C ABI (no GPU needed): the library loads and exports every
+symbol include/moe.h declares; host helpers (capacity, workspace sizes, status strings);
+argument validation rejects bad calls before anything touches a device."""
+
+import ctypes as C
+import math
+import os
+import re
+
+import pytest
+
+from oracle import moe_oracle as O
+from sparse_top_routing_router_b300 import binding as B
+from sparse_top_routing_router_b300 import build as BUILD
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    BUILD.build()
+    return B.lib()
+
+
+def header_functions():
+    src = open(os.path.join(ROOT, "include", "moe.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_\w+)\s*\(", src)))
+
+
+def test_exports_match_header(L):
+    names = header_functions()
+    assert len(names) >= 15
+    for n in names:
+        assert hasattr(L, n), n
+    assert sorted(B.EXPORTS) == names
+
+
+def test_version_and_strings(L):
+    assert L.moe_version() == 10000
+    assert B.status_string(0) == "ok"
+    assert B.status_string(-4) == "device wait timed out"
+    for i, n in enumerate(B.KERNEL_NAMES):
+        assert L.moe_kernel_name(i).decode() == n
+    assert L.moe_kernel_name(99).decode() == "unknown"
+
+
+@pytest.mark.parametrize("c,T,k,E", [(1.0, 6, 2, 4), (2.0, 6, 2, 4), (1.25, 8192, 2, 64),
+                                     (1.0, 16384, 1, 64), (1.25, 16384, 1, 64),
+                                     (0.1, 7, 3, 5), (1.1, 1000, 2, 7), (0.0, 10, 1, 2),
+                                     (3.0, 0, 1, 2), (1e-300, 5, 1, 1), (0.7, 1, 1, 3)])
+def test_capacity_matches_oracle(L, c, T, k, E):
+    assert B.moe_capacity(c, T, k, E) == O.capacity(c, T, k, E)
+
+
+def test_capacity_rejects(L):
+    for bad in [(-1.0, 4, 1, 2), (math.inf, 4, 1, 2), (math.nan, 4, 1, 2), (1.0, -1, 1, 2),
+                (1.0, 4, 0, 2), (1.0, 4, 1, 0), (1e30, 4, 1, 1)]:
+        with pytest.raises(B.MoEError):
+            B.moe_capacity(*bad)
+
+
+def test_workspace_bytes(L):
+    ws = B.moe_workspace_bytes(8192, 7168, 256, 2048, 8, B.MOE_DTYPE_BF16, 1)
+    h = (8192 * 8 + 8192) * 2048 * 2
+    assert h < ws < h + 8192 * 256 * 4 + 2 * 32 * 256 * 4 + 4096
+    assert B.moe_workspace_bytes(-1, 1, 1, 1, 1, 0, 0) == 0
+    assert B.moe_workspace_bytes(0, 64, 8, 64, 2, 0, 0) >= 256
+
+
+def test_validation_before_device(L):
+    """Bad requests fail with the right code and never reach the (absent) device."""
+    vp = C.c_void_p
+    fake = vp(4096)   # never dereferenced: validation fails first
+    d = B.RouterDesc(16, 64, 600, 2, 0, 1, 0)
+    r = L.moe_router_topk(None, C.byref(d), fake, fake, None, None, fake, fake, None, None,
+                          fake, 1 << 20, None)
+    assert r == B.MOE_ERR_UNSUPPORTED and "E = 600" in B.last_error_detail()
+    d = B.RouterDesc(16, 64, 8, 9, 0, 1, 0)
+    r = L.moe_router_topk(None, C.byref(d), fake, fake, None, None, fake, fake, None, None,
+                          fake, 1 << 20, None)
+    assert r == B.MOE_ERR_UNSUPPORTED and "k = 9" in B.last_error_detail()
+    d = B.RouterDesc(16, 64, 8, 2, 7, 1, 0)
+    r = L.moe_router_topk(None, C.byref(d), fake, fake, None, None, fake, fake, None, None,
+                          fake, 1 << 20, None)
+    assert r == B.MOE_ERR_INVALID_ARG and "score" in B.last_error_detail()
+    d = B.RouterDesc(16, 64, 8, 2, 0, 1, 0)
+    r = L.moe_router_topk(None, C.byref(d), vp(4097), fake, None, None, fake, fake, None,
+                          None, fake, 1 << 20, None)
+    assert r == B.MOE_ERR_INVALID_ARG and "aligned" in B.last_error_detail()
+    r = L.moe_router_topk(None, C.byref(d), fake, fake, None, None, fake, fake, None, None,
+                          fake, 64, None)
+    assert r == B.MOE_ERR_INVALID_ARG and "workspace" in B.last_error_detail()
+    r = L.moe_router_topk(None, C.byref(d), fake, fake, None, None, fake, fake, None, None,
+                          fake, 1 << 20, None)
+    assert r == B.MOE_ERR_INVALID_ARG and "ctx" in B.last_error_detail()
+    # dispatch: X without Xperm
+    r = L.moe_dispatch(None, 16, 2, 8, 64, 0, -1, fake, fake, fake, fake, fake, fake, None,
+                       fake, 1 << 20, None)
+    assert r == B.MOE_ERR_INVALID_ARG and "together" in B.last_error_detail()
+    # expert stage: H not a multiple of 64 for bf16
+    e = B.ExpertDesc(16, 96, 8, 128, 2, 0, 0)
+    args = [fake] * 12
+    r = L.moe_grouped_swiglu(None, C.byref(e), *args, 1 << 30, None)
+    assert r == B.MOE_ERR_UNSUPPORTED and "64" in B.last_error_detail()
+    e = B.ExpertDesc(16, 128, 8, 128, 2, 0, 1)
+    args = [fake, fake, fake, fake, fake, fake, None, None, None, fake, None, fake]
+    r = L.moe_grouped_swiglu(None, C.byref(e), *args, 1 << 30, None)
+    assert r == B.MOE_ERR_INVALID_ARG and "shared" in B.last_error_detail()
+    # combine: H not a multiple of 4
+    r = L.moe_combine(None, 4, 2, 6, fake, None, fake, fake, fake, None, None)
+    assert r == B.MOE_ERR_UNSUPPORTED
+    # stats: missing outputs
+    r = L.moe_balance_stats(None, 4, 1, 4, fake, None, fake, 0.01, None, fake, fake, None)
+    assert r == B.MOE_ERR_INVALID_ARG

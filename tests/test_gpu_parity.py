@@ -1,0 +1,67 @@
+"""GPU parity of the whole forward against the fp64 oracle, through the C ABI.
+
+Small cases (several tiles and ragged tails) compare every token; the full-size
+workloads compare the routing of every token and the output of a seeded token sample.
+"""
+
+import gc
+
+import numpy as np
+import pytest
+import torch
+
+from sparse_top_routing_router_b300 import configs as K
+
+from . import parity as P
+
+pytestmark = pytest.mark.gpu
+
+SMALL = [
+    K.TINY_F32,
+    K.scaled(K.MIXTRAL, name="mixtral_small", T=300, H=256, I=512),
+    K.scaled(K.DSV3_PREFILL, name="dsv3_small", T=200, H=512, E=64, I=256),
+    K.scaled(K.DSV3_PREFILL, name="dsv3_small_noshared", T=130, H=256, E=32, I=192,
+             shared=False, k=4),
+    K.scaled(K.SWITCH, name="switch_small", T=1000, H=256, E=16, I=256),
+]
+
+
+def _cleanup():
+    gc.collect()
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("cfg", SMALL, ids=lambda c: c.name)
+def test_small_full_parity(cfg):
+    cfs = cfg.capacity_factors or (None,)
+    for cf in cfs:
+        run = P.run_gpu(cfg, capacity_factor=cf)
+        assert run.status == 0
+        ref = P.oracle_route(run)
+        info = P.check_routing(run, ref)
+        P.check_dispatch(run, P.to_np(run.layer.idx).astype(np.int64))
+        out = P.check_output(run, ref)
+        P.check_stats(run, ref)
+        assert out["tokens"] >= cfg.T - info["excluded_rows"]
+        print(cfg.name, cf, info, out)
+    _cleanup()
+
+
+FULL = [(K.MIXTRAL, None, 48), (K.DSV3_DECODE, None, 64), (K.DSV3_PREFILL, None, 24),
+        (K.SWITCH, 1.0, 96), (K.SWITCH, 1.25, 96)]
+
+
+@pytest.mark.parametrize("cfg,cf,n_tok", FULL,
+                         ids=lambda v: v.name if hasattr(v, "name") else str(v))
+def test_full_size_parity(cfg, cf, n_tok):
+    run = P.run_gpu(cfg, capacity_factor=cf)
+    assert run.status == 0
+    ref = P.oracle_route(run)
+    info = P.check_routing(run, ref)
+    P.check_dispatch(run, P.to_np(run.layer.idx).astype(np.int64))
+    out = P.check_output(run, ref, n_tokens=n_tok)
+    if cfg.alpha:
+        P.check_stats(run, ref)
+    print(cfg.name, cf, info, out)
+    del run
+    _cleanup()

@@ -18,7 +18,6 @@ import argparse
 import hashlib
 import json
 import os
-import re
 import statistics
 import subprocess
 import sys
@@ -126,13 +125,25 @@ def traffic_from_profile():
 
 # --------------------------------------------------------------------------- CPU oracle
 
+def blas_threads() -> int:
+    """Threads numpy's BLAS runs the oracle's matmuls with."""
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 1) for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return max(n)
+    except ImportError:
+        pass
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        if os.environ.get(var, "").isdigit():
+            return int(os.environ[var])
+    return len(os.sched_getaffinity(0))
+
+
 def oracle_sample(cfg, d, cf, n_tokens: int, seed: int):
     """Time the fp64 oracle: routing of all T tokens (capacity is a batch property), then
     experts + combine for a seeded sample of n_tokens.  Expert weights of the sample are
     staged in host memory before the clock starts."""
-    import numpy as np
-    from threadpoolctl import threadpool_info
-
     from oracle import moe_oracle as O
 
     def host(t):
@@ -153,8 +164,7 @@ def oracle_sample(cfg, d, cf, n_tokens: int, seed: int):
     t0 = time.perf_counter()
     O.combine_subset(X, r, lambda e: W[e], tokens, shared)
     t_ffn = time.perf_counter() - t0
-    threads = max([i.get("num_threads", 1) for i in threadpool_info()] or [1])
-    return t_route, t_ffn, int(tokens.size), threads
+    return t_route, t_ffn, int(tokens.size), blas_threads()
 
 
 def run_reference(args, cfg, cf):

@@ -213,6 +213,15 @@ int moe_ctx_set_tracing(moe_ctx* ctx, int enable);
 int moe_ctx_trace_read(moe_ctx* ctx, int* launches, double* total_ms, int n);
 const char* moe_kernel_name(int id);
 
+/* Failure-detection test hook (not for production use).  hook = MOE_TEST_HOOK_NONE
+ * restores normal operation.  MOE_TEST_HOOK_WITHHOLD_LOAD makes the tensor-core expert
+ * kernel skip the first operand load of each CTA, a barrier that nothing completes: the
+ * bounded waits run out after wait_limit_ms (0 keeps the default 2000 ms), the kernel
+ * records MOE_ERR_TIMEOUT in the workspace status word, frees its tensor memory and
+ * returns, and the context stays usable.  Nothing faults, traps or hangs. */
+enum moe_test_hook { MOE_TEST_HOOK_NONE = 0, MOE_TEST_HOOK_WITHHOLD_LOAD = 1 };
+int moe_ctx_set_test_hook(moe_ctx* ctx, int hook, int wait_limit_ms);
+
 const char* moe_status_string(int status);
 /* Text describing why the last call made by this thread failed ("" after a success).
  * Host-only; the pointer stays valid until this thread's next call. */

@@ -23,6 +23,7 @@ MOE_ERR_TIMEOUT = -4
 MOE_ERR_DEVICE_INDEX = -5
 MOE_SCORE_SOFTMAX, MOE_SCORE_SIGMOID = 0, 1
 MOE_DTYPE_BF16, MOE_DTYPE_F32 = 0, 1
+MOE_TEST_HOOK_NONE, MOE_TEST_HOOK_WITHHOLD_LOAD = 0, 1
 
 KERNEL_NAMES = ["router_logits", "router_select", "dispatch_count", "dispatch_scan",
                 "dispatch_scatter", "dispatch_gather", "expert_gate_up", "expert_down",
@@ -32,7 +33,8 @@ MOE_KERNEL_COUNT = len(KERNEL_NAMES)
 EXPORTS = ["moe_ctx_create", "moe_ctx_destroy", "moe_workspace_bytes", "moe_workspace_init",
            "moe_capacity", "moe_router_topk", "moe_dispatch", "moe_grouped_swiglu",
            "moe_combine", "moe_balance_stats", "moe_get_device_status",
-           "moe_ctx_set_tracing", "moe_ctx_trace_read", "moe_kernel_name",
+           "moe_ctx_set_tracing", "moe_ctx_trace_read", "moe_ctx_set_test_hook",
+           "moe_kernel_name",
            "moe_status_string", "moe_last_error_detail", "moe_version"]
 
 
@@ -79,6 +81,7 @@ def lib() -> C.CDLL:
     L.moe_balance_stats.argtypes = [vp, i, i, i, vp, vp, vp, d, vp, vp, vp, vp]
     L.moe_get_device_status.argtypes = [vp, vp, C.POINTER(i), i, vp]
     L.moe_ctx_set_tracing.argtypes = [vp, i]
+    L.moe_ctx_set_test_hook.argtypes = [vp, i, i]
     L.moe_ctx_trace_read.argtypes = [vp, C.POINTER(i), C.POINTER(d), i]
     L.moe_kernel_name.argtypes = [i]
     L.moe_kernel_name.restype = C.c_char_p
@@ -148,6 +151,10 @@ class Context:
 
     def set_tracing(self, enable: bool) -> None:
         _check("moe_ctx_set_tracing", lib().moe_ctx_set_tracing(self.handle, int(enable)))
+
+    def set_test_hook(self, hook: int, wait_limit_ms: int = 0) -> None:
+        _check("moe_ctx_set_test_hook",
+               lib().moe_ctx_set_test_hook(self.handle, hook, wait_limit_ms))
 
     def trace_read(self) -> dict:
         n = MOE_KERNEL_COUNT

@@ -15,11 +15,17 @@
 
 using namespace moe;
 
+namespace {
+constexpr unsigned long long kWaitLimitDefaultNs = 2000000000ull;
+}
+
 struct moe_ctx {
   int device = 0;
   int num_sms = 0;
   EncodeTiledFn encode = nullptr;
   bool tracing = false;
+  int test_hook = MOE_TEST_HOOK_NONE;
+  unsigned long long wait_limit_ns = kWaitLimitDefaultNs;
   struct Rec {
     int id;
     cudaEvent_t a, b;
@@ -332,6 +338,10 @@ int moe_grouped_swiglu(moe_ctx* ctx, const moe_expert_desc* d, const void* X,
   } else {
     return fail(MOE_ERR_INVALID_ARG, "dtype = %d", d->dtype);
   }
+  if (d->T == 0) {
+    int rc = check_ctx(ctx);
+    return rc ? rc : ok();
+  }
   if (!offsets || !W_gate || !W_up || !W_down || !O || !Xperm || !ws)
     return fail(MOE_ERR_INVALID_ARG, "offsets, weights, Xperm, O and ws are required");
   if (d->has_shared && (!X || !Ws_gate || !Ws_up || !Ws_down || !O_shared))
@@ -365,6 +375,8 @@ int moe_grouped_swiglu(moe_ctx* ctx, const moe_expert_desc* d, const void* X,
   a.O = O;
   a.O_shared = O_shared;
   a.status = static_cast<int*>(ws);
+  a.test_hook = ctx->test_hook;
+  a.wait_limit_ns = ctx->wait_limit_ns;
   cudaError_t e;
   if (d->dtype == MOE_DTYPE_BF16) {
     bool bad = false;
@@ -429,6 +441,17 @@ int moe_get_device_status(moe_ctx* ctx, void* ws, int* status, int reset,
   if ((e = cudaMemcpy(status, ws, sizeof(int), cudaMemcpyDeviceToHost)))
     return cuda_fail(e, "cudaMemcpy");
   if (reset && (e = cudaMemset(ws, 0, sizeof(int)))) return cuda_fail(e, "cudaMemset");
+  return ok();
+}
+
+int moe_ctx_set_test_hook(moe_ctx* ctx, int hook, int wait_limit_ms) {
+  if (!ctx) return fail(MOE_ERR_INVALID_ARG, "ctx is null");
+  if (hook != MOE_TEST_HOOK_NONE && hook != MOE_TEST_HOOK_WITHHOLD_LOAD)
+    return fail(MOE_ERR_INVALID_ARG, "hook = %d", hook);
+  if (wait_limit_ms < 0) return fail(MOE_ERR_INVALID_ARG, "wait_limit_ms < 0");
+  ctx->test_hook = hook;
+  ctx->wait_limit_ns =
+      wait_limit_ms ? (unsigned long long)wait_limit_ms * 1000000ull : kWaitLimitDefaultNs;
   return ok();
 }
 

@@ -50,6 +50,8 @@ struct TcParams {
   float* O;
   float* O_shared;
   int* status;
+  int test_hook;
+  unsigned long long wait_limit_ns;
 };
 
 struct __align__(1024) Smem {
@@ -201,11 +203,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       const CUtensorMap* a_map = sh ? &mA_sh : &mA;
       const int ay = ti.row0 + ti.m0;
       for (int kb = 0; kb < nkb; ++kb) {
-        if (!mbar_wait(&S.empty[stage], phase ^ 1u, abort_flag)) {
+        if (!mbar_wait(&S.empty[stage], phase ^ 1u, abort_flag, p.wait_limit_ns)) {
           ok = false;
           break;
         }
         uint8_t* st = S.tiles[stage];
+        if (p.test_hook == MOE_TEST_HOOK_WITHHOLD_LOAD && tile == (int)blockIdx.x && kb == 0) {
+          // test only: the first stage is never filled, so the MMA issuer's bounded wait
+          // on it runs out and the CTA takes its timeout path
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+          continue;
+        }
         mbar_arrive_expect_tx(&S.full[stage], kStageBytes);
         tma_load_2d(st, a_map, &S.full[stage], kb * BK, ay);
         if (MODE == GATE_UP) {
@@ -242,7 +253,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // let every copy already issued land before the CTA's shared memory goes away
       const int zero = 0;
       for (int s = 0; s < kStages; ++s)
-        if (issued_mask >> s & 1u) mbar_wait(&S.full[s], issued_parity >> s & 1u, &zero);
+        if (issued_mask >> s & 1u)
+          mbar_wait(&S.full[s], issued_parity >> s & 1u, &zero, p.wait_limit_ns);
     }
   } else if (warp == 1 && lane == 0) {
     // ---------------------------------------------------------------- MMA issuer
@@ -250,14 +262,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t phase = 0, acc_phase = 0;
     bool ok = true;
     for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-      if (!mbar_wait(&S.tempty[acc], acc_phase ^ 1u, abort_flag)) {
+      if (!mbar_wait(&S.tempty[acc], acc_phase ^ 1u, abort_flag, p.wait_limit_ns)) {
         ok = false;
         break;
       }
       tc_fence_after();
       const uint32_t d = tmem_base + acc * kAccCols;
       for (int kb = 0; kb < nkb; ++kb) {
-        if (!mbar_wait(&S.full[stage], phase, abort_flag)) {
+        if (!mbar_wait(&S.full[stage], phase, abort_flag, p.wait_limit_ns)) {
           ok = false;
           break;
         }
@@ -287,7 +299,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // wait for the MMAs already issued before TMEM is released
       umma_commit(&S.drain);
       const int zero = 0;
-      mbar_wait(&S.drain, 0, &zero);
+      mbar_wait(&S.drain, 0, &zero, p.wait_limit_ns);
     }
   } else if (warp >= 2) {
     // ---------------------------------------------------------------- epilogue
@@ -297,7 +309,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t acc_phase = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
       const TileInfo ti = decode_tile(S, tile, p.n_tile);
-      const bool got = mbar_wait(&S.tfull[acc], acc_phase, abort_flag);
+      const bool got = mbar_wait(&S.tfull[acc], acc_phase, abort_flag, p.wait_limit_ns);
       if (!__all_sync(0xffffffffu, got)) {
         S.abort_flag = 1;
         set_status(p.status, MOE_ERR_TIMEOUT);
@@ -434,6 +446,8 @@ cudaError_t launch_tc(const ExpertArgs& a, EncodeTiledFn enc, bool* encode_faile
   p.O = a.O;
   p.O_shared = a.O_shared;
   p.status = a.status;
+  p.test_hook = a.test_hook;
+  p.wait_limit_ns = a.wait_limit_ns;
 
   const int n_tiles_n = (N + n_tile - 1) / n_tile;
   const long long m_tiles_bound =

@@ -94,6 +94,8 @@ struct ExpertArgs {
   float* O;
   float* O_shared;
   int* status;
+  int test_hook;                  // MOE_TEST_HOOK_* (0 in normal use)
+  unsigned long long wait_limit_ns;
 };
 // bf16 tensor-core path.  `encode` is the driver's cuTensorMapEncodeTiled.
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,

@@ -58,16 +58,17 @@ MOE_DEV bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Wait for the phase of `parity` to complete.  False on timeout or when another role
-// of the CTA raised the abort flag.
-MOE_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, const volatile int* abort_flag) {
+// Wait for the phase of `parity` to complete.  False on timeout (limit_ns) or when
+// another role of the CTA raised the abort flag.
+MOE_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, const volatile int* abort_flag,
+                       unsigned long long limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((i & 63u) == 0) {
       if (*abort_flag) return false;
-      if (globaltimer() - t0 > kWaitLimitNs) return false;
+      if (globaltimer() - t0 > limit_ns) return false;
     }
   }
 }

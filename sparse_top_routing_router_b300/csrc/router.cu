@@ -2,7 +2,7 @@
 // W_g[H,E], then top-k per row and normalisation among the k chosen; "AI Knowledge Map
 // - MoE": score, softmax, top-k hard selection, renormalise).
 //
-// Two kernels:
+// Two kernels (the first in a wide and a narrow form):
 //  router_logits  fp32 CUDA-core GEMM l = X W_g (+ logit offset).  Each 32-long block
 //                 of the reduction is summed with fp32 FMA, and the block partials are
 //                 folded into a (hi, lo) pair with TwoSum (Knuth), so the error is that of
@@ -155,6 +155,90 @@ __global__ void __launch_bounds__(256) router_logits_kernel(RouterArgs a) {
       const int e = e0 + tx * 4 + j;
       if (e >= E) continue;
       float h = hi[i][j], l = lo[i][j];
+      if (a.logit_bias) two_sum(h, l, a.logit_bias[e]);
+      a.logits[(size_t)t * E + e] = h + l;
+    }
+  }
+}
+
+// Narrow routers (E <= 16): a CTA owns 32 tokens and walks H in chunks of 256 (128 for
+// E > 8); thread
+// (token, g) sums h = g, g+8, ... of the chunk (32 or 16 terms) for every expert, folds the
+// block partial into its (hi, lo) pair, and the 8 partial pairs of a token are merged with
+// TwoSum across lanes.  Same error class as router_logits_kernel, 16x less padding work.
+template <typename TX, int EP>
+__global__ void __launch_bounds__(256) router_logits_narrow_kernel(RouterArgs a) {
+  constexpr int TM = 32, HC = EP <= 8 ? 256 : 128;   // static shared memory under 48 KB
+  __shared__ __align__(16) float sX[TM][HC + 8];
+  __shared__ __align__(16) float sW[HC][EP];
+  const TX* X = static_cast<const TX*>(a.X);
+  const int T = a.T, H = a.H, E = a.E;
+  const int tid = threadIdx.x, tl = tid >> 3, g = tid & 7;
+  const int t0 = blockIdx.x * TM;
+  const bool vec_x = (H % 8) == 0;
+  float hi[EP], lo[EP];
+#pragma unroll
+  for (int e = 0; e < EP; ++e) hi[e] = lo[e] = 0.f;
+
+  for (int kb = 0; kb < H; kb += HC) {
+#pragma unroll
+    for (int q = 0; q < TM * HC / 8 / 256; ++q) {
+      const int v = tid + q * 256;
+      const int r = v / (HC / 8), c = (v % (HC / 8)) * 8;
+      const int t = t0 + r, h = kb + c;
+      float x[8];
+      if (t < T && vec_x && h + 8 <= H) {
+        load_x8<TX>(X, (size_t)t * H + h, x);
+      } else {
+#pragma unroll
+        for (int m = 0; m < 8; ++m)
+          x[m] = (t < T && h + m < H) ? load_x1<TX>(X, (size_t)t * H + h + m) : 0.f;
+      }
+      *reinterpret_cast<float4*>(&sX[r][c]) = make_float4(x[0], x[1], x[2], x[3]);
+      *reinterpret_cast<float4*>(&sX[r][c + 4]) = make_float4(x[4], x[5], x[6], x[7]);
+    }
+    for (int i = tid; i < HC * EP; i += 256) {
+      const int r = i / EP, e = i % EP;
+      const int h = kb + r;
+      sW[r][e] = (h < H && e < E) ? a.Wg[(size_t)h * E + e] : 0.f;
+    }
+    __syncthreads();
+    float p[EP];
+#pragma unroll
+    for (int e = 0; e < EP; ++e) p[e] = 0.f;
+#pragma unroll 8
+    for (int j = 0; j < HC / 8; ++j) {
+      const int h = g + 8 * j;
+      const float x = sX[tl][h];
+#pragma unroll
+      for (int q = 0; q < EP / 4; ++q) {
+        const float4 w = *reinterpret_cast<const float4*>(&sW[h][4 * q]);
+        p[4 * q + 0] = fmaf(x, w.x, p[4 * q + 0]);
+        p[4 * q + 1] = fmaf(x, w.y, p[4 * q + 1]);
+        p[4 * q + 2] = fmaf(x, w.z, p[4 * q + 2]);
+        p[4 * q + 3] = fmaf(x, w.w, p[4 * q + 3]);
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < EP; ++e) two_sum(hi[e], lo[e], p[e]);
+    __syncthreads();
+  }
+#pragma unroll
+  for (int o = 1; o < 8; o <<= 1) {
+#pragma unroll
+    for (int e = 0; e < EP; ++e) {
+      const float h2 = __shfl_xor_sync(0xffffffffu, hi[e], o);
+      const float l2 = __shfl_xor_sync(0xffffffffu, lo[e], o);
+      two_sum(hi[e], lo[e], h2);
+      lo[e] += l2;
+    }
+  }
+  const int t = t0 + tl;
+  if (g == 0 && t < T) {
+#pragma unroll
+    for (int e = 0; e < EP; ++e) {
+      if (e >= E) break;
+      float h = hi[e], l = lo[e];
       if (a.logit_bias) two_sum(h, l, a.logit_bias[e]);
       a.logits[(size_t)t * E + e] = h + l;
     }
@@ -453,6 +537,18 @@ cudaError_t launch_select_t(const RouterArgs& a, cudaStream_t s) {
 }  // namespace
 
 cudaError_t launch_router_logits(const RouterArgs& a, cudaStream_t s) {
+  if (a.E <= 16) {
+    const dim3 g((a.T + 31) / 32);
+    const bool bf = a.x_dtype == MOE_DTYPE_BF16;
+    if (a.E <= 8) {
+      if (bf) router_logits_narrow_kernel<__nv_bfloat16, 8><<<g, 256, 0, s>>>(a);
+      else router_logits_narrow_kernel<float, 8><<<g, 256, 0, s>>>(a);
+    } else {
+      if (bf) router_logits_narrow_kernel<__nv_bfloat16, 16><<<g, 256, 0, s>>>(a);
+      else router_logits_narrow_kernel<float, 16><<<g, 256, 0, s>>>(a);
+    }
+    return cudaGetLastError();
+  }
   const dim3 grid((a.T + kTM - 1) / kTM, (a.E + kTE - 1) / kTE);
   if (a.x_dtype == MOE_DTYPE_BF16)
     router_logits_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(a);

@@ -113,3 +113,8 @@ def test_validation_before_device(L):
     # stats: missing outputs
     r = L.moe_balance_stats(None, 4, 1, 4, fake, None, fake, 0.01, None, fake, fake, None)
     assert r == B.MOE_ERR_INVALID_ARG
+
+
+def test_test_hook_validation(L):
+    assert L.moe_ctx_set_test_hook(None, 1, 10) == B.MOE_ERR_INVALID_ARG
+    assert L.moe_ctx_set_tracing(None, 1) == B.MOE_ERR_INVALID_ARG

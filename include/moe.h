@@ -141,6 +141,27 @@ int moe_dispatch(moe_ctx* ctx, int T, int k, int E, int H, int x_dtype, int capa
                  int32_t* offsets, int32_t* row_of_slot, int32_t* slot_of_row,
                  void* Xperm, void* ws, size_t ws_bytes, moe_stream_t stream);
 
+/* Allocation-free dispatch.  The paper has no counterpart to this call: it exists for
+ * callers that cannot call cudaMalloc - code running while a CUDA graph is being captured,
+ * or under a runtime that owns all device memory and will not hand out scratch.  It does
+ * what moe_dispatch does, with the same arguments minus the context and the workspace:
+ * its scratch (the per-chunk count and base tables) is a file-scope static device array
+ * of 1 MiB that every GPU which loads the library keeps until the process exits.
+ *  - T may be at most 65536; larger T returns MOE_ERR_UNSUPPORTED and enqueues nothing.
+ *  - It calls no cudaMalloc, cudaFree or other allocating routine.
+ *  - The first call on a device looks up the array's device address (once per device,
+ *    with that device current); make that first call before any stream capture begins.
+ *  - Every call shares the one array: calls whose work overlaps on the GPU (different
+ *    streams, or different host threads on one device) race and corrupt each other; the
+ *    array keeps the last call's contents, and each call rewrites every entry it reads.
+ *  - Out-of-range expert indices are skipped (their slots get -1) but not reported: there
+ *    is no workspace status word.
+ * Returns MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED or MOE_ERR_CUDA. */
+int moe_dispatch_static(int T, int k, int E, int H, int x_dtype, int capacity,
+                        const int32_t* topk_idx, const void* X, int32_t* counts,
+                        int32_t* offsets, int32_t* row_of_slot, int32_t* slot_of_row,
+                        void* Xperm, moe_stream_t stream);
+
 /* ------------------------------------------------------------------ step 5 */
 
 /* Per-expert SwiGLU FFN over the permuted rows (§14.2.1 step 5, §14.2.2 three

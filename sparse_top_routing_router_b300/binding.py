@@ -31,7 +31,8 @@ KERNEL_NAMES = ["router_logits", "router_select", "dispatch_count", "dispatch_sc
 MOE_KERNEL_COUNT = len(KERNEL_NAMES)
 
 EXPORTS = ["moe_ctx_create", "moe_ctx_destroy", "moe_workspace_bytes", "moe_workspace_init",
-           "moe_capacity", "moe_router_topk", "moe_dispatch", "moe_grouped_swiglu",
+           "moe_capacity", "moe_router_topk", "moe_dispatch", "moe_dispatch_static",
+           "moe_grouped_swiglu",
            "moe_combine", "moe_balance_stats", "moe_get_device_status",
            "moe_ctx_set_tracing", "moe_ctx_trace_read", "moe_ctx_set_test_hook",
            "moe_kernel_name",
@@ -76,6 +77,7 @@ def lib() -> C.CDLL:
     L.moe_router_topk.argtypes = [vp, C.POINTER(RouterDesc), vp, vp, vp, vp, vp, vp, vp, vp,
                                   vp, sz, vp]
     L.moe_dispatch.argtypes = [vp, i, i, i, i, i, i, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    L.moe_dispatch_static.argtypes = [i, i, i, i, i, i, vp, vp, vp, vp, vp, vp, vp, vp]
     L.moe_grouped_swiglu.argtypes = [vp, C.POINTER(ExpertDesc)] + [vp] * 12 + [sz, vp]
     L.moe_combine.argtypes = [vp, i, i, i, vp, vp, vp, vp, vp, vp, vp]
     L.moe_balance_stats.argtypes = [vp, i, i, i, vp, vp, vp, d, vp, vp, vp, vp]

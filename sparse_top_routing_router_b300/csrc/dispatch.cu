@@ -11,6 +11,8 @@
 //           row_of_slot / slot_of_row, or -1 beyond capacity
 //  gather   one warp per token: its X row copied once to each of its kept rows, with
 //           16-byte vector moves
+#include <mutex>
+
 #include "moe_internal.h"
 #include "ptx.cuh"
 
@@ -162,4 +164,100 @@ cudaError_t launch_dispatch_gather(const DispatchArgs& a, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+
+// ---------------------------------------------------------------- allocation-free entry
+//
+// moe_dispatch_static: the same dispatch for callers that cannot call cudaMalloc - code
+// that runs where the device allocator is off limits (inside a region that a CUDA graph is
+// being captured from, under a host runtime or inference engine that owns all device
+// memory and hands out only fixed buffers, or in a process whose allocator must never
+// grow).  Its scratch (the per-chunk count and base tables) lives in the array below,
+// which the module holds on every GPU that loads the library until the process exits.
+
+namespace {
+constexpr int kStaticMaxT = 65536;                                   // tokens per call
+constexpr int kStaticMaxChunks = kStaticMaxT / kDispatchChunk;       // 256
+constexpr size_t kStaticScratchInts = 2ull * kStaticMaxChunks * kMaxE;  // 1 MiB of int32
+constexpr int kMaxDevices = 64;
+}  // namespace
+
+static __device__ __align__(256) int32_t g_dispatch_scratch[kStaticScratchInts];
+
+namespace {
+std::mutex g_scratch_mu;
+int32_t* g_scratch_addr[kMaxDevices] = {};
+
+// Device address of g_dispatch_scratch on the current device, looked up once per device.
+// In host code the array's name is only a host-side stand-in, so kernels must be given
+// this address, never the name.
+cudaError_t static_scratch(int32_t** out) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lk(g_scratch_mu);
+  if (!g_scratch_addr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_dispatch_scratch);
+    if (e != cudaSuccess) return e;
+    g_scratch_addr[dev] = static_cast<int32_t*>(p);
+  }
+  *out = g_scratch_addr[dev];
+  return cudaSuccess;
+}
+}  // namespace
+
 }  // namespace moe
+
+extern "C" int moe_dispatch_static(int T, int k, int E, int H, int x_dtype, int capacity,
+                                   const int32_t* topk_idx, const void* X, int32_t* counts,
+                                   int32_t* offsets, int32_t* row_of_slot,
+                                   int32_t* slot_of_row, void* Xperm, moe_stream_t stream) {
+  using namespace moe;
+  if (T < 0 || E < 1 || E > kMaxE || k < 1 || k > E || k > kMaxK) return MOE_ERR_INVALID_ARG;
+  if (T > kStaticMaxT) return MOE_ERR_UNSUPPORTED;   // beyond the static scratch
+  if (!counts || !offsets) return MOE_ERR_INVALID_ARG;
+  if (T > 0 && (!topk_idx || !row_of_slot || !slot_of_row)) return MOE_ERR_INVALID_ARG;
+  if ((X == nullptr) != (Xperm == nullptr)) return MOE_ERR_INVALID_ARG;
+  if (Xperm) {
+    if (x_dtype != MOE_DTYPE_BF16 && x_dtype != MOE_DTYPE_F32) return MOE_ERR_INVALID_ARG;
+    if (H < 1 || (H * (x_dtype == MOE_DTYPE_BF16 ? 2 : 4)) % 16 != 0) return MOE_ERR_UNSUPPORTED;
+    if ((reinterpret_cast<uintptr_t>(X) | reinterpret_cast<uintptr_t>(Xperm)) & 15u)
+      return MOE_ERR_INVALID_ARG;
+  }
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  int32_t* scratch = nullptr;
+  if (static_scratch(&scratch) != cudaSuccess) return MOE_ERR_CUDA;
+  if (T == 0) {
+    if (cudaMemsetAsync(counts, 0, sizeof(int32_t) * E, s) != cudaSuccess ||
+        cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (E + 1), s) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    return MOE_OK;
+  }
+  const int nchunks = (T + kDispatchChunk - 1) / kDispatchChunk;
+  DispatchArgs a;
+  a.T = T;
+  a.k = k;
+  a.E = E;
+  a.H = H;
+  a.x_dtype = x_dtype;
+  a.capacity = capacity < 0 ? -1 : capacity;
+  a.idx = topk_idx;
+  a.X = X;
+  a.counts = counts;
+  a.offsets = offsets;
+  a.row_of_slot = row_of_slot;
+  a.slot_of_row = slot_of_row;
+  a.Xperm = Xperm;
+  // every entry of both tables is written by count / scan before it is read, so the
+  // previous call's contents need no clearing
+  a.chunk_counts = scratch;
+  a.chunk_base = scratch + (size_t)nchunks * E;
+  a.status = nullptr;
+  if (launch_dispatch_count(a, s) != cudaSuccess || launch_dispatch_scan(a, s) != cudaSuccess ||
+      launch_dispatch_scatter(a, s) != cudaSuccess ||
+      (Xperm && launch_dispatch_gather(a, s) != cudaSuccess))
+    return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+

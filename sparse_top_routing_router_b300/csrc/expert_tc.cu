@@ -3,42 +3,56 @@
 // then back to H; §14.2.2: the expert is a three-matrix SwiGLU).
 //
 // One persistent, warp-specialised kernel template serves both GEMMs of the expert:
-//   GATE_UP: h = SiLU(x W_gate^T) * (x W_up^T), bf16 out.  One 128x256 accumulator holds
-//            the gate tile (columns 0-127) and the up tile (128-255) of the same 128
+//   GATE_UP: h = SiLU(x W_gate^T) * (x W_up^T), bf16 out.  One 256-column accumulator
+//            holds the gate tile (columns 0-127) and the up tile (128-255) of the same
 //            rows, so the SwiGLU is applied in the epilogue straight from TMEM.
-//   DOWN:    o = h W_down^T, fp32 out, 128x256 tiles.
+//   DOWN:    o = h W_down^T, fp32 out, 256-column tiles.
+// and two shapes of work unit:
+//   single CTA (PAIR = false): 128-row tiles, tcgen05.mma.cta_group::1 M=128 N=256; a
+//            stage holds A [128 x 64] and both weight boxes [2 x 128 x 64] (48 KB), 4 stages.
+//   CTA pair   (PAIR = true):  a cluster of 2 CTAs owns a 256-row tile; each CTA loads its
+//            own 128 rows of A and one 128-row weight box (32 KB per stage, 6 stages),
+//            the leader CTA issues tcgen05.mma.cta_group::2 M=256 N=256 over both CTAs'
+//            shared memory, and each CTA's TMEM receives its 128 rows.  Per SM the
+//            operand traffic per MMA cycle drops by a third and the ring is 1.5x deeper.
 // Work items are (group, n-tile, m-tile) with the m-tile fastest, enumerated on the
 // device from the dispatch offsets (the host never learns m_i), assigned round-robin
-// to one CTA per SM.  Neighbouring CTAs thus share the weight tile of an expert through
-// L2.  The shared expert is one more group whose rows are all T tokens.
+// to the resident CTAs (or CTA pairs).  Neighbouring units thus share the weight tile of
+// an expert through L2.  The shared expert is one more group whose rows are all T tokens.
 //
-// Roles (192 threads):
-//   warp 0      TMA producer: A rows [128 x 64] and two weight boxes [128 x 64] per
-//               stage, 128-byte swizzle, 4-stage ring guarded by full/empty mbarriers
-//   warp 1      TMEM allocation (512 columns = two 256-column accumulators) and, on one
-//               lane, the tcgen05.mma issue loop (M=128, N=256, K=16 per instruction)
+// Roles (192 threads per CTA):
+//   warp 0      TMA producer (128-byte swizzle), full/empty mbarrier ring
+//   warp 1      TMEM allocation (512 columns = two 256-column accumulators); one lane of
+//               the (leader) CTA issues the MMAs
 //   warps 2-5   epilogue: tcgen05.ld 32 columns at a time, SwiGLU or fp32 store
 // Every mbarrier wait is bounded (see ptx.cuh); a timeout sets the status word and the
-// CTA drains its in-flight copies and MMAs, frees TMEM and returns.
+// CTA drains what it can of its in-flight copies and MMAs, frees TMEM and returns.
 #include "moe_internal.h"
 #include "ptx.cuh"
 
 namespace moe {
 namespace {
 
-constexpr int BM = 128;
 constexpr int BK = 64;
-constexpr int kStages = 4;
-constexpr int kABytes = BM * BK * 2;
-constexpr int kBBoxBytes = 128 * BK * 2;
-constexpr int kStageBytes = kABytes + 2 * kBBoxBytes;
+constexpr int kBoxBytes = 128 * BK * 2;   // one [128 x 64] bf16 box
 constexpr int kAccCols = 256;
 constexpr int kTmemCols = 512;
 constexpr int kThreads = 192;
 constexpr int kMaxGroups = kMaxE + 1;
-constexpr uint32_t kIdesc = idesc_bf16_f32(128, 256);
 
 enum Mode { GATE_UP = 0, DOWN = 1 };
+
+template <bool PAIR>
+struct Cfg {
+  static constexpr int kStages = PAIR ? 6 : 4;
+  static constexpr int kStageBytes = PAIR ? 2 * kBoxBytes : 3 * kBoxBytes;
+  static constexpr int kTileM = PAIR ? 256 : 128;            // rows per work unit
+  static constexpr int kTxBytes = PAIR ? 4 * kBoxBytes : 3 * kBoxBytes;
+  static constexpr uint32_t kIdesc = idesc_bf16_f32(PAIR ? 256 : 128, 256);
+};
+// bytes that complete one stage: single CTA A + 2 B boxes (48 KB); pair: 2 x (A + B) (64 KB)
+static_assert(Cfg<false>::kTxBytes == 3 * kBoxBytes, "");
+static_assert(Cfg<true>::kTxBytes == 4 * kBoxBytes, "");
 
 struct TcParams {
   const int32_t* offsets;
@@ -54,10 +68,11 @@ struct TcParams {
   unsigned long long wait_limit_ns;
 };
 
+template <bool PAIR>
 struct __align__(1024) Smem {
-  uint8_t tiles[kStages][kStageBytes];
-  uint64_t full[kStages];
-  uint64_t empty[kStages];
+  uint8_t tiles[Cfg<PAIR>::kStages][Cfg<PAIR>::kStageBytes];
+  uint64_t full[Cfg<PAIR>::kStages];
+  uint64_t empty[Cfg<PAIR>::kStages];
   uint64_t tfull[2];
   uint64_t tempty[2];
   uint64_t drain;
@@ -74,20 +89,22 @@ struct TileInfo {
   int g, m0, n0, rows, row0;
 };
 
-__device__ __forceinline__ TileInfo decode_tile(const Smem& S, int tile, int n_tile) {
+template <bool PAIR>
+__device__ __forceinline__ TileInfo decode_tile(const Smem<PAIR>& S, int tile, int n_tile) {
   int lo = 0, hi = S.ngroups - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
     if (S.tile_start[mid] <= tile) lo = mid;
     else hi = mid - 1;
   }
+  constexpr int TM = Cfg<PAIR>::kTileM;
   TileInfo ti;
   ti.g = lo;
   ti.rows = S.grp_rows[lo];
   ti.row0 = S.grp_row0[lo];
-  const int mt = (ti.rows + BM - 1) / BM;
+  const int mt = (ti.rows + TM - 1) / TM;
   const int local = tile - S.tile_start[lo];
-  ti.m0 = (local % mt) * BM;
+  ti.m0 = (local % mt) * TM;
   ti.n0 = (local / mt) * n_tile;
   return ti;
 }
@@ -101,7 +118,7 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   return *reinterpret_cast<const uint32_t*>(&v);
 }
 
-template <int MODE>
+template <int MODE, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap mA,
                         const __grid_constant__ CUtensorMap mA_sh,
@@ -109,12 +126,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const __grid_constant__ CUtensorMap mB1,
                         const __grid_constant__ CUtensorMap mB0_sh,
                         const __grid_constant__ CUtensorMap mB1_sh, const TcParams p) {
+  using C = Cfg<PAIR>;
+  constexpr int kStages = C::kStages;
   extern __shared__ uint8_t smem_raw[];
-  Smem& S = *reinterpret_cast<Smem*>(
+  Smem<PAIR>& S = *reinterpret_cast<Smem<PAIR>*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int n_tiles_n = (p.N + p.n_tile - 1) / p.n_tile;
   const int nkb = (p.K + BK - 1) / BK;
+  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;   // 0 = leader
+  const int unit = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+  const int n_units = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
 
   // ---------------------------------------------------------------- set-up
   const int ngroups = p.E + (p.has_shared ? 1 : 0);
@@ -127,15 +149,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&S.tfull[b], 1);
-      mbar_init(&S.tempty[b], 128);
+      mbar_init(&S.tempty[b], PAIR ? 256 : 128);
     }
     mbar_init(&S.drain, 1);
     fence_mbar_init();
   }
   if (warp == 1) {
-    tmem_alloc(&S.tmem_base, kTmemCols);
-    tmem_relinquish();
+    if (PAIR) {
+      tmem_alloc_pair(&S.tmem_base, kTmemCols);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(&S.tmem_base, kTmemCols);
+      tmem_relinquish();
+    }
   }
+  constexpr int TM = C::kTileM;
   for (int g = tid; g < ngroups; g += kThreads) {
     int rows, row0;
     if (g < p.E) {
@@ -154,7 +182,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     S.grp_rows[g] = rows;
     S.grp_row0[g] = row0;
-    S.tile_start[g] = ((rows + BM - 1) / BM) * n_tiles_n;   // count, scanned below
+    S.tile_start[g] = ((rows + TM - 1) / TM) * n_tiles_n;   // count, scanned below
   }
   __syncthreads();
   if (warp == 0) {
@@ -178,10 +206,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
+  if (PAIR) cluster_sync();   // the peer's barriers exist before anyone signals them
   tc_fence_after();
   const uint32_t tmem_base = S.tmem_base;
   const int total = S.total_tiles;
   const volatile int* abort_flag = &S.abort_flag;
+  const unsigned long long lim = p.wait_limit_ns;
 
   if (warp == 0 && lane == 0) {
     // ---------------------------------------------------------------- TMA producer
@@ -197,18 +227,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t phase = 0;
     uint32_t issued_mask = 0, issued_parity = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-      const TileInfo ti = decode_tile(S, tile, p.n_tile);
+    for (int tile = unit; tile < total && ok; tile += n_units) {
+      const TileInfo ti = decode_tile<PAIR>(S, tile, p.n_tile);
       const bool sh = ti.g >= p.E;
       const CUtensorMap* a_map = sh ? &mA_sh : &mA;
-      const int ay = ti.row0 + ti.m0;
+      const int ay = ti.row0 + ti.m0 + (PAIR ? 128 * (int)rank : 0);
       for (int kb = 0; kb < nkb; ++kb) {
-        if (!mbar_wait(&S.empty[stage], phase ^ 1u, abort_flag, p.wait_limit_ns)) {
+        if (!mbar_wait(&S.empty[stage], phase ^ 1u, abort_flag, lim)) {
           ok = false;
           break;
         }
         uint8_t* st = S.tiles[stage];
-        if (p.test_hook == MOE_TEST_HOOK_WITHHOLD_LOAD && tile == (int)blockIdx.x && kb == 0) {
+        if (p.test_hook == MOE_TEST_HOOK_WITHHOLD_LOAD && tile == unit && kb == 0) {
           // test only: the first stage is never filled, so the MMA issuer's bounded wait
           // on it runs out and the CTA takes its timeout path
           if (++stage == kStages) {
@@ -217,27 +247,37 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           continue;
         }
-        mbar_arrive_expect_tx(&S.full[stage], kStageBytes);
-        tma_load_2d(st, a_map, &S.full[stage], kb * BK, ay);
-        if (MODE == GATE_UP) {
+        const int kx = kb * BK;
+        if (!PAIR) {
+          mbar_arrive_expect_tx(&S.full[stage], C::kTxBytes);
+          tma_load_2d(st, a_map, &S.full[stage], kx, ay);
+          const CUtensorMap* b0 = sh ? &mB0_sh : &mB0;
+          const CUtensorMap* b1 = (MODE == GATE_UP) ? (sh ? &mB1_sh : &mB1) : b0;
+          const int n1 = (MODE == GATE_UP) ? ti.n0 : ti.n0 + 128;
           if (sh) {
-            tma_load_2d(st + kABytes, &mB0_sh, &S.full[stage], kb * BK, ti.n0);
-            tma_load_2d(st + kABytes + kBBoxBytes, &mB1_sh, &S.full[stage], kb * BK, ti.n0);
+            tma_load_2d(st + kBoxBytes, b0, &S.full[stage], kx, ti.n0);
+            tma_load_2d(st + 2 * kBoxBytes, b1, &S.full[stage], kx, n1);
           } else {
-            tma_load_3d(st + kABytes, &mB0, &S.full[stage], kb * BK, ti.n0, ti.g);
-            tma_load_3d(st + kABytes + kBBoxBytes, &mB1, &S.full[stage], kb * BK, ti.n0,
-                        ti.g);
+            tma_load_3d(st + kBoxBytes, b0, &S.full[stage], kx, ti.n0, ti.g);
+            tma_load_3d(st + 2 * kBoxBytes, b1, &S.full[stage], kx, n1, ti.g);
           }
         } else {
-          if (sh) {
-            tma_load_2d(st + kABytes, &mB0_sh, &S.full[stage], kb * BK, ti.n0);
-            tma_load_2d(st + kABytes + kBBoxBytes, &mB0_sh, &S.full[stage], kb * BK,
-                        ti.n0 + 128);
+          // both CTAs' copies count on the leader's barrier; the leader expects all bytes
+          if (rank == 0) mbar_arrive_expect_tx(&S.full[stage], C::kTxBytes);
+          const uint32_t bar = mapa_shared(smem_u32(&S.full[stage]), 0);
+          tma_load_2d_pair(st, a_map, bar, kx, ay);
+          // weight half of this CTA: GATE_UP rank 0 = gate rows, rank 1 = up rows;
+          // DOWN rank r = output rows n0 + 128 r
+          const CUtensorMap* b;
+          int ny = ti.n0;
+          if (MODE == GATE_UP) {
+            b = rank == 0 ? (sh ? &mB0_sh : &mB0) : (sh ? &mB1_sh : &mB1);
           } else {
-            tma_load_3d(st + kABytes, &mB0, &S.full[stage], kb * BK, ti.n0, ti.g);
-            tma_load_3d(st + kABytes + kBBoxBytes, &mB0, &S.full[stage], kb * BK,
-                        ti.n0 + 128, ti.g);
+            b = sh ? &mB0_sh : &mB0;
+            ny += 128 * (int)rank;
           }
+          if (sh) tma_load_2d_pair(st + kBoxBytes, b, bar, kx, ny);
+          else tma_load_3d_pair(st + kBoxBytes, b, bar, kx, ny, ti.g);
         }
         issued_mask |= 1u << stage;
         issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
@@ -251,43 +291,50 @@ __global__ void __launch_bounds__(kThreads, 1)
       S.abort_flag = 1;
       set_status(p.status, MOE_ERR_TIMEOUT);
       // let every copy already issued land before the CTA's shared memory goes away
+      // (in a pair only the leader's barriers count the copies)
       const int zero = 0;
-      for (int s = 0; s < kStages; ++s)
-        if (issued_mask >> s & 1u)
-          mbar_wait(&S.full[s], issued_parity >> s & 1u, &zero, p.wait_limit_ns);
+      if (!PAIR || rank == 0)
+        for (int s = 0; s < kStages; ++s)
+          if (issued_mask >> s & 1u) mbar_wait(&S.full[s], issued_parity >> s & 1u, &zero, lim);
     }
-  } else if (warp == 1 && lane == 0) {
+  } else if (warp == 1 && lane == 0 && rank == 0) {
     // ---------------------------------------------------------------- MMA issuer
     int stage = 0, acc = 0;
     uint32_t phase = 0, acc_phase = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-      if (!mbar_wait(&S.tempty[acc], acc_phase ^ 1u, abort_flag, p.wait_limit_ns)) {
+    for (int tile = unit; tile < total && ok; tile += n_units) {
+      const bool got = PAIR ? mbar_wait_cluster(&S.tempty[acc], acc_phase ^ 1u, abort_flag, lim)
+                            : mbar_wait(&S.tempty[acc], acc_phase ^ 1u, abort_flag, lim);
+      if (!got) {
         ok = false;
         break;
       }
       tc_fence_after();
       const uint32_t d = tmem_base + acc * kAccCols;
       for (int kb = 0; kb < nkb; ++kb) {
-        if (!mbar_wait(&S.full[stage], phase, abort_flag, p.wait_limit_ns)) {
+        if (!mbar_wait(&S.full[stage], phase, abort_flag, lim)) {
           ok = false;
           break;
         }
         tc_fence_after();
         const uint32_t a_addr = smem_u32(S.tiles[stage]);
         const uint64_t adesc = sdesc_kmajor_sw128(a_addr);
-        const uint64_t bdesc = sdesc_kmajor_sw128(a_addr + kABytes);
+        const uint64_t bdesc = sdesc_kmajor_sw128(a_addr + kBoxBytes);
 #pragma unroll
-        for (int kk = 0; kk < BK / 16; ++kk)
-          umma_bf16(d, adesc + 2 * kk, bdesc + 2 * kk, kIdesc, (kb | kk) != 0);
-        umma_commit(&S.empty[stage]);
+        for (int kk = 0; kk < BK / 16; ++kk) {
+          if (PAIR) umma_bf16_pair(d, adesc + 2 * kk, bdesc + 2 * kk, C::kIdesc, (kb | kk) != 0);
+          else umma_bf16(d, adesc + 2 * kk, bdesc + 2 * kk, C::kIdesc, (kb | kk) != 0);
+        }
+        if (PAIR) umma_commit_pair_mc(&S.empty[stage], 0x3);
+        else umma_commit(&S.empty[stage]);
         if (++stage == kStages) {
           stage = 0;
           phase ^= 1u;
         }
       }
       if (!ok) break;
-      umma_commit(&S.tfull[acc]);
+      if (PAIR) umma_commit_pair_mc(&S.tfull[acc], 0x3);
+      else umma_commit(&S.tfull[acc]);
       if (++acc == 2) {
         acc = 0;
         acc_phase ^= 1u;
@@ -297,19 +344,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       S.abort_flag = 1;
       set_status(p.status, MOE_ERR_TIMEOUT);
       // wait for the MMAs already issued before TMEM is released
-      umma_commit(&S.drain);
+      if (PAIR) umma_commit_pair(&S.drain);
+      else umma_commit(&S.drain);
       const int zero = 0;
-      mbar_wait(&S.drain, 0, &zero, p.wait_limit_ns);
+      mbar_wait(&S.drain, 0, &zero, lim);
     }
   } else if (warp >= 2) {
     // ---------------------------------------------------------------- epilogue
     const int q = warp & 3;                 // TMEM lane quadrant this warp may access
-    const int r_in_tile = q * 32 + lane;
+    const int r_in_tile = (PAIR ? 128 * (int)rank : 0) + q * 32 + lane;
+    const uint32_t tempty_leader =
+        PAIR ? mapa_shared(smem_u32(&S.tempty[0]), 0) : 0u;
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
-      const TileInfo ti = decode_tile(S, tile, p.n_tile);
-      const bool got = mbar_wait(&S.tfull[acc], acc_phase, abort_flag, p.wait_limit_ns);
+    for (int tile = unit; tile < total; tile += n_units) {
+      const TileInfo ti = decode_tile<PAIR>(S, tile, p.n_tile);
+      const bool got = mbar_wait(&S.tfull[acc], acc_phase, abort_flag, lim);
       if (!__all_sync(0xffffffffu, got)) {
         S.abort_flag = 1;
         set_status(p.status, MOE_ERR_TIMEOUT);
@@ -360,7 +410,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       tc_fence_before();
-      mbar_arrive(&S.tempty[acc]);
+      if (PAIR) mbar_arrive_cluster(tempty_leader + acc * (uint32_t)sizeof(uint64_t));
+      else mbar_arrive(&S.tempty[acc]);
       if (++acc == 2) {
         acc = 0;
         acc_phase ^= 1u;
@@ -371,18 +422,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ---------------------------------------------------------------- tear-down
   tc_fence_before();
   __syncthreads();
+  if (PAIR) cluster_sync();   // no MMA, copy or arrival targets either CTA any more
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
-    tmem_dealloc(tmem_base, kTmemCols);
+    if (PAIR) tmem_dealloc_pair(tmem_base, kTmemCols);
+    else tmem_dealloc(tmem_base, kTmemCols);
   }
 }
 
 bool encode_2d(EncodeTiledFn enc, CUtensorMap* m, const void* base, uint64_t inner,
-               uint64_t outer, uint32_t box_outer) {
+               uint64_t outer) {
   const cuuint64_t dims[2] = {inner, outer};
   const cuuint64_t strides[1] = {inner * 2};
-  const cuuint32_t box[2] = {BK, box_outer};
+  const cuuint32_t box[2] = {BK, 128};
   const cuuint32_t estr[2] = {1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
              box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -402,7 +455,32 @@ bool encode_3d(EncodeTiledFn enc, CUtensorMap* m, const void* base, uint64_t inn
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int MODE>
+// Number of CTA pairs that can be resident at once (persistent grid), cached per process.
+int max_pairs(const void* fn, size_t smem, int num_sms) {
+  static int cached[2] = {0, 0};
+  const int slot = fn == reinterpret_cast<const void*>(grouped_gemm_kernel<GATE_UP, true>) ? 0 : 1;
+  if (cached[slot]) return cached[slot];
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(num_sms & ~1);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, fn, &cfg) != cudaSuccess || n <= 0) {
+    cudaGetLastError();
+    n = num_sms / 2;
+  }
+  cached[slot] = n;
+  return n;
+}
+
+template <int MODE, bool PAIR>
 cudaError_t launch_tc(const ExpertArgs& a, EncodeTiledFn enc, bool* encode_failed,
                       cudaStream_t s) {
   *encode_failed = false;
@@ -414,19 +492,18 @@ cudaError_t launch_tc(const ExpertArgs& a, EncodeTiledFn enc, bool* encode_faile
   CUtensorMap mA, mA_sh, mB0, mB1, mB0_sh, mB1_sh;
   bool ok = true;
   if (MODE == GATE_UP) {
-    ok &= encode_2d(enc, &mA, a.Xperm, K, Tk, BM);
-    ok &= encode_2d(enc, &mA_sh, a.has_shared ? a.X : a.Xperm, K,
-                    a.has_shared ? a.T : Tk, BM);
+    ok &= encode_2d(enc, &mA, a.Xperm, K, Tk);
+    ok &= encode_2d(enc, &mA_sh, a.has_shared ? a.X : a.Xperm, K, a.has_shared ? a.T : Tk);
     ok &= encode_3d(enc, &mB0, a.W_gate, K, N, a.E);
     ok &= encode_3d(enc, &mB1, a.W_up, K, N, a.E);
-    ok &= encode_2d(enc, &mB0_sh, a.has_shared ? a.Ws_gate : a.W_gate, K, N, 128);
-    ok &= encode_2d(enc, &mB1_sh, a.has_shared ? a.Ws_up : a.W_up, K, N, 128);
+    ok &= encode_2d(enc, &mB0_sh, a.has_shared ? a.Ws_gate : a.W_gate, K, N);
+    ok &= encode_2d(enc, &mB1_sh, a.has_shared ? a.Ws_up : a.W_up, K, N);
   } else {
-    ok &= encode_2d(enc, &mA, a.h, K, h_rows, BM);
+    ok &= encode_2d(enc, &mA, a.h, K, h_rows);
     mA_sh = mA;
     ok &= encode_3d(enc, &mB0, a.W_down, K, N, a.E);
     mB1 = mB0;
-    ok &= encode_2d(enc, &mB0_sh, a.has_shared ? a.Ws_down : a.W_down, K, N, 128);
+    ok &= encode_2d(enc, &mB0_sh, a.has_shared ? a.Ws_down : a.W_down, K, N);
     mB1_sh = mB0_sh;
   }
   if (!ok) {
@@ -449,32 +526,57 @@ cudaError_t launch_tc(const ExpertArgs& a, EncodeTiledFn enc, bool* encode_faile
   p.test_hook = a.test_hook;
   p.wait_limit_ns = a.wait_limit_ns;
 
+  constexpr int TM = Cfg<PAIR>::kTileM;
   const int n_tiles_n = (N + n_tile - 1) / n_tile;
   const long long m_tiles_bound =
-      (Tk + BM - 1) / BM + a.E + (a.has_shared ? (a.T + BM - 1) / BM : 0);
+      (Tk + TM - 1) / TM + a.E + (a.has_shared ? (a.T + TM - 1) / TM : 0);
   const long long tiles_bound = m_tiles_bound * n_tiles_n;
-  const int grid = (int)(tiles_bound < a.num_sms ? (tiles_bound > 0 ? tiles_bound : 1)
-                                                 : a.num_sms);
-  const size_t smem = sizeof(Smem) + 1024;
-  cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<MODE>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)smem);
+  const size_t smem = sizeof(Smem<PAIR>) + 1024;
+  auto* fn = grouped_gemm_kernel<MODE, PAIR>;
+  cudaError_t e =
+      cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  grouped_gemm_kernel<MODE><<<grid, kThreads, smem, s>>>(mA, mA_sh, mB0, mB1, mB0_sh,
-                                                         mB1_sh, p);
-  return cudaGetLastError();
+  if (!PAIR) {
+    const int grid = (int)(tiles_bound < a.num_sms ? (tiles_bound > 0 ? tiles_bound : 1)
+                                                   : a.num_sms);
+    fn<<<grid, kThreads, smem, s>>>(mA, mA_sh, mB0, mB1, mB0_sh, mB1_sh, p);
+    return cudaGetLastError();
+  }
+  const int pairs_max = max_pairs(reinterpret_cast<const void*>(fn), smem, a.num_sms);
+  const int pairs = (int)(tiles_bound < pairs_max ? (tiles_bound > 0 ? tiles_bound : 1)
+                                                  : pairs_max);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * pairs);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, fn, mA, mA_sh, mB0, mB1, mB0_sh, mB1_sh, p);
+}
+
+// CTA pairs pay off once the average expert has enough rows to fill 256-row tiles.
+bool use_pairs(const ExpertArgs& a) {
+  return (long long)a.T * a.k >= 128LL * a.E && a.num_sms >= 2;
 }
 
 }  // namespace
 
 cudaError_t launch_expert_gate_up_tc(const ExpertArgs& a, EncodeTiledFn enc,
                                      bool* encode_failed, cudaStream_t s) {
-  return launch_tc<GATE_UP>(a, enc, encode_failed, s);
+  return use_pairs(a) ? launch_tc<GATE_UP, true>(a, enc, encode_failed, s)
+                      : launch_tc<GATE_UP, false>(a, enc, encode_failed, s);
 }
 
 cudaError_t launch_expert_down_tc(const ExpertArgs& a, EncodeTiledFn enc,
                                   bool* encode_failed, cudaStream_t s) {
-  return launch_tc<DOWN>(a, enc, encode_failed, s);
+  return use_pairs(a) ? launch_tc<DOWN, true>(a, enc, encode_failed, s)
+                      : launch_tc<DOWN, false>(a, enc, encode_failed, s);
 }
 
 }  // namespace moe

@@ -33,7 +33,7 @@ from sparse_top_routing_router_b300.inputs import make_inputs, token_subset  # n
 
 METRIC = "MoE-layer fwd tokens/s on 1 B300; % of bf16 tensor peak / % of HBM roofline"
 DEFAULT_CONFIG = K.MIXTRAL.name
-PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "expert_gate_up_traffic.json")
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "expert_gate_up_traffic.txt")
 KERNEL_SRC = os.path.join(ROOT, "sparse_top_routing_router_b300", "csrc", "expert_tc.cu")
 
 
@@ -65,47 +65,68 @@ def peaks() -> dict:
 
 
 class ClockSampler:
-    """nvidia-smi sampled every 200 ms while the timed region runs."""
+    """nvidia-smi sampled every 100 ms; only samples stamped inside the timed region's
+    wall-clock window are kept."""
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, gpu_index: int):
         self.idx = gpu_index
         self.proc = None
+        self.t0 = self.t1 = None
 
     def start(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
 
+    def mark(self, begin: bool):
+        if begin:
+            self.t0 = time.time()
+        else:
+            self.t1 = time.time()
+
     def stop(self) -> dict:
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        time.sleep(0.25)
+        time.sleep(0.15)
         self.proc.terminate()
         out, _ = self.proc.communicate(timeout=10)
-        sm, mx, reasons = [], [], set()
+        import datetime
+        sm, mx, pw, reasons, n_all = [], [], [], set(), 0
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for line in out.strip().splitlines():
             f = [x.strip() for x in line.split(",")]
-            if len(f) < 9:
+            if len(f) < 10:
                 continue
+            n_all += 1
             try:
-                sm.append(float(f[1]))
-                mx.append(float(f[2]))
+                ts = datetime.datetime.strptime(f[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                sm_v, mx_v = float(f[2]), float(f[3])
             except ValueError:
                 continue
-            for n, v in zip(names, f[5:9]):
+            if self.t0 is not None and not (self.t0 - 0.05 <= ts <= self.t1 + 0.05):
+                continue
+            sm.append(sm_v)
+            mx.append(mx_v)
+            try:
+                pw.append(float(f[4]))
+            except ValueError:
+                pass
+            for n, v in zip(names, f[6:10]):
                 if v.lower() == "active":
                     reasons.add(n)
         return {"sm_mhz": statistics.median(sm) if sm else None,
-                "sm_max_mhz": max(mx) if mx else None, "samples": len(sm),
+                "sm_max_mhz": max(mx) if mx else None,
+                "power_w_median": statistics.median(pw) if pw else None,
+                "samples": len(sm), "samples_total": n_all,
+                "window_s": (self.t1 - self.t0) if self.t0 else None,
                 "reasons": sorted(reasons)}
 
 
@@ -229,15 +250,17 @@ def run_gpu(args, cfg, cf):
     layer.ctx.trace_read()
     clocks = ClockSampler(local)
     clocks.start()
-    time.sleep(0.3)
+    time.sleep(0.5)
     barrier()
     torch.cuda.synchronize()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks.mark(True)
     ev0.record(stream)
     for _ in range(args.steps):
         layer.forward(X)
     ev1.record(stream)
     torch.cuda.synchronize()
+    clocks.mark(False)
     barrier()
     clk = clocks.stop()
     ms = ev0.elapsed_time(ev1)
@@ -250,19 +273,17 @@ def run_gpu(args, cfg, cf):
     ms_step = ms / args.steps
     value = world * cfg.T * args.steps / (ms / 1e3)
 
-    # ---- end to end: pinned host X -> device, forward, device Y -> pinned host
+    # ---- end to end: pinned host X -> device, forward, bf16 Y -> pinned host, the copies
+    # of neighbouring steps overlapped with compute (MoELayer.host_pipeline)
     Xh = torch.empty(X.shape, dtype=X.dtype, pin_memory=True)
     Xh.copy_(X)
-    Yh = torch.empty(layer.Y.shape, dtype=layer.Y.dtype, pin_memory=True)
-    Xd = torch.empty_like(X)
-    for _ in range(2):
-        layer.forward_host(Xh, Yh, Xd)
+    Yh = [torch.empty(cfg.T, cfg.H, dtype=torch.bfloat16, pin_memory=True) for _ in range(2)]
+    layer.host_pipeline(Xh, Yh, 4, stream)
     torch.cuda.synchronize()
     barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(args.steps):
-        layer.forward_host(Xh, Yh, Xd)
+    layer.host_pipeline(Xh, Yh, args.steps, stream)
     e1.record(stream)
     torch.cuda.synchronize()
     barrier()
@@ -282,17 +303,47 @@ def run_gpu(args, cfg, cf):
 
     pk = peaks()
     n_gu, ms_gu = kern["expert_gate_up"]
+    n_dn, ms_dn = kern["expert_down"]
     gu_ms = ms_gu / max(n_gu, 1)
-    gu_flops = 2.0 * (R + (cfg.T if cfg.shared else 0)) * cfg.H * 2 * cfg.I
-    achieved = gu_flops / (gu_ms / 1e3) / 1e12
-    prof = traffic_from_profile()
-    roofline = {"kernel": "expert_gate_up", "bound": "tensor", "achieved": achieved,
-                "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
-                "frac": achieved / pk["bf16_tflops"],
-                "peak_source": pk["source"] + " bf16 burst (MEASURED_PEAKS.json)"
-                if pk["source"] == "measured" else "fallback bf16 burst",
-                "traffic": prof["dram_bytes_per_launch"] if prof else None,
-                "algorithmic_flops_per_launch": gu_flops, "avg_launch_ms": gu_ms}
+    dn_ms = ms_dn / max(n_dn, 1)
+    rows = R + (cfg.T if cfg.shared else 0)
+    gu_flops = 2.0 * rows * cfg.H * 2 * cfg.I
+    dn_flops = 2.0 * rows * cfg.I * cfg.H
+    elt = 2 if cfg.dtype == "bf16" else 4
+    n_touched = int((layer.counts > 0).sum().item()) + (1 if cfg.shared else 0)
+    w_touched = n_touched * 3 * cfg.H * cfg.I * elt
+    # algorithmic bytes of the gate/up launch: its touched weights once, A rows in, h out
+    gu_bytes = n_touched * 2 * cfg.H * cfg.I * elt + rows * cfg.H * elt + rows * cfg.I * 2
+    prof = traffic_from_profile() if cfg.name == K.MIXTRAL.name else None
+    src = (pk["source"] + " (MEASURED_PEAKS.json, burst)") if pk["source"] == "measured" \
+        else "fallback"
+    tensor_bound = R >= 128 * cfg.E     # rows per expert fill the 128/256-row tiles
+    if tensor_bound:
+        achieved = gu_flops / (gu_ms / 1e3) / 1e12
+        roofline = {"kernel": "expert_gate_up", "bound": "tensor", "achieved": achieved,
+                    "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+                    "frac": achieved / pk["bf16_tflops"], "peak_source": src,
+                    "traffic": prof["dram_bytes_per_launch"] if prof else None,
+                    "algorithmic_flops_per_launch": gu_flops, "avg_launch_ms": gu_ms}
+    else:
+        achieved = gu_bytes / (gu_ms / 1e3) / 1e9
+        roofline = {"kernel": "expert_gate_up", "bound": "hbm", "achieved": achieved,
+                    "peak": pk["hbm_gbs"], "unit": "GB/s",
+                    "frac": achieved / pk["hbm_gbs"], "peak_source": src,
+                    "traffic": None, "algorithmic_bytes_per_launch": gu_bytes,
+                    "avg_launch_ms": gu_ms}
+    gemm_tflops = (gu_flops + dn_flops) / ((gu_ms + dn_ms) / 1e3) / 1e12
+    extra = {
+        "expert_gemms": {"tflops": gemm_tflops, "frac_of_bf16_peak": gemm_tflops /
+                         pk["bf16_tflops"], "ms": gu_ms + dn_ms},
+        "touched_experts": n_touched,
+        "hbm_on_touched_weights": {
+            "bytes_per_step": w_touched,
+            "gbs_whole_step": w_touched / (ms_step / 1e3) / 1e9,
+            "frac_whole_step": w_touched / (ms_step / 1e3) / 1e9 / pk["hbm_gbs"],
+            "gbs_expert_gemms": w_touched / ((gu_ms + dn_ms) / 1e3) / 1e9,
+            "frac_expert_gemms": w_touched / ((gu_ms + dn_ms) / 1e3) / 1e9 / pk["hbm_gbs"]},
+    }
     launches = sum(n for n, _ in kern.values())
     layer_flops = cfg.flops(R)
     kernels = {k: {"launches": n, "ms_per_step": t / args.steps,
@@ -313,8 +364,11 @@ def run_gpu(args, cfg, cf):
         "roofline": roofline,
         "e2e": {"value": world * cfg.T * args.steps / (ms_e2e / 1e3), "unit": "tokens/s",
                 "h2d_bytes_per_step": X.numel() * X.element_size(),
-                "d2h_bytes_per_step": layer.Y.numel() * layer.Y.element_size()},
+                "d2h_bytes_per_step": Yh[0].numel() * Yh[0].element_size(),
+                "how": "pinned host X -> device, forward, bf16 Y -> pinned host every step; "
+                       "copies on two copy streams overlap the neighbouring steps' compute"},
         "gpu_launches": launches,
+        **extra,
         "kernels": kernels,
         "clocks": clk,
     }
@@ -333,8 +387,8 @@ def run_gpu(args, cfg, cf):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--config", default=DEFAULT_CONFIG, choices=sorted(K.BY_NAME))
     ap.add_argument("--capacity-factor", type=float, default=None)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])

@@ -17,8 +17,10 @@
  * Conventions for every call
  *  - Pointers are DEVICE pointers unless stated.  The caller owns every buffer.  The
  *    library allocates no device memory: scratch lives in a caller-provided workspace
- *    of moe_workspace_bytes() bytes whose first 256 bytes hold a device status word and
- *    must be zeroed once (moe_workspace_init) before first use.
+ *    of moe_workspace_bytes() bytes whose first 256 bytes hold a device status word
+ *    (int32 at byte 0) and must be zeroed once (moe_workspace_init) before first use.
+ *    The int32 at byte 4 counts the rows the last moe_router_topk call re-decided from
+ *    exact dot products (a diagnostic).
  *  - Every call is asynchronous on `stream`, performs no host synchronisation (except
  *    moe_get_device_status and moe_ctx_trace_read, which say so) and returns an int
  *    status: MOE_OK (0) or a negative MOE_ERR_*.  Argument checks run before anything is
@@ -133,6 +135,7 @@ int moe_router_topk(moe_ctx* ctx, const moe_router_desc* d, const void* X,
  *              offsets[E] = R, the kept slot count
  *   row_of_slot[T*k] int32 out: permuted row of slot t*k+j, or -1 if dropped
  *   slot_of_row[T*k] int32 out: rows [0, R) hold the inverse; rows >= R untouched
+ *   H          hidden size, >= 1 even without a gather (it sizes the workspace layout)
  *   X, Xperm   nullable pair: when both are given, Xperm[row] = X[slot / k] for every
  *              kept row (x_dtype element type, Xperm has T*k rows)
  * Rows are ordered by (expert ascending, token ascending). */

@@ -195,9 +195,11 @@ def moe_router_topk(ctx: Context, X, Wg, k: int, score: int, renorm: bool, topk_
 
 
 def moe_dispatch(ctx: Context, topk_idx, E: int, capacity: int, counts, offsets,
-                 row_of_slot, slot_of_row, ws, X=None, Xperm=None, stream=None) -> None:
+                 row_of_slot, slot_of_row, ws, X=None, Xperm=None, stream=None,
+                 H: Optional[int] = None) -> None:
     T, k = topk_idx.shape
-    H = X.shape[1] if X is not None else 0
+    if H is None:
+        H = X.shape[1] if X is not None else 0
     xd = x_dtype_code(X) if X is not None else MOE_DTYPE_BF16
     _check("moe_dispatch", lib().moe_dispatch(
         ctx.handle, T, k, E, H, xd, capacity, _p(topk_idx), _p(X), _p(counts), _p(offsets),

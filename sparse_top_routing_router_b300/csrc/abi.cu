@@ -17,6 +17,11 @@ using namespace moe;
 
 namespace {
 constexpr unsigned long long kWaitLimitDefaultNs = 2000000000ull;
+// Bounds on the router's fp32 logit error, per unit of max(1, max|l|) * sqrt(H/1024):
+// CUDA-core logits sum 32-term fp32 blocks with compensation; tensor-core logits
+// accumulate the exact bf16 x bf16 products in the MMA's fp32 accumulator.
+constexpr float kRouterEpsCuda = 1.9073486328125e-06f;     // 2^-19
+constexpr float kRouterEpsTensor = 1.52587890625e-05f;     // 2^-16
 }
 
 struct moe_ctx {
@@ -227,7 +232,10 @@ int moe_router_topk(moe_ctx* ctx, const moe_router_desc* d, const void* X, const
   if (!aligned16(X) || !aligned16(Wg) || !aligned16(ws))
     return fail(MOE_ERR_INVALID_ARG, "X, Wg and ws must be 16-byte aligned");
   const WsLayout L = ws_layout(d->T, d->H, d->E, 0, d->k, d->x_dtype, 0);
-  if (ws_bytes < L.chunk_counts) return fail(MOE_ERR_INVALID_ARG, "workspace too small");
+  // the tensor-core router also needs the W_g pieces; the fp32 CUDA-core one does not
+  const bool use_tc = d->x_dtype == MOE_DTYPE_BF16 && d->E >= 32 && d->E % 32 == 0 &&
+                      d->H % 64 == 0 && d->T >= 256 && ws_bytes >= L.chunk_counts;
+  if (ws_bytes < L.wsplit) return fail(MOE_ERR_INVALID_ARG, "workspace too small");
   if ((r = check_ctx(ctx))) return r;
   cudaStream_t s = (cudaStream_t)stream;
   cudaError_t e;
@@ -246,14 +254,45 @@ int moe_router_topk(moe_ctx* ctx, const moe_router_desc* d, const void* X, const
   a.Wg = Wg;
   a.bias = bias;
   a.logit_bias = logit_bias;
-  a.logits = reinterpret_cast<float*>(static_cast<char*>(ws) + L.logits);
+  a.logits = reinterpret_cast<float2*>(static_cast<char*>(ws) + L.logits);
+  a.num_sms = ctx->num_sms;
+  a.wait_limit_ns = ctx->wait_limit_ns;
+  a.wsplit = use_tc ? reinterpret_cast<__nv_bfloat16*>(static_cast<char*>(ws) + L.wsplit)
+                    : nullptr;
+  if (use_tc) {
+    // every slice at most kRouterTcMaxK products long; more slices if the grid is thin
+    const int tiles = ((d->T + 127) / 128) * ((d->E + 255) / 256);
+    const int nkb = 3 * d->H / 64;
+    const int need = (nkb + kRouterTcMaxK / 64 - 1) / (kRouterTcMaxK / 64);
+    int sp = (3 * ctx->num_sms / 2) / tiles;
+    const int cap = router_split_cap(d->T, d->H);
+    sp = sp < need ? need : sp;
+    sp = sp > cap ? cap : sp;
+    a.splits = sp > nkb ? nkb : sp;
+    a.eps_rel = kRouterEpsTensor;
+  } else {
+    a.splits = router_splits(d->T, d->H);
+    a.eps_rel = kRouterEpsCuda;
+  }
   a.idx = topk_idx;
   a.gate = topk_gate;
   a.gap = key_gap;
   a.colsum = prob_colsum;
   a.status = static_cast<int*>(ws);
-  if ((e = traced(ctx, MOE_K_ROUTER_LOGITS, s, [&] { return launch_router_logits(a, s); })))
+  a.refined = static_cast<int*>(ws) + 1;
+  if ((e = cudaMemsetAsync(a.refined, 0, sizeof(int), s))) return cuda_fail(e, "cudaMemsetAsync");
+  if (use_tc) {
+    bool bad = false;
+    e = traced(ctx, MOE_K_ROUTER_LOGITS, s, [&] {
+      cudaError_t r = launch_router_split(a, s);
+      return r != cudaSuccess ? r : launch_router_tc(a, ctx->encode, &bad, s);
+    });
+    if (bad) return fail(MOE_ERR_INVALID_ARG, "tensor map encoding failed (router)");
+    if (e) return cuda_fail(e, "router_logits launch");
+  } else if ((e = traced(ctx, MOE_K_ROUTER_LOGITS, s,
+                         [&] { return launch_router_logits(a, s); }))) {
     return cuda_fail(e, "router_logits launch");
+  }
   if ((e = traced(ctx, MOE_K_ROUTER_SELECT, s, [&] { return launch_router_select(a, s); })))
     return cuda_fail(e, "router_select launch");
   return ok();
@@ -266,6 +305,7 @@ int moe_dispatch(moe_ctx* ctx, int T, int k, int E, int H, int x_dtype, int capa
   int r = check_shape(T, E, k);
   if (r) return r;
   if (!counts || !offsets || !ws) return fail(MOE_ERR_INVALID_ARG, "counts/offsets/ws null");
+  if (H < 1) return fail(MOE_ERR_INVALID_ARG, "H = %d (it also sizes the workspace layout)", H);
   if (T > 0 && (!topk_idx || !row_of_slot || !slot_of_row))
     return fail(MOE_ERR_INVALID_ARG, "topk_idx/row_of_slot/slot_of_row null");
   if ((X == nullptr) != (Xperm == nullptr))

@@ -60,39 +60,60 @@ __global__ void __launch_bounds__(256) combine_kernel(CombineArgs a) {
   }
 }
 
+// One thread per expert, ceil(E/32) warps: warp-shuffle sums, then one cross-warp pass.
 __global__ void __launch_bounds__(kMaxE) balance_stats_kernel(StatsArgs a) {
-  __shared__ double red[kMaxE];
-  const int e = threadIdx.x;
+  __shared__ double part[kMaxE / 32][3];
+  __shared__ double s_mean;
+  const int e = threadIdx.x, lane = e & 31, w = e >> 5, nw = blockDim.x >> 5;
   const double slots = (double)a.T * a.k;
   const bool in = e < a.E;
-  const double m = in ? (double)a.counts[e] : 0.0;
-  const double f = (in && slots > 0) ? m / slots : 0.0;
-  const double p = (in && a.T > 0) ? a.colsum[e] / a.T : 0.0;
+  double m = 0.0, f = 0.0, p = 0.0, fp = 0.0, ent = 0.0;
   if (in) {
+    m = (double)a.counts[e];
+    if (slots > 0) f = m / slots;
+    if (a.T > 0) p = a.colsum[e] / a.T;
     a.f[e] = f;
     a.p[e] = p;
+    fp = f * p;
+    if (f > 0) ent = -f * log(f);
   }
-  auto block_sum = [&](double v) -> double {
-    red[e] = v;
-    __syncthreads();
-    for (int s = kMaxE / 2; s > 0; s >>= 1) {
-      if (e < s) red[e] += red[e + s];
-      __syncthreads();
-    }
-    const double r = red[0];
-    __syncthreads();
-    return r;
+  auto warp_sum = [](double v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
   };
-  const double sum_fp = block_sum(f * p);
-  const double sum_m = block_sum(m);
-  const double mean = a.E > 0 ? sum_m / a.E : 0.0;
-  const double sq = block_sum(in ? (m - mean) * (m - mean) : 0.0);
-  const double ent = block_sum(f > 0 ? -f * log(f) : 0.0);
+  fp = warp_sum(fp);
+  const double msum = warp_sum(m);
+  ent = warp_sum(ent);
+  if (lane == 0) {
+    part[w][0] = fp;
+    part[w][1] = msum;
+    part[w][2] = ent;
+  }
+  __syncthreads();
   if (e == 0) {
-    a.out[0] = a.alpha * a.E * sum_fp;
+    double t = 0.0;
+    for (int q = 0; q < nw; ++q) t += part[q][1];
+    s_mean = a.E > 0 ? t / a.E : 0.0;
+  }
+  __syncthreads();
+  const double mean = s_mean;
+  double sq = in ? (m - mean) * (m - mean) : 0.0;
+  sq = warp_sum(sq);
+  __syncthreads();
+  if (lane == 0) part[w][1] = sq;
+  __syncthreads();
+  if (e == 0) {
+    double sfp = 0.0, ssq = 0.0, sent = 0.0;
+    for (int q = 0; q < nw; ++q) {
+      sfp += part[q][0];
+      ssq += part[q][1];
+      sent += part[q][2];
+    }
+    a.out[0] = a.alpha * a.E * sfp;
     a.out[1] = (a.offsets && slots > 0) ? (slots - (double)a.offsets[a.E]) / slots : 0.0;
-    a.out[2] = mean > 0 ? sqrt(sq / a.E) / mean : 0.0;
-    a.out[3] = ent;
+    a.out[2] = mean > 0 ? sqrt(ssq / a.E) / mean : 0.0;
+    a.out[3] = sent;
   }
 }
 
@@ -104,7 +125,7 @@ cudaError_t launch_combine(const CombineArgs& a, cudaStream_t s) {
 }
 
 cudaError_t launch_balance_stats(const StatsArgs& a, cudaStream_t s) {
-  balance_stats_kernel<<<1, kMaxE, 0, s>>>(a);
+  balance_stats_kernel<<<1, 32 * ((a.E + 31) / 32), 0, s>>>(a);
   return cudaGetLastError();
 }
 

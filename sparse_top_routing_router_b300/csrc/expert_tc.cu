@@ -40,7 +40,7 @@ constexpr int kTmemCols = 512;
 constexpr int kThreads = 192;
 constexpr int kMaxGroups = kMaxE + 1;
 
-enum Mode { GATE_UP = 0, DOWN = 1 };
+enum Mode { GATE_UP = 0, DOWN = 1, ROUTER = 2 };
 
 template <bool PAIR>
 struct Cfg {
@@ -66,6 +66,10 @@ struct TcParams {
   int* status;
   int test_hook;
   unsigned long long wait_limit_ns;
+  // ROUTER: split-K factor, period of A's reduction coordinate, partial-logit output
+  int splits;
+  int a_kmod;
+  float2* logits;
 };
 
 template <bool PAIR>
@@ -86,11 +90,12 @@ struct __align__(1024) Smem {
 };
 
 struct TileInfo {
-  int g, m0, n0, rows, row0;
+  int g, m0, n0, rows, row0, z;
 };
 
 template <bool PAIR>
-__device__ __forceinline__ TileInfo decode_tile(const Smem<PAIR>& S, int tile, int n_tile) {
+__device__ __forceinline__ TileInfo decode_tile(const Smem<PAIR>& S, int tile, int n_tile,
+                                                int n_tiles_n) {
   int lo = 0, hi = S.ngroups - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
@@ -105,7 +110,9 @@ __device__ __forceinline__ TileInfo decode_tile(const Smem<PAIR>& S, int tile, i
   const int mt = (ti.rows + TM - 1) / TM;
   const int local = tile - S.tile_start[lo];
   ti.m0 = (local % mt) * TM;
-  ti.n0 = (local / mt) * n_tile;
+  const int rest = local / mt;                 // n-tile, then split-K slice (router)
+  ti.n0 = (rest % n_tiles_n) * n_tile;
+  ti.z = rest / n_tiles_n;
   return ti;
 }
 
@@ -139,7 +146,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n_units = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
 
   // ---------------------------------------------------------------- set-up
-  const int ngroups = p.E + (p.has_shared ? 1 : 0);
+  const int ngroups = (MODE == ROUTER) ? 1 : p.E + (p.has_shared ? 1 : 0);
   if (tid == 0) {
     S.ngroups = ngroups;
     S.abort_flag = 0;
@@ -166,7 +173,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int TM = C::kTileM;
   for (int g = tid; g < ngroups; g += kThreads) {
     int rows, row0;
-    if (g < p.E) {
+    if (MODE == ROUTER) {
+      rows = p.T;
+      row0 = 0;
+    } else if (g < p.E) {
       const int a = p.offsets[g], b = p.offsets[g + 1];
       if (a < 0 || b < a || b > p.Tk) {
         set_status(p.status, MOE_ERR_DEVICE_INDEX);
@@ -182,7 +192,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     S.grp_rows[g] = rows;
     S.grp_row0[g] = row0;
-    S.tile_start[g] = ((rows + TM - 1) / TM) * n_tiles_n;   // count, scanned below
+    S.tile_start[g] = ((rows + TM - 1) / TM) * n_tiles_n *
+                      (MODE == ROUTER ? p.splits : 1);     // count, scanned below
   }
   __syncthreads();
   if (warp == 0) {
@@ -228,17 +239,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t issued_mask = 0, issued_parity = 0;
     bool ok = true;
     for (int tile = unit; tile < total && ok; tile += n_units) {
-      const TileInfo ti = decode_tile<PAIR>(S, tile, p.n_tile);
-      const bool sh = ti.g >= p.E;
+      const TileInfo ti = decode_tile<PAIR>(S, tile, p.n_tile, n_tiles_n);
+      const bool sh = (MODE == ROUTER) || ti.g >= p.E;
       const CUtensorMap* a_map = sh ? &mA_sh : &mA;
       const int ay = ti.row0 + ti.m0 + (PAIR ? 128 * (int)rank : 0);
-      for (int kb = 0; kb < nkb; ++kb) {
+      const int kb_lo = (MODE == ROUTER) ? (int)((long long)nkb * ti.z / p.splits) : 0;
+      const int kb_hi = (MODE == ROUTER) ? (int)((long long)nkb * (ti.z + 1) / p.splits) : nkb;
+      for (int kb = kb_lo; kb < kb_hi; ++kb) {
         if (!mbar_wait(&S.empty[stage], phase ^ 1u, abort_flag, lim)) {
           ok = false;
           break;
         }
         uint8_t* st = S.tiles[stage];
-        if (p.test_hook == MOE_TEST_HOOK_WITHHOLD_LOAD && tile == unit && kb == 0) {
+        if (p.test_hook == MOE_TEST_HOOK_WITHHOLD_LOAD && tile == unit && kb == kb_lo) {
           // test only: the first stage is never filled, so the MMA issuer's bounded wait
           // on it runs out and the CTA takes its timeout path
           if (++stage == kStages) {
@@ -250,7 +263,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int kx = kb * BK;
         if (!PAIR) {
           mbar_arrive_expect_tx(&S.full[stage], C::kTxBytes);
-          tma_load_2d(st, a_map, &S.full[stage], kx, ay);
+          tma_load_2d(st, a_map, &S.full[stage], MODE == ROUTER ? kx % p.a_kmod : kx, ay);
           const CUtensorMap* b0 = sh ? &mB0_sh : &mB0;
           const CUtensorMap* b1 = (MODE == GATE_UP) ? (sh ? &mB1_sh : &mB1) : b0;
           const int n1 = (MODE == GATE_UP) ? ti.n0 : ti.n0 + 128;
@@ -303,6 +316,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t phase = 0, acc_phase = 0;
     bool ok = true;
     for (int tile = unit; tile < total && ok; tile += n_units) {
+      int kb_lo = 0, kb_hi = nkb;
+      if (MODE == ROUTER) {
+        const TileInfo ti = decode_tile<PAIR>(S, tile, p.n_tile, n_tiles_n);
+        kb_lo = (int)((long long)nkb * ti.z / p.splits);
+        kb_hi = (int)((long long)nkb * (ti.z + 1) / p.splits);
+      }
       const bool got = PAIR ? mbar_wait_cluster(&S.tempty[acc], acc_phase ^ 1u, abort_flag, lim)
                             : mbar_wait(&S.tempty[acc], acc_phase ^ 1u, abort_flag, lim);
       if (!got) {
@@ -311,7 +330,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_after();
       const uint32_t d = tmem_base + acc * kAccCols;
-      for (int kb = 0; kb < nkb; ++kb) {
+      for (int kb = kb_lo; kb < kb_hi; ++kb) {
         if (!mbar_wait(&S.full[stage], phase, abort_flag, lim)) {
           ok = false;
           break;
@@ -322,8 +341,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t bdesc = sdesc_kmajor_sw128(a_addr + kBoxBytes);
 #pragma unroll
         for (int kk = 0; kk < BK / 16; ++kk) {
-          if (PAIR) umma_bf16_pair(d, adesc + 2 * kk, bdesc + 2 * kk, C::kIdesc, (kb | kk) != 0);
-          else umma_bf16(d, adesc + 2 * kk, bdesc + 2 * kk, C::kIdesc, (kb | kk) != 0);
+          const uint32_t accum = (kb != kb_lo || kk != 0) ? 1u : 0u;
+          if (PAIR) umma_bf16_pair(d, adesc + 2 * kk, bdesc + 2 * kk, C::kIdesc, accum);
+          else umma_bf16(d, adesc + 2 * kk, bdesc + 2 * kk, C::kIdesc, accum);
         }
         if (PAIR) umma_commit_pair_mc(&S.empty[stage], 0x3);
         else umma_commit(&S.empty[stage]);
@@ -358,7 +378,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int tile = unit; tile < total; tile += n_units) {
-      const TileInfo ti = decode_tile<PAIR>(S, tile, p.n_tile);
+      const TileInfo ti = decode_tile<PAIR>(S, tile, p.n_tile, n_tiles_n);
       const bool got = mbar_wait(&S.tfull[acc], acc_phase, abort_flag, lim);
       if (!__all_sync(0xffffffffu, got)) {
         S.abort_flag = 1;
@@ -370,7 +390,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int m = ti.m0 + r_in_tile;
       const bool valid = m < ti.rows;
       const bool sh = ti.g >= p.E;
-      if (MODE == GATE_UP) {
+      if (MODE == ROUTER) {
+        float2* dst = p.logits + ((size_t)ti.z * p.T + m) * p.N + ti.n0;
+#pragma unroll 1
+        for (int c = 0; c < 256; c += 32) {
+          uint32_t v[32];
+          tmem_ld32(tb + c, v);
+          tmem_ld_wait();
+          if (valid && ti.n0 + c < p.N) {
+            float4* d4 = reinterpret_cast<float4*>(dst + c);
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              d4[i] = make_float4(__uint_as_float(v[2 * i]), 0.f, __uint_as_float(v[2 * i + 1]),
+                                  0.f);
+          }
+        }
+      } else if (MODE == GATE_UP) {
         const size_t out_row = sh ? (size_t)p.Tk + m : (size_t)ti.row0 + m;
         __nv_bfloat16* dst = p.h + out_row * p.N + ti.n0;
 #pragma unroll 1
@@ -431,8 +466,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-bool encode_2d(EncodeTiledFn enc, CUtensorMap* m, const void* base, uint64_t inner,
-               uint64_t outer) {
+template <typename Enc>
+bool encode_2d(Enc enc, CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer) {
   const cuuint64_t dims[2] = {inner, outer};
   const cuuint64_t strides[1] = {inner * 2};
   const cuuint32_t box[2] = {BK, 128};
@@ -566,6 +601,48 @@ bool use_pairs(const ExpertArgs& a) {
 }
 
 }  // namespace
+
+// Router logits on the tensor cores: A = X [T, H] (its reduction coordinate taken modulo
+// H), B = W_g pieces [E][3H] (hi | mid | lo), so one fp32 accumulator receives
+// sum_h x_h (hi + mid + lo)_h = sum_h x_h w_h with exact bf16 x bf16 products.
+cudaError_t launch_router_tc(const RouterArgs& a, EncodeTiledFnR enc, bool* encode_failed,
+                             cudaStream_t s) {
+  *encode_failed = false;
+  CUtensorMap mX, mW;
+  bool ok = encode_2d(enc, &mX, a.X, a.H, a.T);
+  ok &= encode_2d(enc, &mW, a.wsplit, 3ull * a.H, a.E);
+  if (!ok) {
+    *encode_failed = true;
+    return cudaErrorInvalidValue;
+  }
+  TcParams p = {};
+  p.offsets = nullptr;
+  p.E = 0;
+  p.has_shared = 0;
+  p.T = a.T;
+  p.Tk = a.T;
+  p.K = 3 * a.H;
+  p.N = a.E;
+  p.n_tile = 256;
+  p.h = nullptr;
+  p.O = nullptr;
+  p.O_shared = nullptr;
+  p.status = a.status;
+  p.test_hook = MOE_TEST_HOOK_NONE;
+  p.wait_limit_ns = a.wait_limit_ns;
+  p.splits = a.splits;
+  p.a_kmod = a.H;
+  p.logits = a.logits;
+  const long long tiles = (long long)((a.T + 127) / 128) * ((a.E + 255) / 256) * a.splits;
+  const int grid = (int)(tiles < a.num_sms ? tiles : a.num_sms);
+  const size_t smem = sizeof(Smem<false>) + 1024;
+  auto* fn = grouped_gemm_kernel<ROUTER, false>;
+  cudaError_t e =
+      cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  fn<<<grid, kThreads, smem, s>>>(mX, mX, mW, mW, mW, mW, p);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_expert_gate_up_tc(const ExpertArgs& a, EncodeTiledFn enc,
                                      bool* encode_failed, cudaStream_t s) {

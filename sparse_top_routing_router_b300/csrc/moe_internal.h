@@ -6,6 +6,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <cuda_bf16.h>
+
 #include "../../include/moe.h"
 
 namespace moe {
@@ -17,21 +19,44 @@ constexpr int kDispatchChunk = 256;   // tokens per dispatch CTA
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// Workspace layout, shared by every call of one forward:
-//   [0, 256)              status word (int32) + padding
-//   router logits         T*E fp32
+// The router's reduction over H is split into S slices.  On the CUDA cores the split
+// gives a small batch enough CTAs; on the tensor cores it also bounds the length of each
+// fp32 accumulation chain to kRouterTcMaxK products (the MMA accumulator's rounding error
+// grows with the chain).  Each slice leaves an fp32 (hi, lo) partial per (token, expert);
+// the selection kernel adds the S partials in slice order.
+constexpr int kRouterTcMaxK = 3072;
+inline int router_split_cap(int T, int H) {      // sizes the workspace
+  int s = 1;
+  if (T > 0 && T < 16384) s = 16384 / T < 2 ? 2 : 16384 / T;
+  const int tc = (3 * H + kRouterTcMaxK - 1) / kRouterTcMaxK;
+  if (tc > s) s = tc;
+  return s > 64 ? 64 : s;
+}
+inline int router_splits(int T, int H) {          // CUDA-core logits
+  const int s = router_split_cap(T, H);
+  const int max_by_h = H / 128 > 0 ? H / 128 : 1;
+  return s < max_by_h ? s : max_by_h;
+}
+
+// Workspace layout, shared by every call of one forward (each region's offset depends
+// only on arguments every call that uses it receives):
+//   [0, 256)              status word (int32 at 0), rows re-decided by the last router
+//                         call (int32 at 4), padding
+//   router partial logits S*T*E float2 (S <= router_split_cap(T, H))
+//   router weight pieces  E * 3H bf16 (tensor-core router: W_g split into hi, mid, lo)
 //   dispatch chunk table  2 * nchunks * E int32
 //   expert activations h  (T*k + T) * I elements (bf16, or fp32 for the fp32 path)
 struct WsLayout {
-  size_t logits, chunk_counts, chunk_base, h, total;
+  size_t logits, wsplit, chunk_counts, chunk_base, h, total;
 };
 
 inline WsLayout ws_layout(int T, int H, int E, int I, int k, int dtype, int has_shared) {
-  (void)H;
   WsLayout L;
   size_t off = kWsHeader;
   L.logits = off;
-  off = align_up(off + (size_t)T * E * 4, 256);
+  off = align_up(off + (size_t)router_split_cap(T, H) * T * E * 8, 256);
+  L.wsplit = off;
+  off = align_up(off + (size_t)E * 3 * H * 2, 256);
   const size_t nchunks = ((size_t)T + kDispatchChunk - 1) / kDispatchChunk;
   L.chunk_counts = off;
   off = align_up(off + nchunks * E * 4, 256);
@@ -51,14 +76,30 @@ struct RouterArgs {
   const float* Wg;
   const float* bias;
   const float* logit_bias;
-  float* logits;       // workspace [T, E]
+  float2* logits;      // workspace [S, T, E] (hi, lo) partial sums
+  int splits;          // S
+  __nv_bfloat16* wsplit;   // tensor-core router: W_g as [E][3H] bf16 pieces, else null
+  float eps_rel;       // fp32 logit error bound per unit of max(1, max|l|) * sqrt(H/1024)
+  int num_sms;
+  unsigned long long wait_limit_ns;
   int32_t* idx;
   float* gate;
   float* gap;
   double* colsum;
   int* status;
+  int* refined;        // counter of rows re-decided from exact dot products
 };
 cudaError_t launch_router_logits(const RouterArgs& a, cudaStream_t s);
+// Tensor-core router logits (x bf16, E % 32 == 0, H % 64 == 0): splits W_g into bf16
+// pieces in a.wsplit, then one GEMM [T, 3H] x [3H, E] with split-K partials.
+typedef CUresult (*EncodeTiledFnR)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                   CUtensorMapFloatOOBfill);
+cudaError_t launch_router_split(const RouterArgs& a, cudaStream_t s);
+cudaError_t launch_router_tc(const RouterArgs& a, EncodeTiledFnR enc, bool* encode_failed,
+                             cudaStream_t s);
 cudaError_t launch_router_select(const RouterArgs& a, cudaStream_t s);
 
 struct DispatchArgs {

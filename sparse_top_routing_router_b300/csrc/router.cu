@@ -78,6 +78,10 @@ __global__ void __launch_bounds__(256) router_logits_kernel(RouterArgs a) {
   const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
   const bool vec_x = (H % 8) == 0;
   const bool vec_w = (E % 4) == 0;
+  // this CTA's slice of the reduction: whole 32-blocks [b0, b1)
+  const int nblk = (H + kTK - 1) / kTK;
+  const int b0 = (int)((long long)nblk * blockIdx.z / gridDim.z);
+  const int b1 = (int)((long long)nblk * (blockIdx.z + 1) / gridDim.z);
 
   float hi[4][4], lo[4][4];
 #pragma unroll
@@ -85,7 +89,7 @@ __global__ void __launch_bounds__(256) router_logits_kernel(RouterArgs a) {
 #pragma unroll
     for (int j = 0; j < 4; ++j) hi[i][j] = lo[i][j] = 0.f;
 
-  for (int kb = 0; kb < H; kb += kTK) {
+  for (int kb = b0 * kTK; kb < b1 * kTK; kb += kTK) {
     // X tile [64 tokens][32 h] -> sX[h][token]; one 8-element segment per thread.
     {
       const int r = tid >> 2, c0 = (tid & 3) * 8;
@@ -155,8 +159,7 @@ __global__ void __launch_bounds__(256) router_logits_kernel(RouterArgs a) {
       const int e = e0 + tx * 4 + j;
       if (e >= E) continue;
       float h = hi[i][j], l = lo[i][j];
-      if (a.logit_bias) two_sum(h, l, a.logit_bias[e]);
-      a.logits[(size_t)t * E + e] = h + l;
+      a.logits[((size_t)blockIdx.z * T + t) * E + e] = make_float2(h, l);
     }
   }
 }
@@ -176,11 +179,14 @@ __global__ void __launch_bounds__(256) router_logits_narrow_kernel(RouterArgs a)
   const int tid = threadIdx.x, tl = tid >> 3, g = tid & 7;
   const int t0 = blockIdx.x * TM;
   const bool vec_x = (H % 8) == 0;
+  const int nch = (H + HC - 1) / HC;
+  const int c0 = (int)((long long)nch * blockIdx.y / gridDim.y);
+  const int c1 = (int)((long long)nch * (blockIdx.y + 1) / gridDim.y);
   float hi[EP], lo[EP];
 #pragma unroll
   for (int e = 0; e < EP; ++e) hi[e] = lo[e] = 0.f;
 
-  for (int kb = 0; kb < H; kb += HC) {
+  for (int kb = c0 * HC; kb < c1 * HC; kb += HC) {
 #pragma unroll
     for (int q = 0; q < TM * HC / 8 / 256; ++q) {
       const int v = tid + q * 256;
@@ -239,41 +245,65 @@ __global__ void __launch_bounds__(256) router_logits_narrow_kernel(RouterArgs a)
     for (int e = 0; e < EP; ++e) {
       if (e >= E) break;
       float h = hi[e], l = lo[e];
-      if (a.logit_bias) two_sum(h, l, a.logit_bias[e]);
-      a.logits[(size_t)t * E + e] = h + l;
+      a.logits[((size_t)blockIdx.y * T + t) * E + e] = make_float2(h, l);
     }
   }
+}
+
+// W_g [H, E] fp32 -> pieces [E][3H] bf16 with w = hi + mid + lo exactly: hi = bf16(w),
+// mid = bf16(w - hi), lo = w - hi - mid (8 significant bits at most, so bf16-exact).  The
+// transpose goes through a 32x32 shared tile so both the read and the write coalesce.
+__global__ void __launch_bounds__(256) router_split_kernel(const float* __restrict__ Wg, int H,
+                                                           int E, __nv_bfloat16* __restrict__ out) {
+  __shared__ __nv_bfloat16 t[3][32][33];
+  const int h0 = blockIdx.x * 32, e0 = blockIdx.y * 32;
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+  for (int r = ty; r < 32; r += 8) {
+    const int h = h0 + r, e = e0 + tx;
+    const float w = (h < H && e < E) ? Wg[(size_t)h * E + e] : 0.f;
+    const __nv_bfloat16 hi = __float2bfloat16_rn(w);
+    const float r1 = w - __bfloat162float(hi);
+    const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
+    const float r2 = r1 - __bfloat162float(mid);
+    t[0][tx][r] = hi;
+    t[1][tx][r] = mid;
+    t[2][tx][r] = __float2bfloat16_rn(r2);
+  }
+  __syncthreads();
+  for (int r = ty; r < 32; r += 8) {
+    const int e = e0 + r, h = h0 + tx;
+    if (e < E && h < H) {
+      __nv_bfloat16* row = out + (size_t)e * 3 * H;
+      row[h] = t[0][r][tx];
+      row[H + h] = t[1][r][tx];
+      row[2 * H + h] = t[2][r][tx];
+    }
+  }
+}
+
+// Sum of the S split-K partials of every (token, expert), one thread each, in slice order
+// (TwoSum), written back to slice 0 as a (hi, lo) pair.  Coalesced over experts, and the
+// S loads of a thread are independent.
+__global__ void __launch_bounds__(256) router_reduce_kernel(float2* __restrict__ p, size_t n,
+                                                            int S) {
+  const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  float hs = 0.f, ls = 0.f;
+  for (int z0 = 0; z0 < S; z0 += 8) {
+    float2 v[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) v[q] = (z0 + q < S) ? p[(size_t)(z0 + q) * n + i] : make_float2(0.f, 0.f);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      two_sum(hs, ls, v[q].x);
+      ls += v[q].y;
+    }
+  }
+  p[i] = make_float2(hs, ls);
 }
 
 // ------------------------------------------------------------------ selection
 
-struct Best {
-  float key;
-  int idx;
-};
-
-__device__ __forceinline__ bool better(float k1, int i1, float k2, int i2) {
-  return k1 > k2 || (k1 == k2 && i1 < i2);
-}
-
-__device__ __forceinline__ Best warp_best(Best b) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const float k2 = __shfl_xor_sync(0xffffffffu, b.key, o);
-    const int i2 = __shfl_xor_sync(0xffffffffu, b.idx, o);
-    if (better(k2, i2, b.key, b.idx)) {
-      b.key = k2;
-      b.idx = i2;
-    }
-  }
-  return b;
-}
-
-__device__ __forceinline__ double warp_sum_d(double v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  return v;
-}
 __device__ __forceinline__ float warp_sum_f(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
@@ -285,124 +315,244 @@ __device__ __forceinline__ float warp_max_f(float v) {
   return v;
 }
 
-// float64 dot product of token t with router column e, the whole warp cooperating.
-template <typename TX>
-__device__ double exact_logit(const RouterArgs& a, const TX* X, int t, int e, int lane) {
-  double acc0 = 0.0, acc1 = 0.0;
-  const TX* xr = X + (size_t)t * a.H;
-  int h = lane;
-  for (; h + 32 < a.H; h += 64) {
-    acc0 = fma((double)load_x1<TX>(xr, h), (double)a.Wg[(size_t)h * a.E + e], acc0);
-    acc1 = fma((double)load_x1<TX>(xr, h + 32), (double)a.Wg[(size_t)(h + 32) * a.E + e],
-               acc1);
+// Order-preserving map of a float key to uint32 (larger key -> larger integer), so the
+// warp's hardware integer max reduction finds the largest key in one instruction.  -0 is
+// folded to +0 first so the two compare equal, as the floats do.
+__device__ __forceinline__ uint32_t ordered_key(float f) {
+  const uint32_t u = __float_as_uint(f + 0.f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float key_of(uint32_t o) {
+  return __uint_as_float((o & 0x80000000u) ? (o & 0x7fffffffu) : ~o);
+}
+
+__device__ __forceinline__ void unpack_bf16x8(const uint4 u, float (&v)[8]) {
+  const __nv_bfloat162* p = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 f = __bfloat1622float2(p[i]);
+    v[2 * i] = f.x;
+    v[2 * i + 1] = f.y;
   }
-  if (h < a.H) acc0 = fma((double)load_x1<TX>(xr, h), (double)a.Wg[(size_t)h * a.E + e], acc0);
-  double s = warp_sum_d(acc0 + acc1);
-  if (a.logit_bias) s += (double)a.logit_bias[e];
-  return s;
+}
+
+// Exact dot products of token t with up to kRefineBatch router columns, the whole warp
+// cooperating.  Each product x*w is split exactly by FMA (p + e = x*w) and added to a
+// double-fp32 (hi, lo) accumulator with TwoSum (Knuth); four independent chains per
+// column keep the FP pipes busy.  The sums carry ~48 significant bits - far below the
+// 1e-6 key margins that matter - and no float64 arithmetic runs in the loop.
+constexpr int kRefineBatch = 4;
+constexpr int kChains = 4;
+
+template <typename TX>
+__device__ void exact_logits(const RouterArgs& a, const TX* X, int t,
+                             const int (&ce)[kRefineBatch], int nb, int lane,
+                             double (&out)[kRefineBatch]) {
+  float sh[kRefineBatch][kChains], sl[kRefineBatch][kChains];
+#pragma unroll
+  for (int c = 0; c < kRefineBatch; ++c)
+#pragma unroll
+    for (int q = 0; q < kChains; ++q) sh[c][q] = sl[c][q] = 0.f;
+  const TX* xr = X + (size_t)t * a.H;
+  if (a.wsplit) {
+    // transposed bf16 pieces (tensor-core path: bf16 X, H % 64 == 0); each lane takes 8
+    // consecutive h per 16-byte load; w = hi + mid + lo is exact in fp32
+    const int nvec = a.H / 8;
+    const uint4* x4 = reinterpret_cast<const uint4*>(xr);
+    for (int v = lane; v < nvec; v += 32) {
+      float x[8];
+      unpack_bf16x8(x4[v], x);
+#pragma unroll
+      for (int c = 0; c < kRefineBatch; ++c) {
+        if (c < nb) {
+          const uint4* w4 = reinterpret_cast<const uint4*>(a.wsplit + (size_t)ce[c] * 3 * a.H);
+          float w0[8], w1[8], w2[8];
+          unpack_bf16x8(w4[v], w0);
+          unpack_bf16x8(w4[v + nvec], w1);
+          unpack_bf16x8(w4[v + 2 * nvec], w2);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const float w = (w0[i] + w1[i]) + w2[i];
+            const float p = x[i] * w;
+            const float e = fmaf(x[i], w, -p);
+            two_sum(sh[c][i & 3], sl[c][i & 3], p);
+            sl[c][i & 3] += e;
+          }
+        }
+      }
+    }
+  } else {
+#pragma unroll 4
+    for (int h = lane; h < a.H; h += 32) {
+      const float x = load_x1<TX>(xr, h);
+      const float* wr = a.Wg + (size_t)h * a.E;
+      const int q = (h >> 5) & (kChains - 1);
+#pragma unroll
+      for (int c = 0; c < kRefineBatch; ++c) {
+        if (c < nb) {
+          const float w = wr[ce[c]];
+          const float p = x * w;
+          const float e = fmaf(x, w, -p);   // exact rounding error of the product
+          two_sum(sh[c][q], sl[c][q], p);
+          sl[c][q] += e;
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int c = 0; c < kRefineBatch; ++c) {
+    float h0 = sh[c][0], l0 = sl[c][0];
+#pragma unroll
+    for (int q = 1; q < kChains; ++q) {
+      two_sum(h0, l0, sh[c][q]);
+      l0 += sl[c][q];
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float h2 = __shfl_xor_sync(0xffffffffu, h0, o);
+      const float l2 = __shfl_xor_sync(0xffffffffu, l0, o);
+      two_sum(h0, l0, h2);
+      l0 += l2;
+    }
+    double v = (double)h0 + (double)l0;
+    if (a.logit_bias && c < nb) v += (double)a.logit_bias[ce[c]];
+    out[c] = v;
+  }
 }
 
 constexpr int kSelWarps = 8;
-constexpr int kTokPerWarp = 8;
 
+// One warp per token.  Lane `lane` owns experts lane + 32 j, j < NJ.  The chosen set is a
+// per-lane bitmask (`taken`), so the output order (ascending expert) comes from ballots.
 template <typename TX, int NJ>
-__global__ void __launch_bounds__(kSelWarps * 32) router_select_kernel(RouterArgs a) {
+__global__ void __launch_bounds__(kSelWarps * 32) router_select_kernel(RouterArgs a,
+                                                                      int tok_per_warp) {
   __shared__ float s_col[kSelWarps][NJ * 32];
   const TX* X = static_cast<const TX*>(a.X);
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const int E = a.E, k = a.k;
   const bool sigm = a.score == MOE_SCORE_SIGMOID;
   const float h_scale = sqrtf(fmaxf(1.f, a.H / 1024.f));
+  const uint32_t lt_mask = (1u << lane) - 1u;
 
   float col[NJ];
 #pragma unroll
   for (int j = 0; j < NJ; ++j) col[j] = 0.f;
 
-  const int tbeg = (blockIdx.x * kSelWarps + w) * kTokPerWarp;
-  for (int t = tbeg; t < min(tbeg + kTokPerWarp, a.T); ++t) {
-    float l[NJ], key[NJ];
+  const int tbeg = (blockIdx.x * kSelWarps + w) * tok_per_warp;
+  for (int t = tbeg; t < min(tbeg + tok_per_warp, a.T); ++t) {
+    float l[NJ], sg[NJ];
+    uint32_t ok[NJ];
+    uint32_t have = 0;   // bit j: expert lane + 32 j exists
     float lmax = -INFINITY, amax = 0.f;
 #pragma unroll
     for (int j = 0; j < NJ; ++j) {
       const int e = lane + 32 * j;
+      l[j] = -INFINITY;
+      sg[j] = 0.f;
+      ok[j] = 0u;
       if (e < E) {
-        l[j] = a.logits[(size_t)t * E + e];
-        lmax = fmaxf(lmax, l[j]);
-        amax = fmaxf(amax, fabsf(l[j]));
-        float kv;
+        const float2 pz = a.logits[(size_t)t * E + e];   // splits were reduced to slice 0
+        float hs = pz.x, ls = pz.y;
+        if (a.logit_bias) two_sum(hs, ls, a.logit_bias[e]);   // the fixed logit offset
+        const float lv = hs + ls;
+        a.logits[(size_t)t * E + e] = make_float2(lv, 0.f);   // slice 0 keeps the sum
+        l[j] = lv;
+        lmax = fmaxf(lmax, lv);
+        amax = fmaxf(amax, fabsf(lv));
+        float kv = lv;
         if (sigm) {
-          kv = 1.f / (1.f + expf(-l[j]));
-          if (a.bias) kv += a.bias[e];
-        } else {
-          kv = l[j];
+          sg[j] = __fdividef(1.f, 1.f + __expf(-lv));
+          kv = sg[j] + (a.bias ? a.bias[e] : 0.f);
         }
-        key[j] = (kv != kv) ? -INFINITY : kv;
-      } else {
-        l[j] = -INFINITY;
-        key[j] = -INFINITY;
+        ok[j] = ordered_key(kv != kv ? -INFINITY : kv);
+        have |= 1u << j;
       }
     }
     lmax = warp_max_f(lmax);
     amax = warp_max_f(amax);
 
-    // top-(k+1) by repeated warp argmax
-    uint32_t taken = 0;   // bit j: expert lane+32j already chosen in this pass
+    // top-(k+1) by repeated warp max: hardware max of the ordered keys, then the lowest
+    // expert index holding that key
+    uint32_t taken = 0;
     float kth = 0.f, k1th = -INFINITY;
-    int sel_lane_j[kMaxK];   // chosen experts, descending key
     const int rounds = (k < E) ? k + 1 : k;
     for (int r = 0; r < rounds; ++r) {
-      Best b{-INFINITY, 0x7fffffff};
+      uint32_t mine = 0u;
 #pragma unroll
-      for (int j = 0; j < NJ; ++j) {
-        const int e = lane + 32 * j;
-        if (e < E && !(taken >> j & 1u) && better(key[j], e, b.key, b.idx)) {
-          b.key = key[j];
-          b.idx = e;
-        }
-      }
-      b = warp_best(b);
+      for (int j = 0; j < NJ; ++j)
+        if ((have & ~taken) >> j & 1u) mine = max(mine, ok[j]);
+      const uint32_t best = __reduce_max_sync(0xffffffffu, mine);
+      uint32_t my_e = 0xffffffffu;
+#pragma unroll
+      for (int j = NJ - 1; j >= 0; --j)
+        if (((have & ~taken) >> j & 1u) && ok[j] == best) my_e = lane + 32 * j;
+      const uint32_t win = __reduce_min_sync(0xffffffffu, my_e);
       if (r < k) {
-        sel_lane_j[r] = b.idx;
-        if ((b.idx & 31) == lane) taken |= 1u << (b.idx >> 5);
-        kth = b.key;
+        if (win != 0xffffffffu && (int)(win & 31u) == lane) taken |= 1u << (win >> 5);
+        kth = key_of(best);
       } else {
-        k1th = b.key;
+        k1th = key_of(best);
       }
     }
 
     float gap = (k < E) ? kth - k1th : INFINITY;
     // error bound of the fp32 logits and of the fp32 keys derived from them
-    const float eps_l = ldexpf(1.f, -19) * fmaxf(1.f, amax) * h_scale;
+    const float eps_l = a.eps_rel * fmaxf(1.f, amax) * h_scale;
     const float eps = sigm ? 0.25f * eps_l + ldexpf(1.f, -20) : eps_l;
 
     if (k < E && !(gap > 2.f * eps)) {
-      // Exactness guard: every expert whose key could still belong to the top k.
+      if (lane == 0 && a.refined) atomicAdd(a.refined, 1);
+      // Exactness guard.  With |approx - exact| <= eps for every key, an expert whose
+      // approximate key exceeds k1th + 2 eps beats every expert outside the approximate
+      // top k, so it is in the exact top k ("certain"); any other member of the exact
+      // top k has an approximate key >= kth - 2 eps.  Only the band between the two
+      // needs exact keys; certain experts take +inf so they are picked first.
       const float lim = kth - 2.f * eps;
+      const float sure = k1th + 2.f * eps;
       double ex[NJ];
-      uint32_t cand = 0;
+      uint32_t cand = 0, band = 0;
 #pragma unroll
       for (int j = 0; j < NJ; ++j) {
-        const int e = lane + 32 * j;
         ex[j] = -INFINITY;
-        if (e < E && key[j] >= lim) cand |= 1u << j;
-      }
-#pragma unroll
-      for (int j = 0; j < NJ; ++j) {
-        uint32_t m = __ballot_sync(0xffffffffu, (cand >> j) & 1u);
-        while (m) {
-          const int src = __ffs(m) - 1;
-          m &= m - 1;
-          const int e = src + 32 * j;
-          const double le = exact_logit<TX>(a, X, t, e, lane);
-          double kv = le;
-          if (sigm) {
-            kv = 1.0 / (1.0 + exp(-le));
-            if (a.bias) kv += (double)a.bias[e];
-          }
-          if (lane == src) ex[j] = kv;
+        const float kv = key_of(ok[j]);
+        if ((have >> j & 1u) && kv >= lim) {
+          cand |= 1u << j;
+          if (kv > sure) ex[j] = INFINITY;
+          else band |= 1u << j;
         }
       }
-      // re-decide among the candidates on the float64 keys
+      uint32_t M[NJ];
+#pragma unroll
+      for (int j = 0; j < NJ; ++j) M[j] = __ballot_sync(0xffffffffu, (band >> j) & 1u);
+      for (;;) {
+        int ce[kRefineBatch];
+        int nb = 0;
+#pragma unroll
+        for (int j = 0; j < NJ; ++j) {
+          while (M[j] && nb < kRefineBatch) {
+            const int src = __ffs(M[j]) - 1;
+            M[j] &= M[j] - 1;
+            ce[nb++] = src + 32 * j;
+          }
+        }
+        if (nb == 0) break;
+        double le[kRefineBatch];
+        exact_logits<TX>(a, X, t, ce, nb, lane, le);
+#pragma unroll
+        for (int c = 0; c < kRefineBatch; ++c) {
+          if (c >= nb) break;
+          double kv = le[c];
+          if (sigm) {
+            kv = 1.0 / (1.0 + exp(-le[c]));
+            if (a.bias) kv += (double)a.bias[ce[c]];
+          }
+#pragma unroll
+          for (int j = 0; j < NJ; ++j)
+            if ((ce[c] >> 5) == j && (ce[c] & 31) == lane) ex[j] = kv;
+        }
+      }
+      // re-decide among the candidates on the exact keys (ties to the lower index)
       uint32_t tk = 0;
       double dk = 0.0, dk1 = -INFINITY;
       for (int r = 0; r <= k; ++r) {
@@ -411,8 +561,7 @@ __global__ void __launch_bounds__(kSelWarps * 32) router_select_kernel(RouterArg
 #pragma unroll
         for (int j = 0; j < NJ; ++j) {
           const int e = lane + 32 * j;
-          if ((cand >> j & 1u) && !(tk >> j & 1u) &&
-              (ex[j] > bk || (ex[j] == bk && e < bi))) {
+          if ((cand >> j & 1u) && !(tk >> j & 1u) && (ex[j] > bk || (ex[j] == bk && e < bi))) {
             bk = ex[j];
             bi = e;
           }
@@ -426,7 +575,7 @@ __global__ void __launch_bounds__(kSelWarps * 32) router_select_kernel(RouterArg
             bi = i2;
           }
         }
-        if (bi == 0x7fffffff) break;   // fewer than k+1 candidates (cannot happen)
+        if (bi == 0x7fffffff) break;
         if (r < k) {
           if ((bi & 31) == lane) tk |= 1u << (bi >> 5);
           dk = bk;
@@ -434,77 +583,53 @@ __global__ void __launch_bounds__(kSelWarps * 32) router_select_kernel(RouterArg
           dk1 = bk;
         }
       }
-      // the first k rounds always succeed: the candidates include the approximate top
-      // k+1; rebuild the chosen list from tk
-      int n = 0;
-#pragma unroll
-      for (int j = 0; j < NJ; ++j) {
-        const uint32_t m = __ballot_sync(0xffffffffu, (tk >> j) & 1u);
-        uint32_t mm = m;
-        while (mm) {
-          const int src = __ffs(mm) - 1;
-          mm &= mm - 1;
-          if (n < k) sel_lane_j[n] = src + 32 * j;
-          ++n;
-        }
-      }
+      taken = tk;
       gap = (float)(dk - dk1);
     }
 
-    // gates of the chosen experts (fp32, from the fp32 logits)
-    float zsum = 0.f, ssum = 0.f;
+    // gates of the chosen experts, each computed by the lane that owns the expert
+    float zsum = 0.f, ssum = 0.f, csum = 0.f;
+    float num[NJ];
 #pragma unroll
     for (int j = 0; j < NJ; ++j) {
-      const int e = lane + 32 * j;
-      if (e < E) {
-        if (sigm) ssum += 1.f / (1.f + expf(-l[j]));
-        else zsum += expf(l[j] - lmax);
+      num[j] = 0.f;
+      if (have >> j & 1u) {
+        if (sigm) {
+          ssum += sg[j];
+          num[j] = sg[j];
+        } else {
+          num[j] = __expf(l[j] - lmax);
+          zsum += num[j];
+        }
+        if (taken >> j & 1u) csum += num[j];
       }
     }
     zsum = warp_sum_f(zsum);
     ssum = warp_sum_f(ssum);
-
-    // lane r < k takes chosen expert r and fetches its logit from the owner lane
-    int my_e = 0x7fffffff;
-    float lv = 0.f;
-    for (int r = 0; r < k; ++r) {
-      const int e = sel_lane_j[r];          // warp-uniform
-      float v = 0.f;
+    csum = warp_sum_f(csum);
+    uint32_t B[NJ];
 #pragma unroll
-      for (int j = 0; j < NJ; ++j)
-        if ((e >> 5) == j) v = l[j];
-      v = __shfl_sync(0xffffffffu, v, e & 31);
-      if (lane == r) {
-        lv = v;
-        my_e = e;
+    for (int j = 0; j < NJ; ++j) B[j] = __ballot_sync(0xffffffffu, (taken >> j) & 1u);
+    int base = 0;
+#pragma unroll
+    for (int j = 0; j < NJ; ++j) {
+      if (taken >> j & 1u) {
+        const int pos = base + __popc(B[j] & lt_mask);
+        float g;
+        if (a.renorm) g = __fdividef(num[j], csum);
+        else g = sigm ? num[j] : __fdividef(num[j], zsum);
+        a.idx[(size_t)t * k + pos] = lane + 32 * j;
+        a.gate[(size_t)t * k + pos] = g;
       }
-    }
-    float my_v = 0.f;
-    if (lane < k) my_v = sigm ? 1.f / (1.f + expf(-lv)) : expf(lv - lmax);
-    const float chosen_sum = warp_sum_f(my_v);
-    float g;
-    if (a.renorm) g = my_v / chosen_sum;
-    else g = sigm ? my_v : my_v / zsum;
-    // write in ascending expert order
-    int rank = 0;
-    for (int r = 0; r < k; ++r) {
-      const int e = __shfl_sync(0xffffffffu, my_e, r);
-      if (e < my_e) ++rank;
-    }
-    if (lane < k) {
-      a.idx[(size_t)t * k + rank] = my_e;
-      a.gate[(size_t)t * k + rank] = g;
+      base += __popc(B[j]);
     }
     if (lane == 0 && a.gap) a.gap[t] = gap;
 
     // row probabilities for the balance statistics
     if (a.colsum) {
+      const float inv = __fdividef(1.f, sigm ? ssum : zsum);
 #pragma unroll
-      for (int j = 0; j < NJ; ++j) {
-        const int e = lane + 32 * j;
-        if (e < E) col[j] += sigm ? (1.f / (1.f + expf(-l[j]))) / ssum
-                                  : expf(l[j] - lmax) / zsum;
-      }
+      for (int j = 0; j < NJ; ++j) col[j] += num[j] * inv;
     }
   }
 
@@ -523,14 +648,17 @@ __global__ void __launch_bounds__(kSelWarps * 32) router_select_kernel(RouterArg
 
 template <typename TX>
 cudaError_t launch_select_t(const RouterArgs& a, cudaStream_t s) {
-  const int per_cta = kSelWarps * kTokPerWarp;
+  // one token per warp up to 2^14 tokens, then more: enough warps to fill the GPU, few
+  // enough CTAs that the per-CTA column sums stay cheap
+  const int tpw = a.T <= 16384 ? 1 : (a.T + 16383) / 16384;
+  const int per_cta = kSelWarps * tpw;
   const dim3 grid((a.T + per_cta - 1) / per_cta);
   const dim3 block(kSelWarps * 32);
-  if (a.E <= 32) router_select_kernel<TX, 1><<<grid, block, 0, s>>>(a);
-  else if (a.E <= 64) router_select_kernel<TX, 2><<<grid, block, 0, s>>>(a);
-  else if (a.E <= 128) router_select_kernel<TX, 4><<<grid, block, 0, s>>>(a);
-  else if (a.E <= 256) router_select_kernel<TX, 8><<<grid, block, 0, s>>>(a);
-  else router_select_kernel<TX, 16><<<grid, block, 0, s>>>(a);
+  if (a.E <= 32) router_select_kernel<TX, 1><<<grid, block, 0, s>>>(a, tpw);
+  else if (a.E <= 64) router_select_kernel<TX, 2><<<grid, block, 0, s>>>(a, tpw);
+  else if (a.E <= 128) router_select_kernel<TX, 4><<<grid, block, 0, s>>>(a, tpw);
+  else if (a.E <= 256) router_select_kernel<TX, 8><<<grid, block, 0, s>>>(a, tpw);
+  else router_select_kernel<TX, 16><<<grid, block, 0, s>>>(a, tpw);
   return cudaGetLastError();
 }
 
@@ -538,7 +666,7 @@ cudaError_t launch_select_t(const RouterArgs& a, cudaStream_t s) {
 
 cudaError_t launch_router_logits(const RouterArgs& a, cudaStream_t s) {
   if (a.E <= 16) {
-    const dim3 g((a.T + 31) / 32);
+    const dim3 g((a.T + 31) / 32, a.splits);
     const bool bf = a.x_dtype == MOE_DTYPE_BF16;
     if (a.E <= 8) {
       if (bf) router_logits_narrow_kernel<__nv_bfloat16, 8><<<g, 256, 0, s>>>(a);
@@ -549,7 +677,7 @@ cudaError_t launch_router_logits(const RouterArgs& a, cudaStream_t s) {
     }
     return cudaGetLastError();
   }
-  const dim3 grid((a.T + kTM - 1) / kTM, (a.E + kTE - 1) / kTE);
+  const dim3 grid((a.T + kTM - 1) / kTM, (a.E + kTE - 1) / kTE, a.splits);
   if (a.x_dtype == MOE_DTYPE_BF16)
     router_logits_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(a);
   else
@@ -557,9 +685,23 @@ cudaError_t launch_router_logits(const RouterArgs& a, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+cudaError_t launch_router_split(const RouterArgs& a, cudaStream_t s) {
+  const dim3 grid((a.H + 31) / 32, (a.E + 31) / 32);
+  router_split_kernel<<<grid, 256, 0, s>>>(a.Wg, a.H, a.E, a.wsplit);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_router_select(const RouterArgs& a, cudaStream_t s) {
-  return a.x_dtype == MOE_DTYPE_BF16 ? launch_select_t<__nv_bfloat16>(a, s)
-                                     : launch_select_t<float>(a, s);
+  RouterArgs b = a;
+  if (a.splits > 1) {
+    const size_t n = (size_t)a.T * a.E;
+    router_reduce_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(a.logits, n, a.splits);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    b.splits = 1;
+  }
+  return b.x_dtype == MOE_DTYPE_BF16 ? launch_select_t<__nv_bfloat16>(b, s)
+                                     : launch_select_t<float>(b, s);
 }
 
 }  // namespace moe

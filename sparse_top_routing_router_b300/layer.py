@@ -8,7 +8,7 @@ host program makes (pinned host X in, host Y out).
 
 from __future__ import annotations
 
-from typing import Dict, Optional
+from typing import Dict, List, Optional
 
 import torch
 
@@ -54,9 +54,15 @@ class MoELayer:
         self.stats = torch.empty(4, dtype=torch.float64, device=dev)
         self.T = T
 
-    def forward(self, X: torch.Tensor, stats: bool = True, stream=None) -> torch.Tensor:
+    def forward(self, X: torch.Tensor, stats: bool = True, stream=None,
+                Y: Optional[torch.Tensor] = None,
+                Y_bf16: Optional[torch.Tensor] = None) -> torch.Tensor:
+        """Enqueue the forward of X on `stream` (default: the current stream).  The fp32
+        output goes to Y (default: the layer's own buffer), an optional bf16 copy to
+        Y_bf16."""
         c, w = self.cfg, self.w
         assert X.shape == (self.T, c.H)
+        Y = self.Y if Y is None else Y
         B.moe_router_topk(self.ctx, X, w["Wg"], c.k, self.score, c.renorm, self.idx,
                           self.gate, self.ws, bias=w.get("bias"),
                           logit_bias=w.get("logit_bias"), key_gap=self.gap,
@@ -68,13 +74,13 @@ class MoELayer:
                              w["W_down"], self.O, self.ws, c.k, Ws_gate=w.get("Ws_gate"),
                              Ws_up=w.get("Ws_up"), Ws_down=w.get("Ws_down"),
                              O_shared=self.O_shared, stream=stream)
-        B.moe_combine(self.ctx, self.O, self.row_of_slot, self.gate, self.Y,
-                      O_shared=self.O_shared, stream=stream)
+        B.moe_combine(self.ctx, self.O, self.row_of_slot, self.gate, Y,
+                      O_shared=self.O_shared, Y_bf16=Y_bf16, stream=stream)
         if stats:
             B.moe_balance_stats(self.ctx, self.T, c.k, self.counts, self.colsum, c.alpha,
                                 self.f, self.p, self.stats, offsets=self.offsets,
                                 stream=stream)
-        return self.Y
+        return Y
 
     def forward_host(self, X_host: torch.Tensor, Y_host: torch.Tensor,
                      X_dev: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
@@ -85,6 +91,50 @@ class MoELayer:
         Y = self.forward(X_dev, stream=stream)
         Y_host.copy_(Y, non_blocking=True)
         return Y_host
+
+    def host_pipeline(self, X_host: torch.Tensor, Y_host: List[torch.Tensor], steps: int,
+                      compute: torch.cuda.Stream) -> None:
+        """`steps` end-to-end forwards from pinned host memory to pinned host memory, the
+        copies overlapped with compute: step i's input copy (H2D stream) runs during
+        step i-1's forward (compute stream), and step i's bf16 output copy (D2H stream)
+        during step i+1's forward.  Device X and Y are double-buffered; events order the
+        reuse of each buffer.  Y_host holds two pinned bf16 [T, H] buffers, used in turn."""
+        dev = self.dev
+        if not hasattr(self, "_pipe"):
+            self._pipe = dict(
+                h2d=torch.cuda.Stream(device=dev), d2h=torch.cuda.Stream(device=dev),
+                X=[torch.empty_like(X_host, device=dev) for _ in range(2)],
+                Y=[torch.empty(self.T, self.cfg.H, dtype=torch.float32, device=dev)
+                   for _ in range(2)],
+                Yb=[torch.empty(self.T, self.cfg.H, dtype=torch.bfloat16, device=dev)
+                    for _ in range(2)])
+        P = self._pipe
+        h2d_done = [torch.cuda.Event() for _ in range(2)]
+        comp_done = [None, None]
+        d2h_done = [None, None]
+        for i in range(steps):
+            b = i & 1
+            with torch.cuda.stream(P["h2d"]):
+                if comp_done[b] is not None:
+                    P["h2d"].wait_event(comp_done[b])      # X[b] no longer read
+                P["X"][b].copy_(X_host, non_blocking=True)
+                h2d_done[b].record(P["h2d"])
+            compute.wait_event(h2d_done[b])
+            if d2h_done[b] is not None:
+                compute.wait_event(d2h_done[b])             # Yb[b] already copied out
+            self.forward(P["X"][b], stream=compute, Y=P["Y"][b], Y_bf16=P["Yb"][b])
+            ev = torch.cuda.Event()
+            ev.record(compute)
+            comp_done[b] = ev
+            with torch.cuda.stream(P["d2h"]):
+                P["d2h"].wait_event(ev)
+                Y_host[b].copy_(P["Yb"][b], non_blocking=True)
+                ev2 = torch.cuda.Event()
+                ev2.record(P["d2h"])
+                d2h_done[b] = ev2
+        for e in d2h_done:
+            if e is not None:
+                compute.wait_event(e)
 
     def device_status(self) -> int:
         return B.moe_get_device_status(self.ctx, self.ws, reset=True)

@@ -63,7 +63,9 @@ def test_capacity_rejects(L):
 def test_workspace_bytes(L):
     ws = B.moe_workspace_bytes(8192, 7168, 256, 2048, 8, B.MOE_DTYPE_BF16, 1)
     h = (8192 * 8 + 8192) * 2048 * 2
-    assert h < ws < h + 8192 * 256 * 4 + 2 * 32 * 256 * 4 + 4096
+    logits = 7 * 8192 * 256 * 8          # up to 7 split-K slices of (hi, lo) partial logits
+    wsplit = 256 * 3 * 7168 * 2          # W_g as bf16 pieces for the tensor-core router
+    assert h + wsplit < ws < h + wsplit + logits + 2 * 32 * 256 * 4 + 4096
     assert B.moe_workspace_bytes(-1, 1, 1, 1, 1, 0, 0) == 0
     assert B.moe_workspace_bytes(0, 64, 8, 64, 2, 0, 0) >= 256
 

@@ -123,7 +123,7 @@ def test_bad_routing_index_is_reported(ctx):
     offsets = torch.empty(E + 1, dtype=torch.int32, device="cuda")
     ros = torch.empty(T * k, dtype=torch.int32, device="cuda")
     sor = torch.empty(T * k, dtype=torch.int32, device="cuda")
-    B.moe_dispatch(ctx, idx, E, -1, counts, offsets, ros, sor, ws)
+    B.moe_dispatch(ctx, idx, E, -1, counts, offsets, ros, sor, ws, H=64)
     st = B.moe_get_device_status(ctx, ws)
     assert st == B.MOE_ERR_DEVICE_INDEX
     assert int(ros[5 * k + 1]) == -1

@@ -70,6 +70,9 @@ struct TcParams {
   int splits;
   int a_kmod;
   float2* logits;
+  // which rows of each group this launch covers: 0 all, 1 whole 256-row chunks,
+  // 2 what remains after them
+  int part;
 };
 
 template <bool PAIR>
@@ -86,11 +89,12 @@ struct __align__(1024) Smem {
   int total_tiles;
   int tile_start[kMaxGroups + 1];
   int grp_rows[kMaxGroups];
-  int grp_row0[kMaxGroups];
+  int grp_row0[kMaxGroups];   // first A row of the group's covered rows
+  int grp_out0[kMaxGroups];   // first output row (h, O or O_shared) of those rows
 };
 
 struct TileInfo {
-  int g, m0, n0, rows, row0, z;
+  int g, m0, n0, rows, row0, out0, z;
 };
 
 template <bool PAIR>
@@ -107,6 +111,7 @@ __device__ __forceinline__ TileInfo decode_tile(const Smem<PAIR>& S, int tile, i
   ti.g = lo;
   ti.rows = S.grp_rows[lo];
   ti.row0 = S.grp_row0[lo];
+  ti.out0 = S.grp_out0[lo];
   const int mt = (ti.rows + TM - 1) / TM;
   const int local = tile - S.tile_start[lo];
   ti.m0 = (local % mt) * TM;
@@ -172,10 +177,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   constexpr int TM = C::kTileM;
   for (int g = tid; g < ngroups; g += kThreads) {
-    int rows, row0;
+    int rows, row0, out0;
     if (MODE == ROUTER) {
       rows = p.T;
       row0 = 0;
+      out0 = 0;
     } else if (g < p.E) {
       const int a = p.offsets[g], b = p.offsets[g + 1];
       if (a < 0 || b < a || b > p.Tk) {
@@ -186,12 +192,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         rows = b - a;
         row0 = a;
       }
+      out0 = row0;   // routed rows: h and O rows follow the permuted rows
     } else {
-      rows = p.T;
+      rows = p.T;    // shared expert: A = X (gate/up) or h rows Tk.. (down)
       row0 = (MODE == GATE_UP) ? 0 : p.Tk;
+      out0 = (MODE == GATE_UP) ? p.Tk : 0;   // h rows Tk.., O_shared rows 0..
+    }
+    if (p.part != 0) {
+      const int whole = rows / 256 * 256;
+      if (p.part == 1) {
+        rows = whole;
+      } else {
+        rows -= whole;
+        row0 += whole;
+        out0 += whole;
+      }
     }
     S.grp_rows[g] = rows;
     S.grp_row0[g] = row0;
+    S.grp_out0[g] = out0;
     S.tile_start[g] = ((rows + TM - 1) / TM) * n_tiles_n *
                       (MODE == ROUTER ? p.splits : 1);     // count, scanned below
   }
@@ -406,7 +425,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       } else if (MODE == GATE_UP) {
-        const size_t out_row = sh ? (size_t)p.Tk + m : (size_t)ti.row0 + m;
+        const size_t out_row = (size_t)ti.out0 + m;
         __nv_bfloat16* dst = p.h + out_row * p.N + ti.n0;
 #pragma unroll 1
         for (int c = 0; c < 128; c += 32) {
@@ -428,7 +447,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       } else {
-        float* dst = sh ? p.O_shared + (size_t)m * p.N : p.O + ((size_t)ti.row0 + m) * p.N;
+        float* dst = (sh ? p.O_shared : p.O) + ((size_t)ti.out0 + m) * p.N;
         dst += ti.n0;
 #pragma unroll 1
         for (int c = 0; c < 256; c += 32) {
@@ -517,7 +536,7 @@ int max_pairs(const void* fn, size_t smem, int num_sms) {
 
 template <int MODE, bool PAIR>
 cudaError_t launch_tc(const ExpertArgs& a, EncodeTiledFn enc, bool* encode_failed,
-                      cudaStream_t s) {
+                      cudaStream_t s, int part) {
   *encode_failed = false;
   const int Tk = a.T * a.k;
   const int K = (MODE == GATE_UP) ? a.H : a.I;
@@ -560,6 +579,10 @@ cudaError_t launch_tc(const ExpertArgs& a, EncodeTiledFn enc, bool* encode_faile
   p.status = a.status;
   p.test_hook = a.test_hook;
   p.wait_limit_ns = a.wait_limit_ns;
+  p.splits = 1;
+  p.a_kmod = K;
+  p.logits = nullptr;
+  p.part = part;
 
   constexpr int TM = Cfg<PAIR>::kTileM;
   const int n_tiles_n = (N + n_tile - 1) / n_tile;
@@ -595,9 +618,26 @@ cudaError_t launch_tc(const ExpertArgs& a, EncodeTiledFn enc, bool* encode_faile
   return cudaLaunchKernelEx(&cfg, fn, mA, mA_sh, mB0, mB1, mB0_sh, mB1_sh, p);
 }
 
-// CTA pairs pay off once the average expert has enough rows to fill 256-row tiles.
+// CTA pairs pay off once the average expert has enough rows to fill 256-row tiles.  They
+// then take every group's whole 256-row chunks, and a single-CTA launch takes what
+// remains in 128-row tiles, so a small expert is not padded to 256 rows.
 bool use_pairs(const ExpertArgs& a) {
   return (long long)a.T * a.k >= 128LL * a.E && a.num_sms >= 2;
+}
+
+// Large experts (>= 512 rows on average) lose little to padding their last 256-row tile,
+// and a second launch would cost more than it saves.
+bool use_split_schedule(const ExpertArgs& a) {
+  return (long long)a.T * a.k < 512LL * a.E;
+}
+
+template <int MODE>
+cudaError_t launch_expert(const ExpertArgs& a, EncodeTiledFn enc, bool* bad, cudaStream_t s) {
+  if (!use_pairs(a)) return launch_tc<MODE, false>(a, enc, bad, s, 0);
+  if (!use_split_schedule(a)) return launch_tc<MODE, true>(a, enc, bad, s, 0);
+  cudaError_t e = launch_tc<MODE, true>(a, enc, bad, s, 1);
+  if (e != cudaSuccess) return e;
+  return launch_tc<MODE, false>(a, enc, bad, s, 2);
 }
 
 }  // namespace
@@ -633,6 +673,7 @@ cudaError_t launch_router_tc(const RouterArgs& a, EncodeTiledFnR enc, bool* enco
   p.splits = a.splits;
   p.a_kmod = a.H;
   p.logits = a.logits;
+  p.part = 0;
   const long long tiles = (long long)((a.T + 127) / 128) * ((a.E + 255) / 256) * a.splits;
   const int grid = (int)(tiles < a.num_sms ? tiles : a.num_sms);
   const size_t smem = sizeof(Smem<false>) + 1024;
@@ -646,14 +687,12 @@ cudaError_t launch_router_tc(const RouterArgs& a, EncodeTiledFnR enc, bool* enco
 
 cudaError_t launch_expert_gate_up_tc(const ExpertArgs& a, EncodeTiledFn enc,
                                      bool* encode_failed, cudaStream_t s) {
-  return use_pairs(a) ? launch_tc<GATE_UP, true>(a, enc, encode_failed, s)
-                      : launch_tc<GATE_UP, false>(a, enc, encode_failed, s);
+  return launch_expert<GATE_UP>(a, enc, encode_failed, s);
 }
 
 cudaError_t launch_expert_down_tc(const ExpertArgs& a, EncodeTiledFn enc,
                                   bool* encode_failed, cudaStream_t s) {
-  return use_pairs(a) ? launch_tc<DOWN, true>(a, enc, encode_failed, s)
-                      : launch_tc<DOWN, false>(a, enc, encode_failed, s);
+  return launch_expert<DOWN>(a, enc, encode_failed, s);
 }
 
 }  // namespace moe

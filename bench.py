@@ -46,6 +46,20 @@ def dist_env():
             int(os.environ.get("LOCAL_RANK", "0")))
 
 
+def replica_seed(base: int, rank: int) -> int:
+    """Each replica draws its own batch (and weights) from seed base + rank."""
+    return base + rank
+
+
+def reduce_max_ms(ms: float, dist, device) -> float:
+    """The timed region ends when the slowest rank ends: max over ranks."""
+    if dist is None:
+        return ms
+    t = torch.tensor([ms], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def workload_config(cfg: K.MoEConfig, cf) -> dict:
     d = {"workload": cfg.name, "T": cfg.T, "H": cfg.H, "E": cfg.E, "I": cfg.I, "k": cfg.k,
          "score": cfg.score, "renorm": cfg.renorm, "shared_expert": cfg.shared,
@@ -228,7 +242,7 @@ def run_gpu(args, cfg, cf):
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     dev = torch.device("cuda", local)
-    d = make_inputs(cfg, device=dev, seed=cfg.seed + rank)
+    d = make_inputs(cfg, device=dev, seed=replica_seed(cfg.seed, rank))
     layer = MoELayer(cfg, d, device=local, capacity_factor=cf)
     X = d["X"]
     stream = torch.cuda.current_stream()
@@ -266,10 +280,7 @@ def run_gpu(args, cfg, cf):
     ms = ev0.elapsed_time(ev1)
     kern = layer.ctx.trace_read()
     layer.ctx.set_tracing(False)
-    if dist is not None:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = reduce_max_ms(ms, dist, dev)
     ms_step = ms / args.steps
     value = world * cfg.T * args.steps / (ms / 1e3)
 
@@ -288,10 +299,7 @@ def run_gpu(args, cfg, cf):
     torch.cuda.synchronize()
     barrier()
     ms_e2e = e0.elapsed_time(e1)
-    if dist is not None:
-        t = torch.tensor([ms_e2e], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_e2e = float(t.item())
+    ms_e2e = reduce_max_ms(ms_e2e, dist, dev)
     st = layer.device_status()
     if st != 0:
         raise RuntimeError(f"device status {st} after the timed region")

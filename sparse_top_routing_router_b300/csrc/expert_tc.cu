@@ -70,9 +70,6 @@ struct TcParams {
   int splits;
   int a_kmod;
   float2* logits;
-  // which rows of each group this launch covers: 0 all, 1 whole 256-row chunks,
-  // 2 what remains after them
-  int part;
 };
 
 template <bool PAIR>
@@ -89,8 +86,8 @@ struct __align__(1024) Smem {
   int total_tiles;
   int tile_start[kMaxGroups + 1];
   int grp_rows[kMaxGroups];
-  int grp_row0[kMaxGroups];   // first A row of the group's covered rows
-  int grp_out0[kMaxGroups];   // first output row (h, O or O_shared) of those rows
+  int grp_row0[kMaxGroups];   // first A row of the group
+  int grp_out0[kMaxGroups];   // first output row (h, O or O_shared) of the group
 };
 
 struct TileInfo {
@@ -198,22 +195,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       row0 = (MODE == GATE_UP) ? 0 : p.Tk;
       out0 = (MODE == GATE_UP) ? p.Tk : 0;   // h rows Tk.., O_shared rows 0..
     }
-    if (p.part != 0) {
-      const int whole = rows / 256 * 256;
-      if (p.part == 1) {
-        rows = whole;
-      } else {
-        rows -= whole;
-        row0 += whole;
-        out0 += whole;
-      }
-    }
     S.grp_rows[g] = rows;
     S.grp_row0[g] = row0;
     S.grp_out0[g] = out0;
-    S.tile_start[g] = ((rows + TM - 1) / TM) * n_tiles_n *
-                      (MODE == ROUTER ? p.splits : 1);     // count, scanned below
   }
+  __syncthreads();
+  for (int g = tid; g < ngroups; g += kThreads)
+    S.tile_start[g] = ((S.grp_rows[g] + TM - 1) / TM) * n_tiles_n *
+                      (MODE == ROUTER ? p.splits : 1);     // count, scanned below
   __syncthreads();
   if (warp == 0) {
     int carry = 0;
@@ -536,7 +525,7 @@ int max_pairs(const void* fn, size_t smem, int num_sms) {
 
 template <int MODE, bool PAIR>
 cudaError_t launch_tc(const ExpertArgs& a, EncodeTiledFn enc, bool* encode_failed,
-                      cudaStream_t s, int part) {
+                      cudaStream_t s) {
   *encode_failed = false;
   const int Tk = a.T * a.k;
   const int K = (MODE == GATE_UP) ? a.H : a.I;
@@ -582,7 +571,6 @@ cudaError_t launch_tc(const ExpertArgs& a, EncodeTiledFn enc, bool* encode_faile
   p.splits = 1;
   p.a_kmod = K;
   p.logits = nullptr;
-  p.part = part;
 
   constexpr int TM = Cfg<PAIR>::kTileM;
   const int n_tiles_n = (N + n_tile - 1) / n_tile;
@@ -618,26 +606,18 @@ cudaError_t launch_tc(const ExpertArgs& a, EncodeTiledFn enc, bool* encode_faile
   return cudaLaunchKernelEx(&cfg, fn, mA, mA_sh, mB0, mB1, mB0_sh, mB1_sh, p);
 }
 
-// CTA pairs pay off once the average expert has enough rows to fill 256-row tiles.  They
-// then take every group's whole 256-row chunks, and a single-CTA launch takes what
-// remains in 128-row tiles, so a small expert is not padded to 256 rows.
+// CTA pairs pay off for large experts (>= 512 rows on average).  For smaller ones the
+// 256-row pair tile pads too much (DSV3-shaped prefill, median 130 rows: same-call A/B
+// 7.6 ms single-CTA vs 8.3 ms pairs per forward), and splitting a group between a pair
+// launch and a single-CTA launch streams its weights from HBM twice.
 bool use_pairs(const ExpertArgs& a) {
-  return (long long)a.T * a.k >= 128LL * a.E && a.num_sms >= 2;
-}
-
-// Large experts (>= 512 rows on average) lose little to padding their last 256-row tile,
-// and a second launch would cost more than it saves.
-bool use_split_schedule(const ExpertArgs& a) {
-  return (long long)a.T * a.k < 512LL * a.E;
+  return (long long)a.T * a.k >= 512LL * a.E && a.num_sms >= 2;
 }
 
 template <int MODE>
 cudaError_t launch_expert(const ExpertArgs& a, EncodeTiledFn enc, bool* bad, cudaStream_t s) {
-  if (!use_pairs(a)) return launch_tc<MODE, false>(a, enc, bad, s, 0);
-  if (!use_split_schedule(a)) return launch_tc<MODE, true>(a, enc, bad, s, 0);
-  cudaError_t e = launch_tc<MODE, true>(a, enc, bad, s, 1);
-  if (e != cudaSuccess) return e;
-  return launch_tc<MODE, false>(a, enc, bad, s, 2);
+  return use_pairs(a) ? launch_tc<MODE, true>(a, enc, bad, s)
+                      : launch_tc<MODE, false>(a, enc, bad, s);
 }
 
 }  // namespace
@@ -673,7 +653,6 @@ cudaError_t launch_router_tc(const RouterArgs& a, EncodeTiledFnR enc, bool* enco
   p.splits = a.splits;
   p.a_kmod = a.H;
   p.logits = a.logits;
-  p.part = 0;
   const long long tiles = (long long)((a.T + 127) / 128) * ((a.E + 255) / 256) * a.splits;
   const int grid = (int)(tiles < a.num_sms ? tiles : a.num_sms);
   const size_t smem = sizeof(Smem<false>) + 1024;

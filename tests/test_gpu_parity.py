@@ -23,10 +23,10 @@ SMALL = [
     K.scaled(K.DSV3_PREFILL, name="dsv3_small_noshared", T=130, H=256, E=32, I=192,
              shared=False, k=4),
     K.scaled(K.SWITCH, name="switch_small", T=1000, H=256, E=16, I=256),
-    # enough rows per expert for the CTA-pair (256-row) tensor-core tiles
-    K.scaled(K.MIXTRAL, name="mixtral_small_pairs", T=700, H=256, E=4, I=384),
-    K.scaled(K.DSV3_PREFILL, name="dsv3_small_pairs", T=520, H=256, E=8, I=256, k=2),
-    K.scaled(K.SWITCH, name="switch_small_pairs", T=3000, H=128, E=8, I=128),
+    # >= 512 rows per expert on average: the CTA-pair (256-row) tensor-core tiles
+    K.scaled(K.MIXTRAL, name="mixtral_small_pairs", T=1100, H=256, E=4, I=384),
+    K.scaled(K.DSV3_PREFILL, name="dsv3_small_pairs", T=1100, H=256, E=2, I=256, k=1),
+    K.scaled(K.SWITCH, name="switch_small_pairs", T=4200, H=128, E=8, I=128),
 ]
 
 

@@ -218,7 +218,9 @@ int moe_get_device_status(moe_ctx* ctx, void* ws, int* status, int reset,
 
 /* Kernel timing.  With tracing on, every kernel a call launches is bracketed by CUDA
  * events recorded on that call's stream.  moe_ctx_trace_read synchronises those events
- * and writes, per kernel id, the number of launches and their summed milliseconds
+ * and writes, per kernel id, the number of kernel launches (the router's tensor-core
+ * logits are two kernels, W_g split and GEMM; split-K router logits add a reduce kernel
+ * to router_select) and their summed milliseconds
  * (host arrays of n entries, n >= MOE_KERNEL_COUNT), then clears the record. */
 enum moe_kernel_id {
   MOE_K_ROUTER_LOGITS = 0,

@@ -33,6 +33,7 @@ struct moe_ctx {
   unsigned long long wait_limit_ns = kWaitLimitDefaultNs;
   struct Rec {
     int id;
+    int kernels;   // kernels the bracketed launch function enqueued
     cudaEvent_t a, b;
   };
   std::vector<Rec> recs;
@@ -73,16 +74,16 @@ cudaEvent_t take_event(moe_ctx* c) {
   return e;
 }
 
-// Launches `fn` with optional event bracketing on `s`.
+// Launches `fn` (which enqueues `kernels` kernels) with optional event bracketing on `s`.
 template <typename F>
-cudaError_t traced(moe_ctx* c, int id, cudaStream_t s, F&& fn) {
+cudaError_t traced(moe_ctx* c, int id, cudaStream_t s, F&& fn, int kernels = 1) {
   if (!c->tracing) return fn();
   std::lock_guard<std::mutex> lk(c->mu);
   cudaEvent_t a = take_event(c), b = take_event(c);
   if (a) cudaEventRecord(a, s);
   cudaError_t e = fn();
   if (b) cudaEventRecord(b, s);
-  if (a && b) c->recs.push_back({id, a, b});
+  if (a && b) c->recs.push_back({id, kernels, a, b});
   return e;
 }
 
@@ -233,7 +234,7 @@ int moe_router_topk(moe_ctx* ctx, const moe_router_desc* d, const void* X, const
     return fail(MOE_ERR_INVALID_ARG, "X, Wg and ws must be 16-byte aligned");
   const WsLayout L = ws_layout(d->T, d->H, d->E, 0, d->k, d->x_dtype, 0);
   // the tensor-core router also needs the W_g pieces; the fp32 CUDA-core one does not
-  const bool use_tc = d->x_dtype == MOE_DTYPE_BF16 && d->E >= 32 && d->E % 32 == 0 &&
+  const bool use_tc = d->x_dtype == MOE_DTYPE_BF16 && d->E % 8 == 0 &&
                       d->H % 64 == 0 && d->T >= 256 && ws_bytes >= L.chunk_counts;
   if (ws_bytes < L.wsplit) return fail(MOE_ERR_INVALID_ARG, "workspace too small");
   if ((r = check_ctx(ctx))) return r;
@@ -280,20 +281,23 @@ int moe_router_topk(moe_ctx* ctx, const moe_router_desc* d, const void* X, const
   a.colsum = prob_colsum;
   a.status = static_cast<int*>(ws);
   a.refined = static_cast<int*>(ws) + 1;
+  a.refine_list = reinterpret_cast<int4*>(static_cast<char*>(ws) + L.refine);
   if ((e = cudaMemsetAsync(a.refined, 0, sizeof(int), s))) return cuda_fail(e, "cudaMemsetAsync");
   if (use_tc) {
     bool bad = false;
     e = traced(ctx, MOE_K_ROUTER_LOGITS, s, [&] {
       cudaError_t r = launch_router_split(a, s);
       return r != cudaSuccess ? r : launch_router_tc(a, ctx->encode, &bad, s);
-    });
+    }, 2);
     if (bad) return fail(MOE_ERR_INVALID_ARG, "tensor map encoding failed (router)");
     if (e) return cuda_fail(e, "router_logits launch");
   } else if ((e = traced(ctx, MOE_K_ROUTER_LOGITS, s,
                          [&] { return launch_router_logits(a, s); }))) {
     return cuda_fail(e, "router_logits launch");
   }
-  if ((e = traced(ctx, MOE_K_ROUTER_SELECT, s, [&] { return launch_router_select(a, s); })))
+  // selection and exact re-decision, after a reduce kernel that sums split-K partials
+  if ((e = traced(ctx, MOE_K_ROUTER_SELECT, s, [&] { return launch_router_select(a, s); },
+                  a.splits > 1 ? 3 : 2)))
     return cuda_fail(e, "router_select launch");
   return ok();
 }
@@ -515,7 +519,7 @@ int moe_ctx_trace_read(moe_ctx* ctx, int* launches, double* total_ms, int n) {
     cudaError_t e = cudaEventSynchronize(rec.b);
     if (e == cudaSuccess) e = cudaEventElapsedTime(&ms, rec.a, rec.b);
     if (e != cudaSuccess) rc = cuda_fail(e, "cudaEventElapsedTime");
-    launches[rec.id] += 1;
+    launches[rec.id] += rec.kernels;
     total_ms[rec.id] += ms;
     ctx->pool.push_back(rec.a);
     ctx->pool.push_back(rec.b);

@@ -59,7 +59,7 @@ struct TcParams {
   int E, has_shared, T, Tk;
   int K;        // reduction length
   int N;        // output width
-  int n_tile;   // output columns per tile: 128 (GATE_UP) or 256 (DOWN)
+  int n_tile;   // output columns per tile: 128 (GATE_UP), 256 (DOWN), E to 16 (ROUTER)
   __nv_bfloat16* h;
   float* O;
   float* O_shared;
@@ -70,6 +70,7 @@ struct TcParams {
   int splits;
   int a_kmod;
   float2* logits;
+  uint32_t router_tx;   // bytes per stage: A box + the W_g-piece box(es)
 };
 
 template <bool PAIR>
@@ -270,14 +271,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const int kx = kb * BK;
         if (!PAIR) {
-          mbar_arrive_expect_tx(&S.full[stage], C::kTxBytes);
+          mbar_arrive_expect_tx(&S.full[stage], MODE == ROUTER ? p.router_tx : C::kTxBytes);
           tma_load_2d(st, a_map, &S.full[stage], MODE == ROUTER ? kx % p.a_kmod : kx, ay);
           const CUtensorMap* b0 = sh ? &mB0_sh : &mB0;
           const CUtensorMap* b1 = (MODE == GATE_UP) ? (sh ? &mB1_sh : &mB1) : b0;
           const int n1 = (MODE == GATE_UP) ? ti.n0 : ti.n0 + 128;
           if (sh) {
             tma_load_2d(st + kBoxBytes, b0, &S.full[stage], kx, ti.n0);
-            tma_load_2d(st + 2 * kBoxBytes, b1, &S.full[stage], kx, n1);
+            // a router tile of at most 128 experts takes one box of n_tile rows
+            if (MODE != ROUTER || p.n_tile > 128)
+              tma_load_2d(st + 2 * kBoxBytes, b1, &S.full[stage], kx, n1);
           } else {
             tma_load_3d(st + kBoxBytes, b0, &S.full[stage], kx, ti.n0, ti.g);
             tma_load_3d(st + 2 * kBoxBytes, b1, &S.full[stage], kx, n1, ti.g);
@@ -323,6 +326,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     int stage = 0, acc = 0;
     uint32_t phase = 0, acc_phase = 0;
     bool ok = true;
+    // the router's N is the expert count rounded up to 16 (at most 256)
+    const uint32_t idesc = MODE == ROUTER ? idesc_bf16_f32(128, p.n_tile) : C::kIdesc;
     for (int tile = unit; tile < total && ok; tile += n_units) {
       int kb_lo = 0, kb_hi = nkb;
       if (MODE == ROUTER) {
@@ -351,7 +356,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kk = 0; kk < BK / 16; ++kk) {
           const uint32_t accum = (kb != kb_lo || kk != 0) ? 1u : 0u;
           if (PAIR) umma_bf16_pair(d, adesc + 2 * kk, bdesc + 2 * kk, C::kIdesc, accum);
-          else umma_bf16(d, adesc + 2 * kk, bdesc + 2 * kk, C::kIdesc, accum);
+          else umma_bf16(d, adesc + 2 * kk, bdesc + 2 * kk, idesc, accum);
         }
         if (PAIR) umma_commit_pair_mc(&S.empty[stage], 0x3);
         else umma_commit(&S.empty[stage]);
@@ -401,16 +406,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (MODE == ROUTER) {
         float2* dst = p.logits + ((size_t)ti.z * p.T + m) * p.N + ti.n0;
 #pragma unroll 1
-        for (int c = 0; c < 256; c += 32) {
+        for (int c = 0; c < p.n_tile; c += 32) {
           uint32_t v[32];
           tmem_ld32(tb + c, v);
           tmem_ld_wait();
-          if (valid && ti.n0 + c < p.N) {
+          const int ncol = p.N - ti.n0 - c;   // live columns from c on
+          if (valid && ncol >= 32) {
             float4* d4 = reinterpret_cast<float4*>(dst + c);
 #pragma unroll
             for (int i = 0; i < 16; ++i)
               d4[i] = make_float4(__uint_as_float(v[2 * i]), 0.f, __uint_as_float(v[2 * i + 1]),
                                   0.f);
+          } else if (valid && ncol > 0) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (i < ncol) dst[c + i] = make_float2(__uint_as_float(v[i]), 0.f);
           }
         }
       } else if (MODE == GATE_UP) {
@@ -475,10 +485,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <typename Enc>
-bool encode_2d(Enc enc, CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer) {
+bool encode_2d(Enc enc, CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
+               uint32_t box_rows = 128) {
   const cuuint64_t dims[2] = {inner, outer};
   const cuuint64_t strides[1] = {inner * 2};
-  const cuuint32_t box[2] = {BK, 128};
+  const cuuint32_t box[2] = {BK, box_rows};
   const cuuint32_t estr[2] = {1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
              box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -571,6 +582,7 @@ cudaError_t launch_tc(const ExpertArgs& a, EncodeTiledFn enc, bool* encode_faile
   p.splits = 1;
   p.a_kmod = K;
   p.logits = nullptr;
+  p.router_tx = 0;
 
   constexpr int TM = Cfg<PAIR>::kTileM;
   const int n_tiles_n = (N + n_tile - 1) / n_tile;
@@ -628,9 +640,13 @@ cudaError_t launch_expert(const ExpertArgs& a, EncodeTiledFn enc, bool* bad, cud
 cudaError_t launch_router_tc(const RouterArgs& a, EncodeTiledFnR enc, bool* encode_failed,
                              cudaStream_t s) {
   *encode_failed = false;
+  // MMA N = the expert count rounded up to 16 (at most 256); up to 128 experts the W_g
+  // pieces come as one box of that many rows, beyond that as two 128-row boxes
+  const int n_tile = a.E >= 256 ? 256 : (a.E + 15) & ~15;
+  const uint32_t w_rows = n_tile > 128 ? 128u : (uint32_t)n_tile;
   CUtensorMap mX, mW;
   bool ok = encode_2d(enc, &mX, a.X, a.H, a.T);
-  ok &= encode_2d(enc, &mW, a.wsplit, 3ull * a.H, a.E);
+  ok &= encode_2d(enc, &mW, a.wsplit, 3ull * a.H, a.E, w_rows);
   if (!ok) {
     *encode_failed = true;
     return cudaErrorInvalidValue;
@@ -643,7 +659,7 @@ cudaError_t launch_router_tc(const RouterArgs& a, EncodeTiledFnR enc, bool* enco
   p.Tk = a.T;
   p.K = 3 * a.H;
   p.N = a.E;
-  p.n_tile = 256;
+  p.n_tile = n_tile;
   p.h = nullptr;
   p.O = nullptr;
   p.O_shared = nullptr;
@@ -653,7 +669,9 @@ cudaError_t launch_router_tc(const RouterArgs& a, EncodeTiledFnR enc, bool* enco
   p.splits = a.splits;
   p.a_kmod = a.H;
   p.logits = a.logits;
-  const long long tiles = (long long)((a.T + 127) / 128) * ((a.E + 255) / 256) * a.splits;
+  p.router_tx = kBoxBytes + (n_tile > 128 ? 2u * kBoxBytes : w_rows * BK * 2);
+  const long long tiles =
+      (long long)((a.T + 127) / 128) * ((a.E + p.n_tile - 1) / p.n_tile) * a.splits;
   const int grid = (int)(tiles < a.num_sms ? tiles : a.num_sms);
   const size_t smem = sizeof(Smem<false>) + 1024;
   auto* fn = grouped_gemm_kernel<ROUTER, false>;

@@ -43,11 +43,12 @@ inline int router_splits(int T, int H) {          // CUDA-core logits
 //   [0, 256)              status word (int32 at 0), rows re-decided by the last router
 //                         call (int32 at 4), padding
 //   router partial logits S*T*E float2 (S <= router_split_cap(T, H))
+//   router refine list    T int4 (rows listed for exact re-decision: t, band limits)
 //   router weight pieces  E * 3H bf16 (tensor-core router: W_g split into hi, mid, lo)
 //   dispatch chunk table  2 * nchunks * E int32
 //   expert activations h  (T*k + T) * I elements (bf16, or fp32 for the fp32 path)
 struct WsLayout {
-  size_t logits, wsplit, chunk_counts, chunk_base, h, total;
+  size_t logits, refine, wsplit, chunk_counts, chunk_base, h, total;
 };
 
 inline WsLayout ws_layout(int T, int H, int E, int I, int k, int dtype, int has_shared) {
@@ -55,6 +56,8 @@ inline WsLayout ws_layout(int T, int H, int E, int I, int k, int dtype, int has_
   size_t off = kWsHeader;
   L.logits = off;
   off = align_up(off + (size_t)router_split_cap(T, H) * T * E * 8, 256);
+  L.refine = off;
+  off = align_up(off + (size_t)T * 16, 256);
   L.wsplit = off;
   off = align_up(off + (size_t)E * 3 * H * 2, 256);
   const size_t nchunks = ((size_t)T + kDispatchChunk - 1) / kDispatchChunk;
@@ -88,9 +91,10 @@ struct RouterArgs {
   double* colsum;
   int* status;
   int* refined;        // counter of rows re-decided from exact dot products
+  int4* refine_list;   // [T] (t, lower band limit, sure limit, 0) of those rows
 };
 cudaError_t launch_router_logits(const RouterArgs& a, cudaStream_t s);
-// Tensor-core router logits (x bf16, E % 32 == 0, H % 64 == 0): splits W_g into bf16
+// Tensor-core router logits (x bf16, E % 8 == 0, H % 64 == 0, T >= 256): splits W_g into bf16
 // pieces in a.wsplit, then one GEMM [T, 3H] x [3H, E] with split-K partials.
 typedef CUresult (*EncodeTiledFnR)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                    const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,

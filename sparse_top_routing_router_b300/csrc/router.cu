@@ -2,16 +2,20 @@
 // W_g[H,E], then top-k per row and normalisation among the k chosen; "AI Knowledge Map
 // - MoE": score, softmax, top-k hard selection, renormalise).
 //
-// Two kernels (the first in a wide and a narrow form):
-//  router_logits  fp32 CUDA-core GEMM l = X W_g (+ logit offset).  Each 32-long block
-//                 of the reduction is summed with fp32 FMA, and the block partials are
-//                 folded into a (hi, lo) pair with TwoSum (Knuth), so the error is that of
-//                 32-term fp32 sums, not of an H-term one.
-//  router_select  one warp per token: keys, top-(k+1) by warp argmax (ties to the lower
-//                 expert index), and an exactness guard: when the k-th/(k+1)-th margin
-//                 is within the fp32 error bound, every expert that could still be in
-//                 the top k gets its logit recomputed as a float64 dot product and the
-//                 row is re-decided on those.  Then gates, key gap, row probabilities.
+// Kernels:
+//  router_logits  fp32 CUDA-core GEMM l = X W_g (a wide and a narrow form).  Each 32-long
+//                 block of the reduction is summed with fp32 FMA, and the block partials
+//                 are folded into a (hi, lo) pair with TwoSum (Knuth), so the error is that
+//                 of 32-term fp32 sums, not of an H-term one.  (The tensor-core form of
+//                 the logits lives with the expert GEMMs; router_split_kernel prepares its
+//                 exact bf16 pieces of W_g.)
+//  router_reduce  sums the split-K partials in slice order.
+//  router_select  one warp per token: logit offset, keys, top-(k+1) by warp argmax (ties
+//                 to the lower expert index), gates, key gap, row probabilities.  A row
+//                 whose k-th/(k+1)-th margin is within the fp32 error bound is listed.
+//  router_refine  one CTA per listed row: every expert that could still be in the top k
+//                 gets its logit recomputed exactly (to ~48 bits) and the row is
+//                 re-decided on those.
 #include <math.h>
 
 #include "moe_internal.h"
@@ -336,30 +340,32 @@ __device__ __forceinline__ void unpack_bf16x8(const uint4 u, float (&v)[8]) {
   }
 }
 
-// Exact dot products of token t with up to kRefineBatch router columns, the whole warp
-// cooperating.  Each product x*w is split exactly by FMA (p + e = x*w) and added to a
-// double-fp32 (hi, lo) accumulator with TwoSum (Knuth); four independent chains per
-// column keep the FP pipes busy.  The sums carry ~48 significant bits - far below the
-// 1e-6 key margins that matter - and no float64 arithmetic runs in the loop.
-constexpr int kRefineBatch = 4;
-constexpr int kChains = 4;
+// ------------------------------------------------------------------ exact re-decision
+// Rows whose k-th/(k+1)-th margin lies inside the fp32 error bound are listed by the
+// selection kernel and re-decided by router_refine_kernel, one CTA per listed row.  The
+// CTA's threads share the reduction over H: each product x*w is split exactly by FMA
+// (p + e = x*w) and added to a double-fp32 (hi, lo) accumulator with TwoSum (Knuth); the
+// per-thread pairs are combined by warp shuffles, then across warps in a fixed order.
+// The sums carry ~48 significant bits - far below the 1e-6 key margins that matter - and
+// no float64 arithmetic runs in the loop.
+constexpr int kRefineBatch = 8;       // band experts per pass over H
+constexpr int kRefineThreads = 256;
+constexpr int kRefineWarps = kRefineThreads / 32;
 
 template <typename TX>
-__device__ void exact_logits(const RouterArgs& a, const TX* X, int t,
-                             const int (&ce)[kRefineBatch], int nb, int lane,
-                             double (&out)[kRefineBatch]) {
-  float sh[kRefineBatch][kChains], sl[kRefineBatch][kChains];
+__device__ void exact_logits_cta(const RouterArgs& a, int t, const int* ce, int nb,
+                                 float2 (*part)[kRefineBatch], double* out) {
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  float sh[kRefineBatch], sl[kRefineBatch];
 #pragma unroll
-  for (int c = 0; c < kRefineBatch; ++c)
-#pragma unroll
-    for (int q = 0; q < kChains; ++q) sh[c][q] = sl[c][q] = 0.f;
-  const TX* xr = X + (size_t)t * a.H;
+  for (int c = 0; c < kRefineBatch; ++c) sh[c] = sl[c] = 0.f;
+  const TX* xr = static_cast<const TX*>(a.X) + (size_t)t * a.H;
   if (a.wsplit) {
-    // transposed bf16 pieces (tensor-core path: bf16 X, H % 64 == 0); each lane takes 8
-    // consecutive h per 16-byte load; w = hi + mid + lo is exact in fp32
+    // transposed bf16 pieces (tensor-core path: bf16 X, H % 64 == 0); 8 consecutive h per
+    // 16-byte load; w = hi + mid + lo is exact in fp32
     const int nvec = a.H / 8;
     const uint4* x4 = reinterpret_cast<const uint4*>(xr);
-    for (int v = lane; v < nvec; v += 32) {
+    for (int v = tid; v < nvec; v += kRefineThreads) {
       float x[8];
       unpack_bf16x8(x4[v], x);
 #pragma unroll
@@ -372,41 +378,34 @@ __device__ void exact_logits(const RouterArgs& a, const TX* X, int t,
           unpack_bf16x8(w4[v + 2 * nvec], w2);
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
-            const float w = (w0[i] + w1[i]) + w2[i];
-            const float p = x[i] * w;
-            const float e = fmaf(x[i], w, -p);
-            two_sum(sh[c][i & 3], sl[c][i & 3], p);
-            sl[c][i & 3] += e;
+            const float wv = (w0[i] + w1[i]) + w2[i];
+            const float p = x[i] * wv;
+            const float e = fmaf(x[i], wv, -p);   // exact rounding error of the product
+            two_sum(sh[c], sl[c], p);
+            sl[c] += e;
           }
         }
       }
     }
   } else {
-#pragma unroll 4
-    for (int h = lane; h < a.H; h += 32) {
+    for (int h = tid; h < a.H; h += kRefineThreads) {
       const float x = load_x1<TX>(xr, h);
       const float* wr = a.Wg + (size_t)h * a.E;
-      const int q = (h >> 5) & (kChains - 1);
 #pragma unroll
       for (int c = 0; c < kRefineBatch; ++c) {
         if (c < nb) {
-          const float w = wr[ce[c]];
-          const float p = x * w;
-          const float e = fmaf(x, w, -p);   // exact rounding error of the product
-          two_sum(sh[c][q], sl[c][q], p);
-          sl[c][q] += e;
+          const float wv = wr[ce[c]];
+          const float p = x * wv;
+          const float e = fmaf(x, wv, -p);
+          two_sum(sh[c], sl[c], p);
+          sl[c] += e;
         }
       }
     }
   }
 #pragma unroll
   for (int c = 0; c < kRefineBatch; ++c) {
-    float h0 = sh[c][0], l0 = sl[c][0];
-#pragma unroll
-    for (int q = 1; q < kChains; ++q) {
-      two_sum(h0, l0, sh[c][q]);
-      l0 += sl[c][q];
-    }
+    float h0 = sh[c], l0 = sl[c];
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
       const float h2 = __shfl_xor_sync(0xffffffffu, h0, o);
@@ -414,26 +413,166 @@ __device__ void exact_logits(const RouterArgs& a, const TX* X, int t,
       two_sum(h0, l0, h2);
       l0 += l2;
     }
-    double v = (double)h0 + (double)l0;
-    if (a.logit_bias && c < nb) v += (double)a.logit_bias[ce[c]];
-    out[c] = v;
+    if (lane == 0) part[w][c] = make_float2(h0, l0);
   }
+  __syncthreads();
+  if (tid < nb) {
+    float h0 = part[0][tid].x, l0 = part[0][tid].y;
+#pragma unroll
+    for (int q = 1; q < kRefineWarps; ++q) {
+      two_sum(h0, l0, part[q][tid].x);
+      l0 += part[q][tid].y;
+    }
+    double v = (double)h0 + (double)l0;
+    if (a.logit_bias) v += (double)a.logit_bias[ce[tid]];
+    out[tid] = v;
+  }
+  __syncthreads();
 }
 
 constexpr int kSelWarps = 8;
 
-// One warp per token.  Lane `lane` owns experts lane + 32 j, j < NJ.  The chosen set is a
-// per-lane bitmask (`taken`), so the output order (ascending expert) comes from ballots.
+// One row as the warp sees it: lane `lane` owns experts lane + 32 j, j < NJ.
+template <int NJ>
+struct RowKeys {
+  float l[NJ], sg[NJ];
+  uint32_t ok[NJ];     // order-preserving integer form of the fp32 selection key
+  uint32_t have;       // bit j: expert lane + 32 j exists
+  float lmax, amax;
+};
+
+// Logits and fp32 keys of row t.  first: slot 0 holds the (hi, lo) sum of the split-K
+// partials; the fixed logit offset is added and (l, 0) written back.  Otherwise slot 0
+// already holds (l, 0).
+template <int NJ>
+__device__ __forceinline__ void load_row(const RouterArgs& a, int t, int lane, bool first,
+                                         RowKeys<NJ>& r) {
+  const bool sigm = a.score == MOE_SCORE_SIGMOID;
+  r.have = 0;
+  r.lmax = -INFINITY;
+  r.amax = 0.f;
+#pragma unroll
+  for (int j = 0; j < NJ; ++j) {
+    const int e = lane + 32 * j;
+    r.l[j] = -INFINITY;
+    r.sg[j] = 0.f;
+    r.ok[j] = 0u;
+    if (e < a.E) {
+      const float2 pz = a.logits[(size_t)t * a.E + e];
+      float hs = pz.x, ls = pz.y;
+      if (first && a.logit_bias) two_sum(hs, ls, a.logit_bias[e]);
+      const float lv = hs + ls;
+      if (first) a.logits[(size_t)t * a.E + e] = make_float2(lv, 0.f);
+      r.l[j] = lv;
+      r.lmax = fmaxf(r.lmax, lv);
+      r.amax = fmaxf(r.amax, fabsf(lv));
+      float kv = lv;
+      if (sigm) {
+        r.sg[j] = __fdividef(1.f, 1.f + __expf(-lv));
+        kv = r.sg[j] + (a.bias ? a.bias[e] : 0.f);
+      }
+      r.ok[j] = ordered_key(kv != kv ? -INFINITY : kv);
+      r.have |= 1u << j;
+    }
+  }
+  r.lmax = warp_max_f(r.lmax);
+  r.amax = warp_max_f(r.amax);
+}
+
+// Top-(k+1) by repeated warp max: hardware max of the ordered keys, then the lowest
+// expert index holding that key.  Returns the chosen set as a per-lane bitmask.
+template <int NJ>
+__device__ __forceinline__ uint32_t topk_row(const RowKeys<NJ>& r, int k, int E, int lane,
+                                             float& kth, float& k1th) {
+  uint32_t taken = 0;
+  kth = 0.f;
+  k1th = -INFINITY;
+  const int rounds = (k < E) ? k + 1 : k;
+  for (int q = 0; q < rounds; ++q) {
+    uint32_t mine = 0u;
+#pragma unroll
+    for (int j = 0; j < NJ; ++j)
+      if ((r.have & ~taken) >> j & 1u) mine = max(mine, r.ok[j]);
+    const uint32_t best = __reduce_max_sync(0xffffffffu, mine);
+    uint32_t my_e = 0xffffffffu;
+#pragma unroll
+    for (int j = NJ - 1; j >= 0; --j)
+      if (((r.have & ~taken) >> j & 1u) && r.ok[j] == best) my_e = lane + 32 * j;
+    const uint32_t win = __reduce_min_sync(0xffffffffu, my_e);
+    if (q < k) {
+      if (win != 0xffffffffu && (int)(win & 31u) == lane) taken |= 1u << (win >> 5);
+      kth = key_of(best);
+    } else {
+      k1th = key_of(best);
+    }
+  }
+  return taken;
+}
+
+// Gates of the chosen experts (each computed by the lane that owns the expert), written
+// in ascending expert order with the key gap; optionally the row's probabilities are
+// added to `col`.
+template <int NJ>
+__device__ __forceinline__ void finish_row(const RouterArgs& a, int t, int lane,
+                                           const RowKeys<NJ>& r, uint32_t taken, float gap,
+                                           float (*col)[NJ]) {
+  const bool sigm = a.score == MOE_SCORE_SIGMOID;
+  const int k = a.k;
+  const uint32_t lt_mask = (1u << lane) - 1u;
+  float zsum = 0.f, ssum = 0.f, csum = 0.f;
+  float num[NJ];
+#pragma unroll
+  for (int j = 0; j < NJ; ++j) {
+    num[j] = 0.f;
+    if (r.have >> j & 1u) {
+      if (sigm) {
+        ssum += r.sg[j];
+        num[j] = r.sg[j];
+      } else {
+        num[j] = __expf(r.l[j] - r.lmax);
+        zsum += num[j];
+      }
+      if (taken >> j & 1u) csum += num[j];
+    }
+  }
+  zsum = warp_sum_f(zsum);
+  ssum = warp_sum_f(ssum);
+  csum = warp_sum_f(csum);
+  uint32_t B[NJ];
+#pragma unroll
+  for (int j = 0; j < NJ; ++j) B[j] = __ballot_sync(0xffffffffu, (taken >> j) & 1u);
+  int base = 0;
+#pragma unroll
+  for (int j = 0; j < NJ; ++j) {
+    if (taken >> j & 1u) {
+      const int pos = base + __popc(B[j] & lt_mask);
+      float g;
+      if (a.renorm) g = __fdividef(num[j], csum);
+      else g = sigm ? num[j] : __fdividef(num[j], zsum);
+      a.idx[(size_t)t * k + pos] = lane + 32 * j;
+      a.gate[(size_t)t * k + pos] = g;
+    }
+    base += __popc(B[j]);
+  }
+  if (lane == 0 && a.gap) a.gap[t] = gap;
+  if (col) {
+    const float inv = __fdividef(1.f, sigm ? ssum : zsum);
+#pragma unroll
+    for (int j = 0; j < NJ; ++j) (*col)[j] += num[j] * inv;
+  }
+}
+
+// One warp per token: keys, top-(k+1), gates, key gap, row probabilities.  A row whose
+// margin is within twice the error bound of its fp32 keys is listed, with its band
+// limits, for router_refine_kernel; its outputs here are provisional.
 template <typename TX, int NJ>
 __global__ void __launch_bounds__(kSelWarps * 32) router_select_kernel(RouterArgs a,
                                                                       int tok_per_warp) {
   __shared__ float s_col[kSelWarps][NJ * 32];
-  const TX* X = static_cast<const TX*>(a.X);
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const int E = a.E, k = a.k;
   const bool sigm = a.score == MOE_SCORE_SIGMOID;
   const float h_scale = sqrtf(fmaxf(1.f, a.H / 1024.f));
-  const uint32_t lt_mask = (1u << lane) - 1u;
 
   float col[NJ];
 #pragma unroll
@@ -441,121 +580,101 @@ __global__ void __launch_bounds__(kSelWarps * 32) router_select_kernel(RouterArg
 
   const int tbeg = (blockIdx.x * kSelWarps + w) * tok_per_warp;
   for (int t = tbeg; t < min(tbeg + tok_per_warp, a.T); ++t) {
-    float l[NJ], sg[NJ];
-    uint32_t ok[NJ];
-    uint32_t have = 0;   // bit j: expert lane + 32 j exists
-    float lmax = -INFINITY, amax = 0.f;
-#pragma unroll
-    for (int j = 0; j < NJ; ++j) {
-      const int e = lane + 32 * j;
-      l[j] = -INFINITY;
-      sg[j] = 0.f;
-      ok[j] = 0u;
-      if (e < E) {
-        const float2 pz = a.logits[(size_t)t * E + e];   // splits were reduced to slice 0
-        float hs = pz.x, ls = pz.y;
-        if (a.logit_bias) two_sum(hs, ls, a.logit_bias[e]);   // the fixed logit offset
-        const float lv = hs + ls;
-        a.logits[(size_t)t * E + e] = make_float2(lv, 0.f);   // slice 0 keeps the sum
-        l[j] = lv;
-        lmax = fmaxf(lmax, lv);
-        amax = fmaxf(amax, fabsf(lv));
-        float kv = lv;
-        if (sigm) {
-          sg[j] = __fdividef(1.f, 1.f + __expf(-lv));
-          kv = sg[j] + (a.bias ? a.bias[e] : 0.f);
-        }
-        ok[j] = ordered_key(kv != kv ? -INFINITY : kv);
-        have |= 1u << j;
-      }
-    }
-    lmax = warp_max_f(lmax);
-    amax = warp_max_f(amax);
-
-    // top-(k+1) by repeated warp max: hardware max of the ordered keys, then the lowest
-    // expert index holding that key
-    uint32_t taken = 0;
-    float kth = 0.f, k1th = -INFINITY;
-    const int rounds = (k < E) ? k + 1 : k;
-    for (int r = 0; r < rounds; ++r) {
-      uint32_t mine = 0u;
-#pragma unroll
-      for (int j = 0; j < NJ; ++j)
-        if ((have & ~taken) >> j & 1u) mine = max(mine, ok[j]);
-      const uint32_t best = __reduce_max_sync(0xffffffffu, mine);
-      uint32_t my_e = 0xffffffffu;
-#pragma unroll
-      for (int j = NJ - 1; j >= 0; --j)
-        if (((have & ~taken) >> j & 1u) && ok[j] == best) my_e = lane + 32 * j;
-      const uint32_t win = __reduce_min_sync(0xffffffffu, my_e);
-      if (r < k) {
-        if (win != 0xffffffffu && (int)(win & 31u) == lane) taken |= 1u << (win >> 5);
-        kth = key_of(best);
-      } else {
-        k1th = key_of(best);
-      }
-    }
-
-    float gap = (k < E) ? kth - k1th : INFINITY;
+    RowKeys<NJ> r;
+    load_row<NJ>(a, t, lane, true, r);
+    float kth, k1th;
+    const uint32_t taken = topk_row<NJ>(r, k, E, lane, kth, k1th);
+    const float gap = (k < E) ? kth - k1th : INFINITY;
     // error bound of the fp32 logits and of the fp32 keys derived from them
-    const float eps_l = a.eps_rel * fmaxf(1.f, amax) * h_scale;
+    const float eps_l = a.eps_rel * fmaxf(1.f, r.amax) * h_scale;
     const float eps = sigm ? 0.25f * eps_l + ldexpf(1.f, -20) : eps_l;
-
-    if (k < E && !(gap > 2.f * eps)) {
-      if (lane == 0 && a.refined) atomicAdd(a.refined, 1);
+    if (k < E && !(gap > 2.f * eps) && lane == 0) {
       // Exactness guard.  With |approx - exact| <= eps for every key, an expert whose
       // approximate key exceeds k1th + 2 eps beats every expert outside the approximate
-      // top k, so it is in the exact top k ("certain"); any other member of the exact
-      // top k has an approximate key >= kth - 2 eps.  Only the band between the two
-      // needs exact keys; certain experts take +inf so they are picked first.
-      const float lim = kth - 2.f * eps;
-      const float sure = k1th + 2.f * eps;
-      double ex[NJ];
-      uint32_t cand = 0, band = 0;
+      // top k, so it is in the exact top k ("sure"); any other member of the exact top k
+      // has an approximate key >= kth - 2 eps.  Only the band between the two limits
+      // needs exact keys.
+      const int slot = atomicAdd(a.refined, 1);
+      a.refine_list[slot] = make_int4(t, __float_as_int(kth - 2.f * eps),
+                                      __float_as_int(k1th + 2.f * eps), 0);
+    }
+    finish_row<NJ>(a, t, lane, r, taken, gap, a.colsum ? &col : nullptr);
+  }
+
+  if (a.colsum) {
+#pragma unroll
+    for (int j = 0; j < NJ; ++j) s_col[w][lane + 32 * j] = col[j];
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+      double s = 0.0;
+#pragma unroll
+      for (int q = 0; q < kSelWarps; ++q) s += (double)s_col[q][e];
+      atomicAdd(a.colsum + e, s);
+    }
+  }
+}
+
+// One CTA per listed row (grid-stride over the list): exact logits of the band experts
+// (CTA-wide), then warp 0 re-decides the row among its candidates on the exact keys
+// (ties to the lower index; sure experts rank first) and rewrites its outputs.
+template <typename TX, int NJ>
+__global__ void __launch_bounds__(kRefineThreads) router_refine_kernel(RouterArgs a) {
+  __shared__ int s_ce[kMaxE];        // band experts, ascending
+  __shared__ double s_ex[kMaxE];     // their exact keys
+  __shared__ float2 s_part[kRefineWarps][kRefineBatch];
+  __shared__ int s_nband;
+  const int n = *a.refined;
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int k = a.k;
+  const bool sigm = a.score == MOE_SCORE_SIGMOID;
+  const uint32_t lt_mask = (1u << lane) - 1u;
+  for (int i = blockIdx.x; i < n; i += gridDim.x) {
+    const int4 ent = a.refine_list[i];
+    const int t = ent.x;
+    const float lim = __int_as_float(ent.y), sure = __int_as_float(ent.z);
+    RowKeys<NJ> r;
+    uint32_t cand = 0, band = 0;
+    if (w == 0) {
+      load_row<NJ>(a, t, lane, false, r);
+      int base = 0;
 #pragma unroll
       for (int j = 0; j < NJ; ++j) {
-        ex[j] = -INFINITY;
-        const float kv = key_of(ok[j]);
-        if ((have >> j & 1u) && kv >= lim) {
+        const float kv = key_of(r.ok[j]);
+        if ((r.have >> j & 1u) && kv >= lim) {
           cand |= 1u << j;
-          if (kv > sure) ex[j] = INFINITY;
-          else band |= 1u << j;
+          if (!(kv > sure)) band |= 1u << j;
         }
+        const uint32_t M = __ballot_sync(0xffffffffu, (band >> j) & 1u);
+        if (band >> j & 1u) s_ce[base + __popc(M & lt_mask)] = lane + 32 * j;
+        base += __popc(M);
       }
-      uint32_t M[NJ];
-#pragma unroll
-      for (int j = 0; j < NJ; ++j) M[j] = __ballot_sync(0xffffffffu, (band >> j) & 1u);
-      for (;;) {
-        int ce[kRefineBatch];
-        int nb = 0;
-#pragma unroll
-        for (int j = 0; j < NJ; ++j) {
-          while (M[j] && nb < kRefineBatch) {
-            const int src = __ffs(M[j]) - 1;
-            M[j] &= M[j] - 1;
-            ce[nb++] = src + 32 * j;
-          }
-        }
-        if (nb == 0) break;
-        double le[kRefineBatch];
-        exact_logits<TX>(a, X, t, ce, nb, lane, le);
-#pragma unroll
-        for (int c = 0; c < kRefineBatch; ++c) {
-          if (c >= nb) break;
-          double kv = le[c];
-          if (sigm) {
-            kv = 1.0 / (1.0 + exp(-le[c]));
-            if (a.bias) kv += (double)a.bias[ce[c]];
-          }
-#pragma unroll
-          for (int j = 0; j < NJ; ++j)
-            if ((ce[c] >> 5) == j && (ce[c] & 31) == lane) ex[j] = kv;
-        }
+      if (lane == 0) s_nband = base;
+    }
+    __syncthreads();
+    const int nband = s_nband;
+    for (int b0 = 0; b0 < nband; b0 += kRefineBatch)
+      exact_logits_cta<TX>(a, t, s_ce + b0, min(kRefineBatch, nband - b0), s_part, s_ex + b0);
+    if (sigm) {
+      for (int c = threadIdx.x; c < nband; c += blockDim.x) {
+        double kv = 1.0 / (1.0 + exp(-s_ex[c]));
+        if (a.bias) kv += (double)a.bias[s_ce[c]];
+        s_ex[c] = kv;
       }
-      // re-decide among the candidates on the exact keys (ties to the lower index)
+      __syncthreads();
+    }
+    if (w == 0) {
+      double ex[NJ];
+      int base = 0;
+#pragma unroll
+      for (int j = 0; j < NJ; ++j) {
+        const uint32_t M = __ballot_sync(0xffffffffu, (band >> j) & 1u);
+        ex[j] = !(cand >> j & 1u) ? -INFINITY
+                : (band >> j & 1u) ? s_ex[base + __popc(M & lt_mask)] : INFINITY;
+        base += __popc(M);
+      }
       uint32_t tk = 0;
       double dk = 0.0, dk1 = -INFINITY;
-      for (int r = 0; r <= k; ++r) {
+      for (int q = 0; q <= k; ++q) {
         double bk = -INFINITY;
         int bi = 0x7fffffff;
 #pragma unroll
@@ -576,90 +695,42 @@ __global__ void __launch_bounds__(kSelWarps * 32) router_select_kernel(RouterArg
           }
         }
         if (bi == 0x7fffffff) break;
-        if (r < k) {
+        if (q < k) {
           if ((bi & 31) == lane) tk |= 1u << (bi >> 5);
           dk = bk;
         } else {
           dk1 = bk;
         }
       }
-      taken = tk;
-      gap = (float)(dk - dk1);
+      finish_row<NJ>(a, t, lane, r, tk, (float)(dk - dk1), nullptr);
     }
-
-    // gates of the chosen experts, each computed by the lane that owns the expert
-    float zsum = 0.f, ssum = 0.f, csum = 0.f;
-    float num[NJ];
-#pragma unroll
-    for (int j = 0; j < NJ; ++j) {
-      num[j] = 0.f;
-      if (have >> j & 1u) {
-        if (sigm) {
-          ssum += sg[j];
-          num[j] = sg[j];
-        } else {
-          num[j] = __expf(l[j] - lmax);
-          zsum += num[j];
-        }
-        if (taken >> j & 1u) csum += num[j];
-      }
-    }
-    zsum = warp_sum_f(zsum);
-    ssum = warp_sum_f(ssum);
-    csum = warp_sum_f(csum);
-    uint32_t B[NJ];
-#pragma unroll
-    for (int j = 0; j < NJ; ++j) B[j] = __ballot_sync(0xffffffffu, (taken >> j) & 1u);
-    int base = 0;
-#pragma unroll
-    for (int j = 0; j < NJ; ++j) {
-      if (taken >> j & 1u) {
-        const int pos = base + __popc(B[j] & lt_mask);
-        float g;
-        if (a.renorm) g = __fdividef(num[j], csum);
-        else g = sigm ? num[j] : __fdividef(num[j], zsum);
-        a.idx[(size_t)t * k + pos] = lane + 32 * j;
-        a.gate[(size_t)t * k + pos] = g;
-      }
-      base += __popc(B[j]);
-    }
-    if (lane == 0 && a.gap) a.gap[t] = gap;
-
-    // row probabilities for the balance statistics
-    if (a.colsum) {
-      const float inv = __fdividef(1.f, sigm ? ssum : zsum);
-#pragma unroll
-      for (int j = 0; j < NJ; ++j) col[j] += num[j] * inv;
-    }
-  }
-
-  if (a.colsum) {
-#pragma unroll
-    for (int j = 0; j < NJ; ++j) s_col[w][lane + 32 * j] = col[j];
-    __syncthreads();
-    for (int e = threadIdx.x; e < E; e += blockDim.x) {
-      double s = 0.0;
-#pragma unroll
-      for (int q = 0; q < kSelWarps; ++q) s += (double)s_col[q][e];
-      atomicAdd(a.colsum + e, s);
-    }
+    __syncthreads();   // s_ce / s_ex are reused by the next listed row
   }
 }
 
-template <typename TX>
-cudaError_t launch_select_t(const RouterArgs& a, cudaStream_t s) {
+template <typename TX, int NJ>
+cudaError_t launch_select_nj(const RouterArgs& a, cudaStream_t s) {
   // one token per warp up to 2^14 tokens, then more: enough warps to fill the GPU, few
   // enough CTAs that the per-CTA column sums stay cheap
   const int tpw = a.T <= 16384 ? 1 : (a.T + 16383) / 16384;
   const int per_cta = kSelWarps * tpw;
-  const dim3 grid((a.T + per_cta - 1) / per_cta);
-  const dim3 block(kSelWarps * 32);
-  if (a.E <= 32) router_select_kernel<TX, 1><<<grid, block, 0, s>>>(a, tpw);
-  else if (a.E <= 64) router_select_kernel<TX, 2><<<grid, block, 0, s>>>(a, tpw);
-  else if (a.E <= 128) router_select_kernel<TX, 4><<<grid, block, 0, s>>>(a, tpw);
-  else if (a.E <= 256) router_select_kernel<TX, 8><<<grid, block, 0, s>>>(a, tpw);
-  else router_select_kernel<TX, 16><<<grid, block, 0, s>>>(a, tpw);
+  router_select_kernel<TX, NJ><<<(a.T + per_cta - 1) / per_cta, kSelWarps * 32, 0, s>>>(a, tpw);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  // the listed rows are few; most of these CTAs find nothing to do and exit
+  const int sms = a.num_sms > 0 ? a.num_sms : 1;
+  const int grid = a.T < 2 * sms ? a.T : 2 * sms;
+  router_refine_kernel<TX, NJ><<<grid, kRefineThreads, 0, s>>>(a);
   return cudaGetLastError();
+}
+
+template <typename TX>
+cudaError_t launch_select_t(const RouterArgs& a, cudaStream_t s) {
+  if (a.E <= 32) return launch_select_nj<TX, 1>(a, s);
+  if (a.E <= 64) return launch_select_nj<TX, 2>(a, s);
+  if (a.E <= 128) return launch_select_nj<TX, 4>(a, s);
+  if (a.E <= 256) return launch_select_nj<TX, 8>(a, s);
+  return launch_select_nj<TX, 16>(a, s);
 }
 
 }  // namespace

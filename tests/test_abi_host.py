@@ -65,7 +65,8 @@ def test_workspace_bytes(L):
     h = (8192 * 8 + 8192) * 2048 * 2
     logits = 7 * 8192 * 256 * 8          # up to 7 split-K slices of (hi, lo) partial logits
     wsplit = 256 * 3 * 7168 * 2          # W_g as bf16 pieces for the tensor-core router
-    assert h + wsplit < ws < h + wsplit + logits + 2 * 32 * 256 * 4 + 4096
+    refine = 8192 * 16                   # rows listed for exact re-decision
+    assert h + wsplit < ws < h + wsplit + logits + refine + 2 * 32 * 256 * 4 + 4096
     assert B.moe_workspace_bytes(-1, 1, 1, 1, 1, 0, 0) == 0
     assert B.moe_workspace_bytes(0, 64, 8, 64, 2, 0, 0) >= 256
 

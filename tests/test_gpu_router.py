@@ -53,8 +53,9 @@ def ctx():
 @pytest.mark.parametrize("cfg,eps_rel", [
     (K.scaled(K.DSV3_PREFILL, name="dsv3_router_tc", T=1024), EPS_TENSOR),
     (K.scaled(K.SWITCH, name="switch_router_tc", T=2048), EPS_TENSOR),
+    (K.scaled(K.MIXTRAL, name="mixtral_router_tc", T=1024), EPS_TENSOR),   # MMA N = 16
     (K.DSV3_DECODE, EPS_CUDA),                                      # split-K CUDA cores
-    (K.scaled(K.MIXTRAL, name="mixtral_router", T=1024), EPS_CUDA),  # narrow CUDA cores
+    (K.scaled(K.MIXTRAL, name="mixtral_router", T=200), EPS_CUDA),   # narrow CUDA cores
 ], ids=lambda v: getattr(v, "name", str(v)))
 def test_logit_error_within_guard(ctx, cfg, eps_rel):
     l_gpu, l_ref, _, _ = _run(cfg, ctx)

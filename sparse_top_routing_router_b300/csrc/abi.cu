@@ -260,16 +260,30 @@ int moe_router_topk(moe_ctx* ctx, const moe_router_desc* d, const void* X, const
   a.wait_limit_ns = ctx->wait_limit_ns;
   a.wsplit = use_tc ? reinterpret_cast<__nv_bfloat16*>(static_cast<char*>(ws) + L.wsplit)
                     : nullptr;
+  a.logits_part = nullptr;
   if (use_tc) {
-    // every slice at most kRouterTcMaxK products long; more slices if the grid is thin
+    // Every slice at most kRouterTcMaxK products long.  Among the slice counts the
+    // workspace holds, take the one with the least time per slice-wave: tiles * S work
+    // units over num_sms CTAs take ceil(tiles * S / num_sms) rounds of 1/S of a tile each.
     const int tiles = ((d->T + 127) / 128) * ((d->E + 255) / 256);
     const int nkb = 3 * d->H / 64;
     const int need = (nkb + kRouterTcMaxK / 64 - 1) / (kRouterTcMaxK / 64);
-    int sp = (3 * ctx->num_sms / 2) / tiles;
     const int cap = router_split_cap(d->T, d->H);
-    sp = sp < need ? need : sp;
-    sp = sp > cap ? cap : sp;
-    a.splits = sp > nkb ? nkb : sp;
+    int hi = cap >= 2 ? 2 * (cap - 1) : 1;   // fp32 partials behind slice 0
+    if (hi > nkb) hi = nkb;
+    const int sms = ctx->num_sms > 0 ? ctx->num_sms : 1;
+    int best = need > hi ? hi : need;
+    double best_t = 1e30;
+    for (int sp = best; sp <= hi; ++sp) {
+      const double t = (double)((tiles * sp + sms - 1) / sms) / sp;
+      if (t < best_t - 1e-12) {
+        best_t = t;
+        best = sp;
+      }
+    }
+    a.splits = best;
+    if (best > 1)
+      a.logits_part = reinterpret_cast<float*>(a.logits + (size_t)d->T * d->E);
     a.eps_rel = kRouterEpsTensor;
   } else {
     a.splits = router_splits(d->T, d->H);

@@ -39,6 +39,7 @@ constexpr int kAccCols = 256;
 constexpr int kTmemCols = 512;
 constexpr int kThreads = 192;
 constexpr int kMaxGroups = kMaxE + 1;
+constexpr int kMaxRing = 12;   // router tiles of a narrow N cut the same bytes into more stages
 
 enum Mode { GATE_UP = 0, DOWN = 1, ROUTER = 2 };
 
@@ -69,15 +70,18 @@ struct TcParams {
   // ROUTER: split-K factor, period of A's reduction coordinate, partial-logit output
   int splits;
   int a_kmod;
-  float2* logits;
+  float2* logits;       // splits == 1: (l, 0) per (token, expert)
+  float* logits_part;   // splits > 1: fp32 partial per (slice, token, expert)
   uint32_t router_tx;   // bytes per stage: A box + the W_g-piece box(es)
+  int ring;             // stages of the ring (ROUTER; the others use Cfg::kStages)
+  uint32_t stage_bytes; // bytes between stages (ROUTER; a multiple of 1024)
 };
 
 template <bool PAIR>
 struct __align__(1024) Smem {
   uint8_t tiles[Cfg<PAIR>::kStages][Cfg<PAIR>::kStageBytes];
-  uint64_t full[Cfg<PAIR>::kStages];
-  uint64_t empty[Cfg<PAIR>::kStages];
+  uint64_t full[kMaxRing];
+  uint64_t empty[kMaxRing];
   uint64_t tfull[2];
   uint64_t tempty[2];
   uint64_t drain;
@@ -137,7 +141,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const __grid_constant__ CUtensorMap mB0_sh,
                         const __grid_constant__ CUtensorMap mB1_sh, const TcParams p) {
   using C = Cfg<PAIR>;
-  constexpr int kStages = C::kStages;
+  const int kStages = MODE == ROUTER ? p.ring : C::kStages;
+  const uint32_t stage_bytes = MODE == ROUTER ? p.stage_bytes : (uint32_t)C::kStageBytes;
   extern __shared__ uint8_t smem_raw[];
   Smem<PAIR>& S = *reinterpret_cast<Smem<PAIR>*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -259,7 +264,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = false;
           break;
         }
-        uint8_t* st = S.tiles[stage];
+        uint8_t* st = &S.tiles[0][0] + (size_t)stage * stage_bytes;
         if (p.test_hook == MOE_TEST_HOOK_WITHHOLD_LOAD && tile == unit && kb == kb_lo) {
           // test only: the first stage is never filled, so the MMA issuer's bounded wait
           // on it runs out and the CTA takes its timeout path
@@ -349,7 +354,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc_fence_after();
-        const uint32_t a_addr = smem_u32(S.tiles[stage]);
+        const uint32_t a_addr = smem_u32(&S.tiles[0][0] + (size_t)stage * stage_bytes);
         const uint64_t adesc = sdesc_kmajor_sw128(a_addr);
         const uint64_t bdesc = sdesc_kmajor_sw128(a_addr + kBoxBytes);
 #pragma unroll
@@ -404,23 +409,41 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool valid = m < ti.rows;
       const bool sh = ti.g >= p.E;
       if (MODE == ROUTER) {
-        float2* dst = p.logits + ((size_t)ti.z * p.T + m) * p.N + ti.n0;
+        // one slice: the logits as (l, 0) pairs; several: fp32 partials for the reduce
+        const size_t cell = ((size_t)ti.z * p.T + m) * p.N + ti.n0;
 #pragma unroll 1
         for (int c = 0; c < p.n_tile; c += 32) {
           uint32_t v[32];
           tmem_ld32(tb + c, v);
           tmem_ld_wait();
           const int ncol = p.N - ti.n0 - c;   // live columns from c on
-          if (valid && ncol >= 32) {
-            float4* d4 = reinterpret_cast<float4*>(dst + c);
+          if (!valid || ncol <= 0) continue;
+          if (p.splits == 1) {
+            float2* dst = p.logits + cell + c;
+            if (ncol >= 32) {
+              float4* d4 = reinterpret_cast<float4*>(dst);
 #pragma unroll
-            for (int i = 0; i < 16; ++i)
-              d4[i] = make_float4(__uint_as_float(v[2 * i]), 0.f, __uint_as_float(v[2 * i + 1]),
-                                  0.f);
-          } else if (valid && ncol > 0) {
+              for (int i = 0; i < 16; ++i)
+                d4[i] = make_float4(__uint_as_float(v[2 * i]), 0.f,
+                                    __uint_as_float(v[2 * i + 1]), 0.f);
+            } else {
 #pragma unroll
-            for (int i = 0; i < 32; ++i)
-              if (i < ncol) dst[c + i] = make_float2(__uint_as_float(v[i]), 0.f);
+              for (int i = 0; i < 32; ++i)
+                if (i < ncol) dst[i] = make_float2(__uint_as_float(v[i]), 0.f);
+            }
+          } else {
+            float* dst = p.logits_part + cell + c;
+            if (ncol >= 32) {
+              float4* d4 = reinterpret_cast<float4*>(dst);
+#pragma unroll
+              for (int i = 0; i < 8; ++i)
+                d4[i] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
+                                    __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
+            } else {
+#pragma unroll
+              for (int i = 0; i < 32; ++i)
+                if (i < ncol) dst[i] = __uint_as_float(v[i]);
+            }
           }
         }
       } else if (MODE == GATE_UP) {
@@ -582,7 +605,10 @@ cudaError_t launch_tc(const ExpertArgs& a, EncodeTiledFn enc, bool* encode_faile
   p.splits = 1;
   p.a_kmod = K;
   p.logits = nullptr;
+  p.logits_part = nullptr;
   p.router_tx = 0;
+  p.ring = Cfg<PAIR>::kStages;
+  p.stage_bytes = Cfg<PAIR>::kStageBytes;
 
   constexpr int TM = Cfg<PAIR>::kTileM;
   const int n_tiles_n = (N + n_tile - 1) / n_tile;
@@ -669,7 +695,14 @@ cudaError_t launch_router_tc(const RouterArgs& a, EncodeTiledFnR enc, bool* enco
   p.splits = a.splits;
   p.a_kmod = a.H;
   p.logits = a.logits;
+  p.logits_part = a.logits_part;
   p.router_tx = kBoxBytes + (n_tile > 128 ? 2u * kBoxBytes : w_rows * BK * 2);
+  // the ring's bytes cut into as many stages as fit (a narrow N leaves most of a 48 KB
+  // stage unused, and more stages in flight hide more of the load latency)
+  p.stage_bytes = (p.router_tx + 1023u) & ~1023u;
+  constexpr uint32_t kRingBytes = (uint32_t)sizeof(Smem<false>::tiles);
+  p.ring = (int)(kRingBytes / p.stage_bytes);
+  if (p.ring > kMaxRing) p.ring = kMaxRing;
   const long long tiles =
       (long long)((a.T + 127) / 128) * ((a.E + p.n_tile - 1) / p.n_tile) * a.splits;
   const int grid = (int)(tiles < a.num_sms ? tiles : a.num_sms);

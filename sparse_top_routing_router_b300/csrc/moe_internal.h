@@ -22,8 +22,9 @@ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 // The router's reduction over H is split into S slices.  On the CUDA cores the split
 // gives a small batch enough CTAs; on the tensor cores it also bounds the length of each
 // fp32 accumulation chain to kRouterTcMaxK products (the MMA accumulator's rounding error
-// grows with the chain).  Each slice leaves an fp32 (hi, lo) partial per (token, expert);
-// the selection kernel adds the S partials in slice order.
+// grows with the chain).  Each CUDA-core slice leaves an fp32 (hi, lo) partial per (token,
+// expert), each tensor-core slice a plain fp32 one (so up to 2 (cap - 1) of them fit
+// behind slice 0); a reduce kernel adds the S partials in slice order.
 constexpr int kRouterTcMaxK = 3072;
 inline int router_split_cap(int T, int H) {      // sizes the workspace
   int s = 1;
@@ -79,7 +80,8 @@ struct RouterArgs {
   const float* Wg;
   const float* bias;
   const float* logit_bias;
-  float2* logits;      // workspace [S, T, E] (hi, lo) partial sums
+  float2* logits;      // workspace [S, T, E] (hi, lo) partial sums; slice 0 the result
+  float* logits_part;  // tensor-core split-K: fp32 partials [S, T, E] after slice 0, or null
   int splits;          // S
   __nv_bfloat16* wsplit;   // tensor-core router: W_g as [E][3H] bf16 pieces, else null
   float eps_rel;       // fp32 logit error bound per unit of max(1, max|l|) * sqrt(H/1024)

@@ -306,6 +306,24 @@ __global__ void __launch_bounds__(256) router_reduce_kernel(float2* __restrict__
   p[i] = make_float2(hs, ls);
 }
 
+// The same for fp32 partials (tensor-core slices), read from `q` [S, n]; the (hi, lo) sum
+// goes to p[i].
+__global__ void __launch_bounds__(256) router_reduce_f32_kernel(const float* __restrict__ q,
+                                                                float2* __restrict__ p,
+                                                                size_t n, int S) {
+  const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  float hs = 0.f, ls = 0.f;
+  for (int z0 = 0; z0 < S; z0 += 8) {
+    float v[8];
+#pragma unroll
+    for (int z = 0; z < 8; ++z) v[z] = (z0 + z < S) ? q[(size_t)(z0 + z) * n + i] : 0.f;
+#pragma unroll
+    for (int z = 0; z < 8; ++z) two_sum(hs, ls, v[z]);
+  }
+  p[i] = make_float2(hs, ls);
+}
+
 // ------------------------------------------------------------------ selection
 
 __device__ __forceinline__ float warp_sum_f(float v) {
@@ -766,7 +784,11 @@ cudaError_t launch_router_select(const RouterArgs& a, cudaStream_t s) {
   RouterArgs b = a;
   if (a.splits > 1) {
     const size_t n = (size_t)a.T * a.E;
-    router_reduce_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(a.logits, n, a.splits);
+    if (a.logits_part)
+      router_reduce_f32_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(a.logits_part,
+                                                                            a.logits, n, a.splits);
+    else
+      router_reduce_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(a.logits, n, a.splits);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     b.splits = 1;

@@ -52,6 +52,11 @@ class MoELayer:
         self.f = torch.empty(c.E, dtype=torch.float64, device=dev)
         self.p = torch.empty(c.E, dtype=torch.float64, device=dev)
         self.stats = torch.empty(4, dtype=torch.float64, device=dev)
+        # the balance statistics need only the routing and the counts, so they run on a
+        # side stream beside the expert GEMMs and combine
+        self._side = torch.cuda.Stream(device=dev)
+        self._routed = torch.cuda.Event()
+        self._stats_done = torch.cuda.Event()
         self.T = T
 
     def forward(self, X: torch.Tensor, stats: bool = True, stream=None,
@@ -63,6 +68,7 @@ class MoELayer:
         c, w = self.cfg, self.w
         assert X.shape == (self.T, c.H)
         Y = self.Y if Y is None else Y
+        stream = torch.cuda.current_stream(self.dev) if stream is None else stream
         B.moe_router_topk(self.ctx, X, w["Wg"], c.k, self.score, c.renorm, self.idx,
                           self.gate, self.ws, bias=w.get("bias"),
                           logit_bias=w.get("logit_bias"), key_gap=self.gap,
@@ -70,6 +76,13 @@ class MoELayer:
         B.moe_dispatch(self.ctx, self.idx, c.E, self.capacity, self.counts, self.offsets,
                        self.row_of_slot, self.slot_of_row, self.ws, X=X, Xperm=self.Xperm,
                        stream=stream)
+        if stats:
+            self._routed.record(stream)
+            self._side.wait_event(self._routed)
+            B.moe_balance_stats(self.ctx, self.T, c.k, self.counts, self.colsum, c.alpha,
+                                self.f, self.p, self.stats, offsets=self.offsets,
+                                stream=self._side)
+            self._stats_done.record(self._side)
         B.moe_grouped_swiglu(self.ctx, X, self.Xperm, self.offsets, w["W_gate"], w["W_up"],
                              w["W_down"], self.O, self.ws, c.k, Ws_gate=w.get("Ws_gate"),
                              Ws_up=w.get("Ws_up"), Ws_down=w.get("Ws_down"),
@@ -77,9 +90,7 @@ class MoELayer:
         B.moe_combine(self.ctx, self.O, self.row_of_slot, self.gate, Y,
                       O_shared=self.O_shared, Y_bf16=Y_bf16, stream=stream)
         if stats:
-            B.moe_balance_stats(self.ctx, self.T, c.k, self.counts, self.colsum, c.alpha,
-                                self.f, self.p, self.stats, offsets=self.offsets,
-                                stream=stream)
+            stream.wait_event(self._stats_done)   # the forward ends when both streams do
         return Y
 
     def forward_host(self, X_host: torch.Tensor, Y_host: torch.Tensor,

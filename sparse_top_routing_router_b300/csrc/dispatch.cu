@@ -39,16 +39,24 @@ __global__ void __launch_bounds__(kChunk) dispatch_count_kernel(DispatchArgs a) 
     a.chunk_counts[(size_t)c * a.E + e] = hist[e];
 }
 
-// One CTA of 512 threads: thread e walks the chunks of expert e.
+// One CTA of 512 threads: thread e walks the chunks of expert e, 16 chunk counts loaded
+// at a time (independent loads, then the running sums).
 __global__ void __launch_bounds__(kMaxE) dispatch_scan_kernel(DispatchArgs a, int nchunks) {
   __shared__ int s_warp[kMaxE / 32];
+  constexpr int kBatch = 16;
   const int e = threadIdx.x;
   int run = 0;
   if (e < a.E) {
-    for (int c = 0; c < nchunks; ++c) {
-      const size_t i = (size_t)c * a.E + e;
-      a.chunk_base[i] = run;
-      run += a.chunk_counts[i];
+    for (int c0 = 0; c0 < nchunks; c0 += kBatch) {
+      int v[kBatch];
+#pragma unroll
+      for (int q = 0; q < kBatch; ++q)
+        v[q] = (c0 + q < nchunks) ? a.chunk_counts[(size_t)(c0 + q) * a.E + e] : 0;
+#pragma unroll
+      for (int q = 0; q < kBatch; ++q) {
+        if (c0 + q < nchunks) a.chunk_base[(size_t)(c0 + q) * a.E + e] = run;
+        run += v[q];
+      }
     }
     a.counts[e] = run;
   }

@@ -285,43 +285,54 @@ __global__ void __launch_bounds__(256) router_split_kernel(const float* __restri
   }
 }
 
-// Sum of the S split-K partials of every (token, expert), one thread each, in slice order
-// (TwoSum), written back to slice 0 as a (hi, lo) pair.  Coalesced over experts, and the
-// S loads of a thread are independent.
-__global__ void __launch_bounds__(256) router_reduce_kernel(float2* __restrict__ p, size_t n,
-                                                            int S) {
-  const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= n) return;
+// Sum of the S split-K partials of every (token, expert) in slice order: G consecutive
+// lanes share one element, lane r adding the r-th contiguous run of slices with TwoSum,
+// then the G runs are combined in lane order (a fixed order, so the result does not vary
+// between runs).  G > 1 when there are too few elements to keep the GPU's loads in
+// flight; the result goes to slice 0 as a (hi, lo) pair.  F32 selects plain fp32
+// partials in `q` (tensor-core slices), else (hi, lo) partials in `p` itself.
+template <bool F32, int G>
+__global__ void __launch_bounds__(256) router_reduce_kernel(float2* __restrict__ p,
+                                                            const float* __restrict__ q,
+                                                            size_t n, int S) {
+  const size_t gid = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const size_t i = gid / G;
+  const int r = (int)(gid % G);
+  const bool live = i < n;
+  const int per = (S + G - 1) / G;
+  const int z_lo = min(S, r * per), z_hi = min(S, z_lo + per);
   float hs = 0.f, ls = 0.f;
-  for (int z0 = 0; z0 < S; z0 += 8) {
-    float2 v[8];
+  if (live) {
+    for (int z0 = z_lo; z0 < z_hi; z0 += 8) {
+      float2 v[8];
 #pragma unroll
-    for (int q = 0; q < 8; ++q) v[q] = (z0 + q < S) ? p[(size_t)(z0 + q) * n + i] : make_float2(0.f, 0.f);
+      for (int z = 0; z < 8; ++z) {
+        v[z] = make_float2(0.f, 0.f);
+        if (z0 + z < z_hi) {
+          if (F32) v[z].x = q[(size_t)(z0 + z) * n + i];
+          else v[z] = p[(size_t)(z0 + z) * n + i];
+        }
+      }
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      two_sum(hs, ls, v[q].x);
-      ls += v[q].y;
+      for (int z = 0; z < 8; ++z) {
+        two_sum(hs, ls, v[z].x);
+        ls += v[z].y;
+      }
     }
   }
-  p[i] = make_float2(hs, ls);
-}
-
-// The same for fp32 partials (tensor-core slices), read from `q` [S, n]; the (hi, lo) sum
-// goes to p[i].
-__global__ void __launch_bounds__(256) router_reduce_f32_kernel(const float* __restrict__ q,
-                                                                float2* __restrict__ p,
-                                                                size_t n, int S) {
-  const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= n) return;
-  float hs = 0.f, ls = 0.f;
-  for (int z0 = 0; z0 < S; z0 += 8) {
-    float v[8];
+  if (G > 1) {
+    // lane r takes lane r + o's sum, o = 1, 2, 4: the runs are added in slice order
 #pragma unroll
-    for (int z = 0; z < 8; ++z) v[z] = (z0 + z < S) ? q[(size_t)(z0 + z) * n + i] : 0.f;
-#pragma unroll
-    for (int z = 0; z < 8; ++z) two_sum(hs, ls, v[z]);
+    for (int o = 1; o < G; o <<= 1) {
+      const float h2 = __shfl_down_sync(0xffffffffu, hs, o, G);
+      const float l2 = __shfl_down_sync(0xffffffffu, ls, o, G);
+      if ((r & (2 * o - 1)) == 0) {
+        two_sum(hs, ls, h2);
+        ls += l2;
+      }
+    }
   }
-  p[i] = make_float2(hs, ls);
+  if (live && r == 0) p[i] = make_float2(hs, ls);
 }
 
 // ------------------------------------------------------------------ selection
@@ -784,11 +795,21 @@ cudaError_t launch_router_select(const RouterArgs& a, cudaStream_t s) {
   RouterArgs b = a;
   if (a.splits > 1) {
     const size_t n = (size_t)a.T * a.E;
-    if (a.logits_part)
-      router_reduce_f32_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(a.logits_part,
-                                                                            a.logits, n, a.splits);
-    else
-      router_reduce_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(a.logits, n, a.splits);
+    // lanes per element: enough threads for ~2 waves of loads, at most 8, at most S
+    const size_t want = (size_t)2 * 2048 * (a.num_sms > 0 ? a.num_sms : 1);
+    int G = 1;
+    while (G < 8 && G < a.splits && n * G < want) G <<= 1;
+    const unsigned blocks = (unsigned)((n * G + 255) / 256);
+    const bool f32 = a.logits_part != nullptr;
+#define MOE_REDUCE(GG)                                                                      \
+  (f32 ? router_reduce_kernel<true, GG><<<blocks, 256, 0, s>>>(a.logits, a.logits_part, n,   \
+                                                                a.splits)                   \
+       : router_reduce_kernel<false, GG><<<blocks, 256, 0, s>>>(a.logits, nullptr, n, a.splits))
+    if (G == 1) MOE_REDUCE(1);
+    else if (G == 2) MOE_REDUCE(2);
+    else if (G == 4) MOE_REDUCE(4);
+    else MOE_REDUCE(8);
+#undef MOE_REDUCE
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     b.splits = 1;

@@ -266,8 +266,10 @@ int moe_router_topk(moe_ctx* ctx, const moe_router_desc* d, const void* X, const
     // workspace holds, take the one with the least time per slice-wave: tiles * S work
     // units over num_sms CTAs take ceil(tiles * S / num_sms) rounds of 1/S of a tile each.
     const int tiles = ((d->T + 127) / 128) * ((d->E + 255) / 256);
-    const int nkb = 3 * d->H / 64;
-    const int need = (nkb + kRouterTcMaxK / 64 - 1) / (kRouterTcMaxK / 64);
+    const bool fused = router_tc_fused(d->E);
+    const int nkb = (fused ? 1 : 3) * d->H / 64;
+    const int kb_chain = kRouterTcMaxK / (fused ? 3 * 64 : 64);   // k-blocks per chain
+    const int need = (nkb + kb_chain - 1) / kb_chain;
     const int cap = router_split_cap(d->T, d->H);
     int hi = cap >= 2 ? 2 * (cap - 1) : 1;   // fp32 partials behind slice 0
     if (hi > nkb) hi = nkb;

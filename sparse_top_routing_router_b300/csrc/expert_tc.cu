@@ -72,6 +72,9 @@ struct TcParams {
   int a_kmod;
   float2* logits;       // splits == 1: (l, 0) per (token, expert)
   float* logits_part;   // splits > 1: fp32 partial per (slice, token, expert)
+  int pieces;           // ROUTER: 3 = per 64 h one X box and three W_g-piece boxes;
+                        // 1 = reduction over [X, X, X] . [hi; mid; lo] (K = 3H)
+  uint32_t piece_bytes; // ROUTER, pieces == 3: bytes of one W_g-piece box
   uint32_t router_tx;   // bytes per stage: A box + the W_g-piece box(es)
   int ring;             // stages of the ring (ROUTER; the others use Cfg::kStages)
   uint32_t stage_bytes; // bytes between stages (ROUTER; a multiple of 1024)
@@ -275,7 +278,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           continue;
         }
         const int kx = kb * BK;
-        if (!PAIR) {
+        if (MODE == ROUTER && p.pieces == 3) {
+          // one X box and the hi, mid, lo boxes of the same 64 h
+          mbar_arrive_expect_tx(&S.full[stage], p.router_tx);
+          tma_load_2d(st, a_map, &S.full[stage], kx, ay);
+#pragma unroll
+          for (int q = 0; q < 3; ++q)
+            tma_load_2d(st + kBoxBytes + q * p.piece_bytes, &mB0_sh, &S.full[stage],
+                        kx + q * p.a_kmod, ti.n0);
+        } else if (!PAIR) {
           mbar_arrive_expect_tx(&S.full[stage], MODE == ROUTER ? p.router_tx : C::kTxBytes);
           tma_load_2d(st, a_map, &S.full[stage], MODE == ROUTER ? kx % p.a_kmod : kx, ay);
           const CUtensorMap* b0 = sh ? &mB0_sh : &mB0;
@@ -357,11 +368,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t a_addr = smem_u32(&S.tiles[0][0] + (size_t)stage * stage_bytes);
         const uint64_t adesc = sdesc_kmajor_sw128(a_addr);
         const uint64_t bdesc = sdesc_kmajor_sw128(a_addr + kBoxBytes);
+        if (MODE == ROUTER && p.pieces == 3) {
 #pragma unroll
-        for (int kk = 0; kk < BK / 16; ++kk) {
-          const uint32_t accum = (kb != kb_lo || kk != 0) ? 1u : 0u;
-          if (PAIR) umma_bf16_pair(d, adesc + 2 * kk, bdesc + 2 * kk, C::kIdesc, accum);
-          else umma_bf16(d, adesc + 2 * kk, bdesc + 2 * kk, idesc, accum);
+          for (int kk = 0; kk < BK / 16; ++kk) {
+#pragma unroll
+            for (int q = 0; q < 3; ++q) {
+              const uint64_t bq = sdesc_kmajor_sw128(a_addr + kBoxBytes + q * p.piece_bytes);
+              const uint32_t accum = (kb != kb_lo || kk != 0 || q != 0) ? 1u : 0u;
+              umma_bf16(d, adesc + 2 * kk, bq + 2 * kk, idesc, accum);
+            }
+          }
+        } else {
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            const uint32_t accum = (kb != kb_lo || kk != 0) ? 1u : 0u;
+            if (PAIR) umma_bf16_pair(d, adesc + 2 * kk, bdesc + 2 * kk, C::kIdesc, accum);
+            else umma_bf16(d, adesc + 2 * kk, bdesc + 2 * kk, idesc, accum);
+          }
         }
         if (PAIR) umma_commit_pair_mc(&S.empty[stage], 0x3);
         else umma_commit(&S.empty[stage]);
@@ -606,6 +629,8 @@ cudaError_t launch_tc(const ExpertArgs& a, EncodeTiledFn enc, bool* encode_faile
   p.a_kmod = K;
   p.logits = nullptr;
   p.logits_part = nullptr;
+  p.pieces = 1;
+  p.piece_bytes = 0;
   p.router_tx = 0;
   p.ring = Cfg<PAIR>::kStages;
   p.stage_bytes = Cfg<PAIR>::kStageBytes;
@@ -683,7 +708,13 @@ cudaError_t launch_router_tc(const RouterArgs& a, EncodeTiledFnR enc, bool* enco
   p.has_shared = 0;
   p.T = a.T;
   p.Tk = a.T;
-  p.K = 3 * a.H;
+  // up to 128 experts: per 64 h one X box and the three piece boxes (X read once);
+  // beyond: the reduction runs over [X, X, X] . [hi; mid; lo] (the pieces would not fit
+  // a stage together)
+  const bool fused = router_tc_fused(a.E);
+  p.pieces = fused ? 3 : 1;
+  p.piece_bytes = w_rows * BK * 2;
+  p.K = fused ? a.H : 3 * a.H;
   p.N = a.E;
   p.n_tile = n_tile;
   p.h = nullptr;
@@ -696,7 +727,8 @@ cudaError_t launch_router_tc(const RouterArgs& a, EncodeTiledFnR enc, bool* enco
   p.a_kmod = a.H;
   p.logits = a.logits;
   p.logits_part = a.logits_part;
-  p.router_tx = kBoxBytes + (n_tile > 128 ? 2u * kBoxBytes : w_rows * BK * 2);
+  p.router_tx = fused ? kBoxBytes + 3u * p.piece_bytes
+                      : kBoxBytes + (n_tile > 128 ? 2u * kBoxBytes : p.piece_bytes);
   // the ring's bytes cut into as many stages as fit (a narrow N leaves most of a 48 KB
   // stage unused, and more stages in flight hide more of the load latency)
   p.stage_bytes = (p.router_tx + 1023u) & ~1023u;

@@ -33,6 +33,9 @@ inline int router_split_cap(int T, int H) {      // sizes the workspace
   if (tc > s) s = tc;
   return s > 64 ? 64 : s;
 }
+// Tensor-core router with at most 128 experts: the three W_g pieces of a 64-wide block of
+// H share one X box, so a k-block carries 3 * 64 products (else 64 of the [X, X, X] row).
+inline bool router_tc_fused(int E) { return E <= 128; }
 inline int router_splits(int T, int H) {          // CUDA-core logits
   const int s = router_split_cap(T, H);
   const int max_by_h = H / 128 > 0 ? H / 128 : 1;

@@ -147,5 +147,22 @@ class MoELayer:
             if e is not None:
                 compute.wait_event(e)
 
+    def capture(self, X: torch.Tensor, stats: bool = True,
+                Y_bf16: Optional[torch.Tensor] = None) -> torch.cuda.CUDAGraph:
+        """Record one forward of the device buffer X into a CUDA graph and return it;
+        `graph.replay()` then reruns the whole forward on whatever X holds, with one
+        launch from the host instead of one per kernel (small batches are host-bound).
+        The forward allocates nothing and never synchronises, so it captures as is.  One
+        eager forward first loads the module and fills the per-process caches; tracing
+        must be off."""
+        s = torch.cuda.Stream(device=self.dev)
+        s.wait_stream(torch.cuda.current_stream(self.dev))
+        self.forward(X, stats=stats, stream=s, Y_bf16=Y_bf16)
+        s.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            self.forward(X, stats=stats, stream=s, Y_bf16=Y_bf16)
+        return g
+
     def device_status(self) -> int:
         return B.moe_get_device_status(self.ctx, self.ws, reset=True)

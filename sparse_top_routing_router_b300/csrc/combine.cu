@@ -3,8 +3,9 @@
 // combine: "LLM Internals §14.2.1 step 6" - weight each expert output by its gate, write
 // it back to the token's position through the inverse of the step-4 permutation, add the
 // shared expert; "AI Knowledge Map - MoE": y = sum over S of g_e E_e(x).  One CTA per
-// token, 16-byte vector loads, a fixed summation order (choices j ascending, then the
-// shared expert), so the result is bitwise reproducible.
+// token (and column chunk, for small batches), 16-byte vector loads, a fixed summation
+// order (choices j ascending, then the shared expert), so the result is bitwise
+// reproducible.
 //
 // balance_stats: §14.2.3 L = alpha * N * sum f_i p_i and the three monitoring signals it
 // names (routing entropy, per-expert load, drop rate), plus the load CV of the
@@ -27,8 +28,10 @@ __global__ void __launch_bounds__(256) combine_kernel(CombineArgs a) {
   }
   __syncthreads();
   const int nv = a.H / 4;
+  const int per = (nv + gridDim.y - 1) / gridDim.y;   // column chunk of this CTA
+  const int v0 = blockIdx.y * per, v1 = min(nv, v0 + per);
   float4* Y = reinterpret_cast<float4*>(a.Y + (size_t)t * a.H);
-  for (int v = threadIdx.x; v < nv; v += blockDim.x) {
+  for (int v = v0 + threadIdx.x; v < v1; v += blockDim.x) {
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int j = 0; j < a.k; ++j) {
       const int r = s_row[j];
@@ -120,7 +123,13 @@ __global__ void __launch_bounds__(kMaxE) balance_stats_kernel(StatsArgs a) {
 }  // namespace
 
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t s) {
-  combine_kernel<<<a.T, 256, 0, s>>>(a);
+  // CTA per token and column chunk: a small batch is split along H so that the GPU gets
+  // about two CTAs per SM, each chunk at least 256 float4 wide
+  const int nv = a.H / 4;
+  const int ymax = nv / 256 > 0 ? nv / 256 : 1;
+  int ysplit = (2 * kGridSms + a.T - 1) / (a.T > 0 ? a.T : 1);
+  ysplit = ysplit < 1 ? 1 : (ysplit > ymax ? ymax : ysplit);
+  combine_kernel<<<dim3(a.T, ysplit), 256, 0, s>>>(a);
   return cudaGetLastError();
 }
 

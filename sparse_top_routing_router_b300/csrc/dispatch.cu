@@ -121,6 +121,9 @@ __global__ void __launch_bounds__(kChunk) dispatch_scatter_kernel(DispatchArgs a
   }
 }
 
+// Warp per token and column chunk: the token's row is read once (16-byte vectors) and
+// written to each of its kept rows.  gridDim.y splits the row into chunks so that a
+// small batch still gives every SM several warps.
 template <int VEC_BYTES>
 __global__ void __launch_bounds__(256) dispatch_gather_kernel(DispatchArgs a,
                                                               int row_bytes) {
@@ -135,10 +138,12 @@ __global__ void __launch_bounds__(256) dispatch_gather_kernel(DispatchArgs a,
   }
   if (nk == 0) return;
   const int nvec = row_bytes / 16;
+  const int per = (nvec + gridDim.y - 1) / gridDim.y;
+  const int v0 = blockIdx.y * per, v1 = min(nvec, v0 + per);
   const uint4* src = reinterpret_cast<const uint4*>(static_cast<const char*>(a.X) +
                                                     (size_t)t * row_bytes);
   char* dst = static_cast<char*>(a.Xperm);
-  for (int v = lane; v < nvec; v += 32) {
+  for (int v = v0 + lane; v < v1; v += 32) {
     const uint4 x = src[v];
     for (int q = 0; q < nk; ++q)
       reinterpret_cast<uint4*>(dst + (size_t)rows[q] * row_bytes)[v] = x;
@@ -168,7 +173,14 @@ cudaError_t launch_dispatch_scatter(const DispatchArgs& a, cudaStream_t s) {
 cudaError_t launch_dispatch_gather(const DispatchArgs& a, cudaStream_t s) {
   const int elt = a.x_dtype == MOE_DTYPE_BF16 ? 2 : 4;
   const int row_bytes = a.H * elt;
-  dispatch_gather_kernel<16><<<(a.T + 7) / 8, 256, 0, s>>>(a, row_bytes);
+  // about 32 warps per SM in all: split rows into chunks of at least 32 vectors when the
+  // batch alone gives fewer
+  const int nvec = row_bytes / 16;
+  const long long want = (long long)kGridSms * 32;
+  int ysplit = (int)((want + a.T - 1) / (a.T > 0 ? a.T : 1));
+  const int ymax = nvec / 32 > 0 ? nvec / 32 : 1;
+  ysplit = ysplit < 1 ? 1 : (ysplit > ymax ? ymax : ysplit);
+  dispatch_gather_kernel<16><<<dim3((a.T + 7) / 8, ysplit), 256, 0, s>>>(a, row_bytes);
   return cudaGetLastError();
 }
 

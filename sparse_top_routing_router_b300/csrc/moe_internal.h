@@ -16,6 +16,7 @@ constexpr int kMaxE = 512;
 constexpr int kMaxK = 32;
 constexpr size_t kWsHeader = 256;     // status word + padding
 constexpr int kDispatchChunk = 256;   // tokens per dispatch CTA
+constexpr int kGridSms = 148;         // B300 SMs: sizes the grids of the small-batch splits
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 

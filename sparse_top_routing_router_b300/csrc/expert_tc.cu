@@ -670,9 +670,10 @@ cudaError_t launch_tc(const ExpertArgs& a, EncodeTiledFn enc, bool* encode_faile
 }
 
 // CTA pairs pay off for large experts (>= 512 rows on average).  For smaller ones the
-// 256-row pair tile pads too much (DSV3-shaped prefill, median 130 rows: same-call A/B
-// 7.6 ms single-CTA vs 8.3 ms pairs per forward), and splitting a group between a pair
-// launch and a single-CTA launch streams its weights from HBM twice.
+// 256-row pair tile pads too much (DSV3-shaped prefill, groups of 0 to 2113 rows: same-call
+// A/B 7.6 ms single-CTA vs 8.3 ms pairs per forward).  Splitting a group between a pair
+// launch and a single-CTA launch streams its weights from HBM twice, and sending whole
+// groups to one launch or the other gained at most 1 % under the power cap.
 bool use_pairs(const ExpertArgs& a) {
   return (long long)a.T * a.k >= 512LL * a.E && a.num_sms >= 2;
 }

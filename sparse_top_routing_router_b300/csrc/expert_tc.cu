@@ -72,6 +72,7 @@ struct TcParams {
   int a_kmod;
   float2* logits;       // splits == 1: (l, 0) per (token, expert)
   float* logits_part;   // splits > 1: fp32 partial per (slice, token, expert)
+  int swap_rows;        // single CTA: tails of at most this many rows swap operands (0: none)
   int pieces;           // ROUTER: 3 = per 64 h one X box and three W_g-piece boxes;
                         // 1 = reduction over [X, X, X] . [hi; mid; lo] (K = 3H)
   uint32_t piece_bytes; // ROUTER, pieces == 3: bytes of one W_g-piece box
@@ -126,6 +127,31 @@ __device__ __forceinline__ TileInfo decode_tile(const Smem<PAIR>& S, int tile, i
   return ti;
 }
 
+// Tiny tail tiles of the single-CTA kernel (at most kSwapRows rows left in the group, as
+// in nearly every group of a decode-sized batch) swap the operands:
+// D^T = W_box . X^T, one MMA per 128-row weight box, M = 128 weight rows and N = the
+// live rows rounded up to 16.  A normal tile would spend a full M = 128 MMA on a handful
+// of rows; the swapped one does about an eighth of the multiply-adds (less power under
+// the board's cap) and reads fewer operand bytes.  Swapping larger tails was slower:
+// every M = 128 MMA still reads its whole weight operand from shared memory, so two
+// swapped MMAs per k-step cost as much as one full tile once N passes ~64.  Only batches
+// of under 16 rows per expert on average use them (TcParams::swap_rows): in a skewed
+// prefill (DSV3-shaped) the faster tiny tiles let the CTAs that share a weight tile drift
+// apart, more weight loads then come from HBM, and the forward was 3 % slower (while the
+// decode-sized layer gained 1.5 %).  The TMA loads are those of a normal tile.
+// Accumulator columns: box 0 (gate, or W_down rows n0..) at 0, box 1 (up, or W_down rows
+// n0+128..) at kSwapCol1.
+constexpr int kSwapRows = 16;
+constexpr int kSwapCol1 = 128;
+
+__device__ __forceinline__ bool is_swapped_tail(const TileInfo& ti, int swap_rows) {
+  return ti.rows - ti.m0 <= swap_rows;
+}
+
+__device__ __forceinline__ int swap_cols(const TileInfo& ti) {
+  return (ti.rows - ti.m0 + 15) & ~15;   // 16..kSwapRows rounded up to 16
+}
+
 __device__ __forceinline__ float silu_mul(float g, float u) {
   return g / (1.f + __expf(-g)) * u;
 }
@@ -135,7 +161,9 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   return *reinterpret_cast<const uint32_t*>(&v);
 }
 
-template <int MODE, bool PAIR>
+// SWAP: single-CTA launches of decode-sized batches, whose tiny tails swap operands; a
+// separate instantiation, so that the other kernels keep their code unchanged.
+template <int MODE, bool PAIR, bool SWAP = false>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap mA,
                         const __grid_constant__ CUtensorMap mA_sh,
@@ -346,10 +374,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t idesc = MODE == ROUTER ? idesc_bf16_f32(128, p.n_tile) : C::kIdesc;
     for (int tile = unit; tile < total && ok; tile += n_units) {
       int kb_lo = 0, kb_hi = nkb;
+      bool swap = false;
+      uint32_t sw_idesc = 0;
       if (MODE == ROUTER) {
         const TileInfo ti = decode_tile<PAIR>(S, tile, p.n_tile, n_tiles_n);
         kb_lo = (int)((long long)nkb * ti.z / p.splits);
         kb_hi = (int)((long long)nkb * (ti.z + 1) / p.splits);
+      } else if (SWAP) {
+        const TileInfo ti = decode_tile<PAIR>(S, tile, p.n_tile, n_tiles_n);
+        swap = is_swapped_tail(ti, p.swap_rows);
+        if (swap) sw_idesc = idesc_bf16_f32(128, swap_cols(ti));
       }
       const bool got = PAIR ? mbar_wait_cluster(&S.tempty[acc], acc_phase ^ 1u, abort_flag, lim)
                             : mbar_wait(&S.tempty[acc], acc_phase ^ 1u, abort_flag, lim);
@@ -377,6 +411,15 @@ __global__ void __launch_bounds__(kThreads, 1)
               const uint32_t accum = (kb != kb_lo || kk != 0 || q != 0) ? 1u : 0u;
               umma_bf16(d, adesc + 2 * kk, bq + 2 * kk, idesc, accum);
             }
+          }
+        } else if (SWAP && MODE != ROUTER && swap) {
+          // tiny tail: each weight box is the M = 128 operand, the rows the N operand
+          const uint64_t bdesc1 = sdesc_kmajor_sw128(a_addr + 2 * kBoxBytes);
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            const uint32_t accum = (kb != kb_lo || kk != 0) ? 1u : 0u;
+            umma_bf16(d, bdesc + 2 * kk, adesc + 2 * kk, sw_idesc, accum);
+            umma_bf16(d + kSwapCol1, bdesc1 + 2 * kk, adesc + 2 * kk, sw_idesc, accum);
           }
         } else {
 #pragma unroll
@@ -431,7 +474,35 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int m = ti.m0 + r_in_tile;
       const bool valid = m < ti.rows;
       const bool sh = ti.g >= p.E;
-      if (MODE == ROUTER) {
+      if (SWAP && MODE != ROUTER && is_swapped_tail(ti, p.swap_rows)) {
+        // D^T: this lane holds weight row q*32+lane of each box, the columns are rows
+        const int r = ti.rows - ti.m0;
+        const int nn = q * 32 + lane;
+        uint32_t v0[32], v1[32];
+        tmem_ld32(tb, v0);                 // r <= kSwapRows <= 32: one load per box
+        tmem_ld32(tb + kSwapCol1, v1);
+        tmem_ld_wait();
+        if (MODE == GATE_UP) {
+          if (ti.n0 + nn < p.N) {
+            __nv_bfloat16* dst = p.h + ((size_t)ti.out0 + ti.m0) * p.N + ti.n0 + nn;
+#pragma unroll
+            for (int i = 0; i < kSwapRows; ++i)
+              if (i < r)
+                dst[(size_t)i * p.N] = __float2bfloat16_rn(
+                    silu_mul(__uint_as_float(v0[i]), __uint_as_float(v1[i])));
+          }
+        } else {
+          float* dst = (sh ? p.O_shared : p.O) + ((size_t)ti.out0 + ti.m0) * p.N + ti.n0 + nn;
+          const bool ok0 = ti.n0 + nn < p.N, ok1 = ti.n0 + 128 + nn < p.N;
+#pragma unroll
+          for (int i = 0; i < kSwapRows; ++i) {
+            if (i < r) {
+              if (ok0) dst[(size_t)i * p.N] = __uint_as_float(v0[i]);
+              if (ok1) dst[(size_t)i * p.N + 128] = __uint_as_float(v1[i]);
+            }
+          }
+        }
+      } else if (MODE == ROUTER) {
         // one slice: the logits as (l, 0) pairs; several: fp32 partials for the reduce
         const size_t cell = ((size_t)ti.z * p.T + m) * p.N + ti.n0;
 #pragma unroll 1
@@ -629,6 +700,8 @@ cudaError_t launch_tc(const ExpertArgs& a, EncodeTiledFn enc, bool* encode_faile
   p.a_kmod = K;
   p.logits = nullptr;
   p.logits_part = nullptr;
+  // decode-sized batches (under 16 rows per expert on average): swap the tiny tails
+  p.swap_rows = (!PAIR && (long long)a.T * a.k < 16LL * a.E) ? kSwapRows : 0;
   p.pieces = 1;
   p.piece_bytes = 0;
   p.router_tx = 0;
@@ -641,7 +714,8 @@ cudaError_t launch_tc(const ExpertArgs& a, EncodeTiledFn enc, bool* encode_faile
       (Tk + TM - 1) / TM + a.E + (a.has_shared ? (a.T + TM - 1) / TM : 0);
   const long long tiles_bound = m_tiles_bound * n_tiles_n;
   const size_t smem = sizeof(Smem<PAIR>) + 1024;
-  auto* fn = grouped_gemm_kernel<MODE, PAIR>;
+  auto* fn = p.swap_rows > 0 ? grouped_gemm_kernel<MODE, PAIR, !PAIR>
+                             : grouped_gemm_kernel<MODE, PAIR, false>;
   cudaError_t e =
       cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;

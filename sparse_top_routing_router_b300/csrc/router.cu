@@ -748,7 +748,7 @@ cudaError_t launch_select_nj(const RouterArgs& a, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   // the listed rows are few; most of these CTAs find nothing to do and exit
   const int sms = a.num_sms > 0 ? a.num_sms : 1;
-  const int grid = a.T < 2 * sms ? a.T : 2 * sms;
+  const int grid = a.T < 8 * sms ? a.T : 8 * sms;
   router_refine_kernel<TX, NJ><<<grid, kRefineThreads, 0, s>>>(a);
   return cudaGetLastError();
 }

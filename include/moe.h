@@ -115,9 +115,12 @@ int moe_capacity(double c, int T, int k, int E);
  *   key_gap    [T] fp32 out (nullable): key_(k) - key_(k+1) of the row (+inf if k == E)
  *   prob_colsum[E] fp64 out (nullable): sum over tokens of p[t, e] (softmax row, or the
  *              sigmoid affinities normalised over the row); zeroed by the call
- * Selection is exact: logits are computed in fp32 with compensated accumulation, and
- * any row whose k-th/(k+1)-th margin falls inside the fp32 error bound is re-decided
- * from float64 dot products.  Ties go to the lower expert index. */
+ * Selection is exact: the logits are fp32 (bf16 X with E % 8 == 0, H % 64 == 0 and
+ * T >= 256: tensor cores over exact bf16 pieces of W_g, accumulation chains of at most
+ * 3072 products; otherwise CUDA-core fp32 with 32-term blocks and compensated
+ * accumulation), and any row whose k-th/(k+1)-th margin falls inside their error bound
+ * is re-decided from dot products carried to ~48 significant bits (error-free products,
+ * double-fp32 sums).  Ties go to the lower expert index. */
 int moe_router_topk(moe_ctx* ctx, const moe_router_desc* d, const void* X,
                     const float* Wg, const float* bias, const float* logit_bias,
                     int32_t* topk_idx, float* topk_gate, float* key_gap,

@@ -20,8 +20,8 @@ from sparse_top_routing_router_b300.inputs import make_inputs
 
 pytestmark = pytest.mark.gpu
 
-EPS_TENSOR = 2.0 ** -17     # bound used for tensor-core logits
-EPS_CUDA = 2.0 ** -19       # bound used for CUDA-core logits
+EPS_TENSOR = 2.0 ** -17     # half the bound the selection assumes for tensor-core logits
+EPS_CUDA = 2.0 ** -19       # the bound the selection assumes for CUDA-core logits
 
 
 def _run(cfg, ctx):

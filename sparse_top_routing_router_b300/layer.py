@@ -95,12 +95,16 @@ class MoELayer:
 
     def forward_host(self, X_host: torch.Tensor, Y_host: torch.Tensor,
                      X_dev: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
-        """Host X (pinned) -> device, forward, device Y -> host Y (pinned)."""
+        """Host X (pinned) -> device, forward, device Y -> host Y (pinned), all three on
+        `stream` (default: the current stream).  Returns once they are enqueued:
+        synchronise the stream before reading Y_host."""
+        s = torch.cuda.current_stream(self.dev) if stream is None else stream
         if X_dev is None:
             X_dev = torch.empty_like(X_host, device=self.dev)
-        X_dev.copy_(X_host, non_blocking=True)
-        Y = self.forward(X_dev, stream=stream)
-        Y_host.copy_(Y, non_blocking=True)
+        with torch.cuda.stream(s):
+            X_dev.copy_(X_host, non_blocking=True)
+            Y = self.forward(X_dev, stream=s)
+            Y_host.copy_(Y, non_blocking=True)
         return Y_host
 
     def host_pipeline(self, X_host: torch.Tensor, Y_host: List[torch.Tensor], steps: int,

@@ -202,3 +202,19 @@ def test_bounded_wait_timeout_is_reported(ctx):
     assert run.status == 0
     ref = P.oracle_route(run)
     P.check_output(run, ref)
+
+
+def test_forward_host_matches_device(ctx):
+    """The end-to-end call (pinned host X in, host Y out, on a side stream) returns the
+    device forward's Y."""
+    cfg = _small(T=96, H=128, shared=True)
+    d = make_inputs(cfg, device="cuda")
+    layer = MoELayer(cfg, d, ctx=ctx)
+    Y_dev = layer.forward(d["X"]).clone()
+    X_host = d["X"].cpu().pin_memory()
+    Y_host = torch.empty(cfg.T, cfg.H, dtype=torch.float32, pin_memory=True)
+    s = torch.cuda.Stream()
+    layer.forward_host(X_host, Y_host, stream=s)
+    s.synchronize()
+    assert torch.equal(Y_host, Y_dev.cpu())
+    assert layer.device_status() == 0

@@ -152,6 +152,18 @@ __device__ __forceinline__ int swap_cols(const TileInfo& ti) {
   return (ti.rows - ti.m0 + 15) & ~15;   // 16..kSwapRows rounded up to 16
 }
 
+// CTA pairs: a group's last tile of at most 128 rows runs as M = 128 (64 rows from each
+// CTA) instead of M = 256.  In that shape each CTA's TMEM holds its 64 rows twice over:
+// lanes 0-63 with accumulator columns 0-127 and lanes 64-127 with columns 128-255, both in
+// TMEM columns 0-127 (an in-bounds probe of the instruction's data-path layout
+// established this).  Same-call A/B on the Mixtral-shaped layer (8 groups of 969-1073
+// rows, 5 of them with a tail of at most 128): 2.52 ms per forward before, 2.49 with half
+// tiles, 2.53 with the 64-row weight boxes alone.
+template <bool PAIR>
+__device__ __forceinline__ bool half_tile(const TileInfo& ti) {
+  return PAIR && ti.rows - ti.m0 <= 128;
+}
+
 __device__ __forceinline__ float silu_mul(float g, float u) {
   return g / (1.f + __expf(-g)) * u;
 }
@@ -287,7 +299,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const TileInfo ti = decode_tile<PAIR>(S, tile, p.n_tile, n_tiles_n);
       const bool sh = (MODE == ROUTER) || ti.g >= p.E;
       const CUtensorMap* a_map = sh ? &mA_sh : &mA;
-      const int ay = ti.row0 + ti.m0 + (PAIR ? 128 * (int)rank : 0);
+      // a pair's half tile (M = 128) takes 64 rows from each CTA
+      const int ay = ti.row0 + ti.m0 + (PAIR ? (half_tile<PAIR>(ti) ? 64 : 128) * (int)rank : 0);
       const int kb_lo = (MODE == ROUTER) ? (int)((long long)nkb * ti.z / p.splits) : 0;
       const int kb_hi = (MODE == ROUTER) ? (int)((long long)nkb * (ti.z + 1) / p.splits) : nkb;
       for (int kb = kb_lo; kb < kb_hi; ++kb) {
@@ -334,18 +347,26 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (rank == 0) mbar_arrive_expect_tx(&S.full[stage], C::kTxBytes);
           const uint32_t bar = mapa_shared(smem_u32(&S.full[stage]), 0);
           tma_load_2d_pair(st, a_map, bar, kx, ay);
-          // weight half of this CTA: GATE_UP rank 0 = gate rows, rank 1 = up rows;
-          // DOWN rank r = output rows n0 + 128 r
-          const CUtensorMap* b;
-          int ny = ti.n0;
+          // weight half of this CTA.  GATE_UP: gate rows n0 + 64 r .. + 63, then the up rows
+          // of the same outputs (64-row boxes), so that the B operand reads
+          // [gate 0-63 | up 0-63 | gate 64-127 | up 64-127] and every TMEM lane holds the
+          // gate and up of the same outputs in either tile height.  DOWN: output rows
+          // n0 + 128 r .. + 127.
           if (MODE == GATE_UP) {
-            b = rank == 0 ? (sh ? &mB0_sh : &mB0) : (sh ? &mB1_sh : &mB1);
+            const int ny = ti.n0 + 64 * (int)rank;
+            if (sh) {
+              tma_load_2d_pair(st + kBoxBytes, &mB0_sh, bar, kx, ny);
+              tma_load_2d_pair(st + kBoxBytes + kBoxBytes / 2, &mB1_sh, bar, kx, ny);
+            } else {
+              tma_load_3d_pair(st + kBoxBytes, &mB0, bar, kx, ny, ti.g);
+              tma_load_3d_pair(st + kBoxBytes + kBoxBytes / 2, &mB1, bar, kx, ny, ti.g);
+            }
           } else {
-            b = sh ? &mB0_sh : &mB0;
-            ny += 128 * (int)rank;
+            const CUtensorMap* b = sh ? &mB0_sh : &mB0;
+            const int ny = ti.n0 + 128 * (int)rank;
+            if (sh) tma_load_2d_pair(st + kBoxBytes, b, bar, kx, ny);
+            else tma_load_3d_pair(st + kBoxBytes, b, bar, kx, ny, ti.g);
           }
-          if (sh) tma_load_2d_pair(st + kBoxBytes, b, bar, kx, ny);
-          else tma_load_3d_pair(st + kBoxBytes, b, bar, kx, ny, ti.g);
         }
         issued_mask |= 1u << stage;
         issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
@@ -385,6 +406,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         swap = is_swapped_tail(ti, p.swap_rows);
         if (swap) sw_idesc = idesc_bf16_f32(128, swap_cols(ti));
       }
+      uint32_t pair_idesc = C::kIdesc;
+      if (PAIR && half_tile<PAIR>(decode_tile<PAIR>(S, tile, p.n_tile, n_tiles_n)))
+        pair_idesc = idesc_bf16_f32(128, 256);
       const bool got = PAIR ? mbar_wait_cluster(&S.tempty[acc], acc_phase ^ 1u, abort_flag, lim)
                             : mbar_wait(&S.tempty[acc], acc_phase ^ 1u, abort_flag, lim);
       if (!got) {
@@ -425,7 +449,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
             const uint32_t accum = (kb != kb_lo || kk != 0) ? 1u : 0u;
-            if (PAIR) umma_bf16_pair(d, adesc + 2 * kk, bdesc + 2 * kk, C::kIdesc, accum);
+            if (PAIR) umma_bf16_pair(d, adesc + 2 * kk, bdesc + 2 * kk, pair_idesc, accum);
             else umma_bf16(d, adesc + 2 * kk, bdesc + 2 * kk, idesc, accum);
           }
         }
@@ -474,7 +498,58 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int m = ti.m0 + r_in_tile;
       const bool valid = m < ti.rows;
       const bool sh = ti.g >= p.E;
-      if (SWAP && MODE != ROUTER && is_swapped_tail(ti, p.swap_rows)) {
+      if (PAIR && MODE != ROUTER) {
+        // A full tile (M = 256): this lane is row 128 r + q*32 + lane with all 256
+        // accumulator columns.  A half tile (M = 128): row 64 r + (q & 1)*32 + lane, and
+        // accumulator columns 128 (q >> 1) .. + 127 in TMEM columns 0-127.  GATE_UP
+        // accumulator columns run [gate | up] per 64 outputs (see the producer).
+        const bool hf = half_tile<PAIR>(ti);
+        const int row = hf ? 64 * (int)rank + (q & 1) * 32 + lane : 128 * (int)rank + q * 32 + lane;
+        const int mm = ti.m0 + row;
+        const bool ok_row = mm < ti.rows;
+        const int hc0 = hf ? (q >> 1) : 0, hc1 = hf ? (q >> 1) : 1;
+#pragma unroll 1
+        for (int hc = hc0; hc <= hc1; ++hc) {
+          const uint32_t tcol = hf ? 0u : 128u * (uint32_t)hc;
+          if (MODE == GATE_UP) {
+            __nv_bfloat16* dst = p.h + ((size_t)ti.out0 + mm) * p.N + ti.n0 + 64 * hc;
+#pragma unroll 1
+            for (int c = 0; c < 64; c += 32) {
+              uint32_t g[32], u[32];
+              tmem_ld32(tb + tcol + c, g);
+              tmem_ld32(tb + tcol + 64 + c, u);
+              tmem_ld_wait();
+              if (ok_row && ti.n0 + 64 * hc + c < p.N) {
+                uint32_t pk[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                  pk[i] = pack_bf16(silu_mul(__uint_as_float(g[2 * i]), __uint_as_float(u[2 * i])),
+                                    silu_mul(__uint_as_float(g[2 * i + 1]),
+                                             __uint_as_float(u[2 * i + 1])));
+                uint4* d4 = reinterpret_cast<uint4*>(dst + c);
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                  d4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+              }
+            }
+          } else {
+            float* dst = (sh ? p.O_shared : p.O) + ((size_t)ti.out0 + mm) * p.N + ti.n0 + 128 * hc;
+#pragma unroll 1
+            for (int c = 0; c < 128; c += 32) {
+              uint32_t v[32];
+              tmem_ld32(tb + tcol + c, v);
+              tmem_ld_wait();
+              if (ok_row && ti.n0 + 128 * hc + c < p.N) {
+                float4* d4 = reinterpret_cast<float4*>(dst + c);
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                  d4[i] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
+                                      __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
+              }
+            }
+          }
+        }
+      } else if (SWAP && MODE != ROUTER && is_swapped_tail(ti, p.swap_rows)) {
         // D^T: this lane holds weight row q*32+lane of each box, the columns are rows
         const int r = ti.rows - ti.m0;
         const int nn = q * 32 + lane;
@@ -615,10 +690,10 @@ bool encode_2d(Enc enc, CUtensorMap* m, const void* base, uint64_t inner, uint64
 }
 
 bool encode_3d(EncodeTiledFn enc, CUtensorMap* m, const void* base, uint64_t inner,
-               uint64_t mid, uint64_t outer) {
+               uint64_t mid, uint64_t outer, uint32_t box_rows = 128) {
   const cuuint64_t dims[3] = {inner, mid, outer};
   const cuuint64_t strides[2] = {inner * 2, inner * mid * 2};
-  const cuuint32_t box[3] = {BK, 128, 1};
+  const cuuint32_t box[3] = {BK, box_rows, 1};
   const cuuint32_t estr[3] = {1, 1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
              box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -665,10 +740,12 @@ cudaError_t launch_tc(const ExpertArgs& a, EncodeTiledFn enc, bool* encode_faile
   if (MODE == GATE_UP) {
     ok &= encode_2d(enc, &mA, a.Xperm, K, Tk);
     ok &= encode_2d(enc, &mA_sh, a.has_shared ? a.X : a.Xperm, K, a.has_shared ? a.T : Tk);
-    ok &= encode_3d(enc, &mB0, a.W_gate, K, N, a.E);
-    ok &= encode_3d(enc, &mB1, a.W_up, K, N, a.E);
-    ok &= encode_2d(enc, &mB0_sh, a.has_shared ? a.Ws_gate : a.W_gate, K, N);
-    ok &= encode_2d(enc, &mB1_sh, a.has_shared ? a.Ws_up : a.W_up, K, N);
+    // pairs load gate and up as 64-row boxes (the [gate | up] per 64 outputs order)
+    const uint32_t wb = PAIR ? 64u : 128u;
+    ok &= encode_3d(enc, &mB0, a.W_gate, K, N, a.E, wb);
+    ok &= encode_3d(enc, &mB1, a.W_up, K, N, a.E, wb);
+    ok &= encode_2d(enc, &mB0_sh, a.has_shared ? a.Ws_gate : a.W_gate, K, N, wb);
+    ok &= encode_2d(enc, &mB1_sh, a.has_shared ? a.Ws_up : a.W_up, K, N, wb);
   } else {
     ok &= encode_2d(enc, &mA, a.h, K, h_rows);
     mA_sh = mA;

@@ -27,6 +27,8 @@
 //   warps 2-5   epilogue: tcgen05.ld 32 columns at a time, SwiGLU or fp32 store
 // Every mbarrier wait is bounded (see ptx.cuh); a timeout sets the status word and the
 // CTA drains what it can of its in-flight copies and MMAs, frees TMEM and returns.
+#include <string.h>
+
 #include "moe_internal.h"
 #include "ptx.cuh"
 
@@ -99,6 +101,12 @@ struct __align__(1024) Smem {
   int grp_out0[kMaxGroups];   // first output row (h, O or O_shared) of the group
 };
 
+// The gate and up weights as 64-row boxes: a CTA pair's half tile takes them in the
+// order [gate 0-63 | up 0-63 | gate 64-127 | up 64-127] (see half_tile).
+struct HalfMaps {
+  CUtensorMap gate, up, gate_sh, up_sh;
+};
+
 struct TileInfo {
   int g, m0, n0, rows, row0, out0, z;
 };
@@ -156,9 +164,9 @@ __device__ __forceinline__ int swap_cols(const TileInfo& ti) {
 // CTA) instead of M = 256.  In that shape each CTA's TMEM holds its 64 rows twice over:
 // lanes 0-63 with accumulator columns 0-127 and lanes 64-127 with columns 128-255, both in
 // TMEM columns 0-127 (an in-bounds probe of the instruction's data-path layout
-// established this).  Same-call A/B on the Mixtral-shaped layer (8 groups of 969-1073
-// rows, 5 of them with a tail of at most 128): 2.52 ms per forward before, 2.49 with half
-// tiles, 2.53 with the 64-row weight boxes alone.
+// established this), and a half tile loads gate and up as 64-row boxes (HalfMaps).
+// Same-call A/Bs on the Mixtral-shaped layer (8 groups of 969-1073 rows, 5 with a tail of
+// at most 128): 2.48-2.52 ms per forward before, 2.46-2.49 with half tiles.
 template <bool PAIR>
 __device__ __forceinline__ bool half_tile(const TileInfo& ti) {
   return PAIR && ti.rows - ti.m0 <= 128;
@@ -182,7 +190,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const __grid_constant__ CUtensorMap mB0,
                         const __grid_constant__ CUtensorMap mB1,
                         const __grid_constant__ CUtensorMap mB0_sh,
-                        const __grid_constant__ CUtensorMap mB1_sh, const TcParams p) {
+                        const __grid_constant__ CUtensorMap mB1_sh,
+                        const __grid_constant__ HalfMaps hm, const TcParams p) {
   using C = Cfg<PAIR>;
   const int kStages = MODE == ROUTER ? p.ring : C::kStages;
   const uint32_t stage_bytes = MODE == ROUTER ? p.stage_bytes : (uint32_t)C::kStageBytes;
@@ -347,20 +356,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (rank == 0) mbar_arrive_expect_tx(&S.full[stage], C::kTxBytes);
           const uint32_t bar = mapa_shared(smem_u32(&S.full[stage]), 0);
           tma_load_2d_pair(st, a_map, bar, kx, ay);
-          // weight half of this CTA.  GATE_UP: gate rows n0 + 64 r .. + 63, then the up rows
-          // of the same outputs (64-row boxes), so that the B operand reads
-          // [gate 0-63 | up 0-63 | gate 64-127 | up 64-127] and every TMEM lane holds the
-          // gate and up of the same outputs in either tile height.  DOWN: output rows
-          // n0 + 128 r .. + 127.
-          if (MODE == GATE_UP) {
+          // weight half of this CTA.  GATE_UP full tile: rank 0 the gate rows, rank 1 the
+          // up rows n0 .. + 127; half tile: gate rows n0 + 64 r .. + 63, then the up rows
+          // of the same outputs (64-row boxes), so that every TMEM lane holds the gate and
+          // up of the same outputs.  DOWN: output rows n0 + 128 r .. + 127.
+          if (MODE == GATE_UP && half_tile<PAIR>(ti)) {
             const int ny = ti.n0 + 64 * (int)rank;
             if (sh) {
-              tma_load_2d_pair(st + kBoxBytes, &mB0_sh, bar, kx, ny);
-              tma_load_2d_pair(st + kBoxBytes + kBoxBytes / 2, &mB1_sh, bar, kx, ny);
+              tma_load_2d_pair(st + kBoxBytes, &hm.gate_sh, bar, kx, ny);
+              tma_load_2d_pair(st + kBoxBytes + kBoxBytes / 2, &hm.up_sh, bar, kx, ny);
             } else {
-              tma_load_3d_pair(st + kBoxBytes, &mB0, bar, kx, ny, ti.g);
-              tma_load_3d_pair(st + kBoxBytes + kBoxBytes / 2, &mB1, bar, kx, ny, ti.g);
+              tma_load_3d_pair(st + kBoxBytes, &hm.gate, bar, kx, ny, ti.g);
+              tma_load_3d_pair(st + kBoxBytes + kBoxBytes / 2, &hm.up, bar, kx, ny, ti.g);
             }
+          } else if (MODE == GATE_UP) {
+            const CUtensorMap* b = rank == 0 ? (sh ? &mB0_sh : &mB0) : (sh ? &mB1_sh : &mB1);
+            if (sh) tma_load_2d_pair(st + kBoxBytes, b, bar, kx, ti.n0);
+            else tma_load_3d_pair(st + kBoxBytes, b, bar, kx, ti.n0, ti.g);
           } else {
             const CUtensorMap* b = sh ? &mB0_sh : &mB0;
             const int ny = ti.n0 + 128 * (int)rank;
@@ -500,16 +512,38 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool sh = ti.g >= p.E;
       if (PAIR && MODE != ROUTER) {
         // A full tile (M = 256): this lane is row 128 r + q*32 + lane with all 256
-        // accumulator columns.  A half tile (M = 128): row 64 r + (q & 1)*32 + lane, and
-        // accumulator columns 128 (q >> 1) .. + 127 in TMEM columns 0-127.  GATE_UP
-        // accumulator columns run [gate | up] per 64 outputs (see the producer).
+        // accumulator columns (GATE_UP: gate 0-127, up 128-255).  A half tile (M = 128):
+        // row 64 r + (q & 1)*32 + lane, and accumulator columns 128 (q >> 1) .. + 127 in
+        // TMEM columns 0-127 (GATE_UP: [gate | up] per 64 outputs, see the producer).
         const bool hf = half_tile<PAIR>(ti);
         const int row = hf ? 64 * (int)rank + (q & 1) * 32 + lane : 128 * (int)rank + q * 32 + lane;
         const int mm = ti.m0 + row;
         const bool ok_row = mm < ti.rows;
         const int hc0 = hf ? (q >> 1) : 0, hc1 = hf ? (q >> 1) : 1;
+        if (MODE == GATE_UP && !hf) {
+          __nv_bfloat16* dst = p.h + ((size_t)ti.out0 + mm) * p.N + ti.n0;
 #pragma unroll 1
-        for (int hc = hc0; hc <= hc1; ++hc) {
+          for (int c = 0; c < 128; c += 32) {
+            uint32_t g[32], u[32];
+            tmem_ld32(tb + c, g);
+            tmem_ld32(tb + 128 + c, u);
+            tmem_ld_wait();
+            if (ok_row && ti.n0 + c < p.N) {
+              uint32_t pk[16];
+#pragma unroll
+              for (int i = 0; i < 16; ++i)
+                pk[i] = pack_bf16(silu_mul(__uint_as_float(g[2 * i]), __uint_as_float(u[2 * i])),
+                                  silu_mul(__uint_as_float(g[2 * i + 1]),
+                                           __uint_as_float(u[2 * i + 1])));
+              uint4* d4 = reinterpret_cast<uint4*>(dst + c);
+#pragma unroll
+              for (int i = 0; i < 4; ++i)
+                d4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+            }
+          }
+        }
+#pragma unroll 1
+        for (int hc = hc0; hc <= hc1 && !(MODE == GATE_UP && !hf); ++hc) {
           const uint32_t tcol = hf ? 0u : 128u * (uint32_t)hc;
           if (MODE == GATE_UP) {
             __nv_bfloat16* dst = p.h + ((size_t)ti.out0 + mm) * p.N + ti.n0 + 64 * hc;
@@ -736,16 +770,22 @@ cudaError_t launch_tc(const ExpertArgs& a, EncodeTiledFn enc, bool* encode_faile
   const int n_tile = (MODE == GATE_UP) ? 128 : 256;
   const int h_rows = Tk + (a.has_shared ? a.T : 0);
   CUtensorMap mA, mA_sh, mB0, mB1, mB0_sh, mB1_sh;
+  HalfMaps hm;
+  memset(&hm, 0, sizeof(hm));
   bool ok = true;
   if (MODE == GATE_UP) {
     ok &= encode_2d(enc, &mA, a.Xperm, K, Tk);
     ok &= encode_2d(enc, &mA_sh, a.has_shared ? a.X : a.Xperm, K, a.has_shared ? a.T : Tk);
-    // pairs load gate and up as 64-row boxes (the [gate | up] per 64 outputs order)
-    const uint32_t wb = PAIR ? 64u : 128u;
-    ok &= encode_3d(enc, &mB0, a.W_gate, K, N, a.E, wb);
-    ok &= encode_3d(enc, &mB1, a.W_up, K, N, a.E, wb);
-    ok &= encode_2d(enc, &mB0_sh, a.has_shared ? a.Ws_gate : a.W_gate, K, N, wb);
-    ok &= encode_2d(enc, &mB1_sh, a.has_shared ? a.Ws_up : a.W_up, K, N, wb);
+    ok &= encode_3d(enc, &mB0, a.W_gate, K, N, a.E);
+    ok &= encode_3d(enc, &mB1, a.W_up, K, N, a.E);
+    ok &= encode_2d(enc, &mB0_sh, a.has_shared ? a.Ws_gate : a.W_gate, K, N);
+    ok &= encode_2d(enc, &mB1_sh, a.has_shared ? a.Ws_up : a.W_up, K, N);
+    if (PAIR) {   // 64-row boxes for the half tiles
+      ok &= encode_3d(enc, &hm.gate, a.W_gate, K, N, a.E, 64);
+      ok &= encode_3d(enc, &hm.up, a.W_up, K, N, a.E, 64);
+      ok &= encode_2d(enc, &hm.gate_sh, a.has_shared ? a.Ws_gate : a.W_gate, K, N, 64);
+      ok &= encode_2d(enc, &hm.up_sh, a.has_shared ? a.Ws_up : a.W_up, K, N, 64);
+    }
   } else {
     ok &= encode_2d(enc, &mA, a.h, K, h_rows);
     mA_sh = mA;
@@ -799,7 +839,7 @@ cudaError_t launch_tc(const ExpertArgs& a, EncodeTiledFn enc, bool* encode_faile
   if (!PAIR) {
     const int grid = (int)(tiles_bound < a.num_sms ? (tiles_bound > 0 ? tiles_bound : 1)
                                                    : a.num_sms);
-    fn<<<grid, kThreads, smem, s>>>(mA, mA_sh, mB0, mB1, mB0_sh, mB1_sh, p);
+    fn<<<grid, kThreads, smem, s>>>(mA, mA_sh, mB0, mB1, mB0_sh, mB1_sh, hm, p);
     return cudaGetLastError();
   }
   const int pairs_max = max_pairs(reinterpret_cast<const void*>(fn), smem, a.num_sms);
@@ -817,7 +857,7 @@ cudaError_t launch_tc(const ExpertArgs& a, EncodeTiledFn enc, bool* encode_faile
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, fn, mA, mA_sh, mB0, mB1, mB0_sh, mB1_sh, p);
+  return cudaLaunchKernelEx(&cfg, fn, mA, mA_sh, mB0, mB1, mB0_sh, mB1_sh, hm, p);
 }
 
 // CTA pairs pay off for large experts (>= 512 rows on average).  For smaller ones the
@@ -895,7 +935,9 @@ cudaError_t launch_router_tc(const RouterArgs& a, EncodeTiledFnR enc, bool* enco
   cudaError_t e =
       cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  fn<<<grid, kThreads, smem, s>>>(mX, mX, mW, mW, mW, mW, p);
+  HalfMaps hm;
+  memset(&hm, 0, sizeof(hm));
+  fn<<<grid, kThreads, smem, s>>>(mX, mX, mW, mW, mW, mW, hm, p);
   return cudaGetLastError();
 }
 

@@ -25,6 +25,8 @@ SMALL = [
     K.scaled(K.SWITCH, name="switch_small", T=1000, H=256, E=16, I=256),
     # E = 40: tensor-core router logits with N = 48 and a partial 32-column epilogue chunk
     K.scaled(K.DSV3_PREFILL, name="dsv3_small_e40", T=300, H=256, E=40, I=128, k=6),
+    # E = 320 experts: tensor-core router logits over two 256-wide expert tiles
+    K.scaled(K.DSV3_PREFILL, name="dsv3_small_e320", T=400, H=256, E=320, I=128, k=6),
     # decode-sized: a few rows per expert (operand-swapped tiny tiles) plus the shared expert
     K.scaled(K.DSV3_PREFILL, name="dsv3_small_decode", T=24, H=256, E=64, I=128),
     # uneven group sizes (0 to 583 rows of 2400) beside a 600-row shared expert

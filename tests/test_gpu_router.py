@@ -54,6 +54,8 @@ def ctx():
     (K.scaled(K.DSV3_PREFILL, name="dsv3_router_tc", T=1024), EPS_TENSOR),
     (K.scaled(K.SWITCH, name="switch_router_tc", T=2048), EPS_TENSOR),
     (K.scaled(K.MIXTRAL, name="mixtral_router_tc", T=1024), EPS_TENSOR),   # MMA N = 16
+    # E = 320: two 256-wide expert tiles, the second one partly past the last expert
+    (K.scaled(K.DSV3_PREFILL, name="e320_router_tc", T=512, E=320, k=6), EPS_TENSOR),
     (K.DSV3_DECODE, EPS_CUDA),                                      # split-K CUDA cores
     (K.scaled(K.MIXTRAL, name="mixtral_router", T=200), EPS_CUDA),   # narrow CUDA cores
 ], ids=lambda v: getattr(v, "name", str(v)))

@@ -99,6 +99,7 @@ struct __align__(1024) Smem {
   int grp_rows[kMaxGroups];
   int grp_row0[kMaxGroups];   // first A row of the group
   int grp_out0[kMaxGroups];   // first output row (h, O or O_shared) of the group
+  float stage[4][32][33];     // epilogue: one 32 x 32 fp32 chunk per warp, padded rows
 };
 
 // The gate and up weights as 64-row boxes: a CTA pair's half tile takes them in the
@@ -170,6 +171,27 @@ __device__ __forceinline__ int swap_cols(const TileInfo& ti) {
 template <bool PAIR>
 __device__ __forceinline__ bool half_tile(const TileInfo& ti) {
   return PAIR && ti.rows - ti.m0 <= 128;
+}
+
+// A warp's 32 rows x 32 fp32 columns (thread = row, v = its 32 columns, as tcgen05.ld
+// 32x32b returns them) to global memory row-contiguously: through the warp's padded
+// shared-memory chunk (conflict-free both ways), then every store writes 4 rows x 128 B.
+// A direct store from the TMEM layout would touch 32 rows x 16 B per instruction.
+// dst0 = the chunk's (row 0, column 0); rows from nrows on are skipped.
+__device__ __forceinline__ void store_chunk_f32(float (*stg)[33], const uint32_t (&v)[32],
+                                                int lane, float* dst0, size_t ld, int nrows) {
+#pragma unroll
+  for (int i = 0; i < 32; ++i) stg[lane][i] = __uint_as_float(v[i]);
+  __syncwarp();
+  const int f = lane & 7;
+#pragma unroll
+  for (int pass = 0; pass < 8; ++pass) {
+    const int r = pass * 4 + (lane >> 3);
+    if (r < nrows)
+      *reinterpret_cast<float4*>(dst0 + (size_t)r * ld + 4 * f) =
+          make_float4(stg[r][4 * f], stg[r][4 * f + 1], stg[r][4 * f + 2], stg[r][4 * f + 3]);
+  }
+  __syncwarp();
 }
 
 __device__ __forceinline__ float silu_mul(float g, float u) {
@@ -567,19 +589,18 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
             }
           } else {
-            float* dst = (sh ? p.O_shared : p.O) + ((size_t)ti.out0 + mm) * p.N + ti.n0 + 128 * hc;
+            // this warp's 32 rows start at row - lane
+            const int wrow = ti.m0 + row - lane;
+            const int nrows = min(32, max(0, ti.rows - wrow));
+            float* dst = (sh ? p.O_shared : p.O) + ((size_t)ti.out0 + wrow) * p.N + ti.n0 +
+                         128 * hc;
 #pragma unroll 1
             for (int c = 0; c < 128; c += 32) {
               uint32_t v[32];
               tmem_ld32(tb + tcol + c, v);
               tmem_ld_wait();
-              if (ok_row && ti.n0 + 128 * hc + c < p.N) {
-                float4* d4 = reinterpret_cast<float4*>(dst + c);
-#pragma unroll
-                for (int i = 0; i < 8; ++i)
-                  d4[i] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
-                                      __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
-              }
+              if (ti.n0 + 128 * hc + c < p.N)
+                store_chunk_f32(S.stage[q], v, lane, dst + c, p.N, nrows);
             }
           }
         }
@@ -672,20 +693,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       } else {
-        float* dst = (sh ? p.O_shared : p.O) + ((size_t)ti.out0 + m) * p.N;
-        dst += ti.n0;
+        // this warp's 32 rows start at m - lane
+        const int wrow = m - lane;
+        const int nrows = min(32, max(0, ti.rows - wrow));
+        float* dst = (sh ? p.O_shared : p.O) + ((size_t)ti.out0 + wrow) * p.N + ti.n0;
 #pragma unroll 1
         for (int c = 0; c < 256; c += 32) {
           uint32_t v[32];
           tmem_ld32(tb + c, v);
           tmem_ld_wait();
-          if (valid && ti.n0 + c < p.N) {
-            float4* d4 = reinterpret_cast<float4*>(dst + c);
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-              d4[i] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
-                                  __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
-          }
+          if (ti.n0 + c < p.N) store_chunk_f32(S.stage[q], v, lane, dst + c, p.N, nrows);
         }
       }
       tc_fence_before();

@@ -23,14 +23,18 @@ Sources (page title and section):
         expert.
   [SN]  "Mixture of Experts (MoE)" study notes, Case 1: top-k pseudo-code (softmax over
         the k chosen values).
+  [P1]  "MoE 03: efficiency frontiers", DeepSeek's hardware-aware design: each token
+        goes to at most 4 of the 8 nodes that hold the experts.
 
-Readings where the pages are silent (each is listed in the design doc):
+Readings where the pages are silent:
   * ties in top-k go to the lower expert index; the chosen set is written in ascending
     expert order (the pages define S as a set);
   * capacity keeps the lowest token indices of each expert;
   * a dropped slot contributes nothing; the other gates are not renormalised;
   * f_i counts router choices before capacity, f_i = m_i / (T*k);
   * for sigmoid scoring, p_i averages the row-normalised affinities s / sum_e s;
+  * group-limited routing scores a group by its k/M largest UNBIASED affinities, and
+    its groups are runs of consecutive expert indices;
   * SwiGLU expert: h = SiLU(x W_gate) * (x W_up), y = h W_down, SiLU(z) = z*sigmoid(z),
     no biases.
 
@@ -117,6 +121,60 @@ def select_topk(key: np.ndarray, k: int) -> Tuple[np.ndarray, np.ndarray]:
         gap = np.full(T, np.inf)
     idx = np.sort(order[:, :k], axis=1)
     return idx.astype(np.int64), gap
+
+
+def routing_affinity(l: np.ndarray, score: str) -> np.ndarray:
+    """The affinity of token t for expert e, unbiased: softmax(l)_e for softmax scoring,
+    s = sigmoid(l_e) for sigmoid scoring  [LI §14.2.1 step 2; §14.2.3 eq. 16, where the
+    bias enters only the top-k comparison]."""
+    if score == "softmax":
+        return softmax_rows(l)
+    if score == "sigmoid":
+        return sigmoid(l)
+    raise ValueError(score)
+
+
+def group_limited_topk(key: np.ndarray, affinity: np.ndarray, k: int, n_groups: int,
+                       topk_groups: int) -> Tuple[np.ndarray, np.ndarray]:
+    """Node-limited (group-limited) routing  [LI §14.2.3, node-limited routing; P1].
+
+    The E experts sit in n_groups equal groups of consecutive indices (the experts of
+    one node).  A group's score is the sum of its k / topk_groups largest affinities.
+    Each token may use only the experts of its topk_groups best groups (ties to the
+    lower group index); among those it takes the k largest keys (ties to the lower
+    expert index).  The affinity is the unbiased one (routing_affinity): the page
+    scores a node by its experts' affinities, and the selection bias enters only the
+    top-k comparison of experts.
+
+    Returns idx[T, k] (ascending expert index) and gap[T] = the smaller of the group
+    margin S_(M) - S_(M+1) and the key margin key_(k) - key_(k+1) among the allowed
+    experts (a margin that does not exist counts as +inf).
+    """
+    T, E = key.shape
+    G, M = n_groups, topk_groups
+    if G < 1 or E % G or not 1 <= M <= G or k % M or k // M > E // G or M * (E // G) < k:
+        raise ValueError("unsupported group-limited routing shape")
+    gs, n = E // G, k // M
+    rows = np.arange(T)
+    per_group = np.asarray(affinity, dtype=f64).reshape(T, G, gs)
+    top_n = -np.sort(-per_group, axis=2)[:, :, :n]          # descending
+    S = top_n.sum(axis=2)                                   # [T, G] group scores
+    g_order = np.argsort(-S, axis=1, kind="stable")
+    if M < G:
+        g_gap = S[rows, g_order[:, M - 1]] - S[rows, g_order[:, M]]
+    else:
+        g_gap = np.full(T, np.inf)
+    allowed_g = np.zeros((T, G), dtype=bool)
+    allowed_g[rows[:, None], g_order[:, :M]] = True
+    allowed = np.repeat(allowed_g, gs, axis=1)
+    masked = np.where(allowed, key, -np.inf)
+    order = np.argsort(-masked, axis=1, kind="stable")
+    if M * gs > k:
+        k_gap = key[rows, order[:, k - 1]] - key[rows, order[:, k]]
+    else:
+        k_gap = np.full(T, np.inf)
+    idx = np.sort(order[:, :k], axis=1)
+    return idx.astype(np.int64), np.minimum(g_gap, k_gap)
 
 
 def gates_for(l: np.ndarray, idx: np.ndarray, score: str, renorm: bool) -> np.ndarray:
@@ -246,11 +304,17 @@ def balance_stats(counts: np.ndarray, prob_colsum: np.ndarray, T: int, k: int,
 # ---------------------------------------------------------------------------
 
 def route(X, Wg, k: int, score: str, renorm: bool, bias=None, logit_bias=None,
-          C: Optional[int] = None) -> Dict[str, np.ndarray]:
-    """Steps 2-4 on every token (capacity is a property of the whole batch)."""
+          C: Optional[int] = None, n_groups: int = 0,
+          topk_groups: int = 0) -> Dict[str, np.ndarray]:
+    """Steps 2-4 on every token (capacity is a property of the whole batch).  With
+    n_groups > 1 the selection is group-limited (group_limited_topk)."""
     l = router_logits(X, Wg, logit_bias)
     key = selection_keys(l, score, bias)
-    idx, gap = select_topk(key, k)
+    if n_groups > 1:
+        idx, gap = group_limited_topk(key, routing_affinity(l, score), k, n_groups,
+                                      topk_groups)
+    else:
+        idx, gap = select_topk(key, k)
     g = gates_for(l, idx, score, renorm)
     d = dispatch(idx, Wg.shape[1], C)
     d.update(logits=l, key=key, idx=idx, gap=gap, gate=g,

@@ -340,3 +340,94 @@ def test_route_probabilities_and_gap():
     np.testing.assert_allclose(r["gap"], srt[:, 1] - srt[:, 2], atol=0)
     r = O.route(X, Wg, 2, "sigmoid", True, bias=np.zeros(4))
     np.testing.assert_allclose(r["prob_colsum"].sum(), 10.0, atol=1e-12)
+
+
+# ---------------------------------------------------------------- group-limited routing
+
+def _group_limited_brute(key, aff, k, G, M):
+    """Group-limited top-k of one row as maxima over subsets: a group's score is the
+    largest sum of k/M of its affinities; the groups used are the M-subset with the
+    largest total score; the experts are the k-subset of the allowed ones with the
+    largest total key.  (Distinct random values: every maximiser is unique.)"""
+    E = len(key)
+    gs, n = E // G, k // M
+    score = [max(sum(c) for c in itertools.combinations(aff[g * gs:(g + 1) * gs], n))
+             for g in range(G)]
+    groups = max(itertools.combinations(range(G), M), key=lambda c: sum(score[g] for g in c))
+    allowed = [e for e in range(E) if e // gs in groups]
+    chosen = max(itertools.combinations(allowed, k), key=lambda c: sum(key[e] for e in c))
+    others_g = [score[g] for g in range(G) if g not in groups]
+    g_gap = min(score[g] for g in groups) - max(others_g) if others_g else math.inf
+    others_e = [key[e] for e in allowed if e not in chosen]
+    k_gap = min(key[e] for e in chosen) - max(others_e) if others_e else math.inf
+    return sorted(chosen), min(g_gap, k_gap)
+
+
+@pytest.mark.parametrize("E,G,M,k", [(12, 4, 2, 4), (12, 3, 1, 2), (16, 4, 2, 2),
+                                     (12, 6, 3, 3), (8, 4, 2, 4)])
+def test_group_limited_brute_force(E, G, M, k):
+    rng = np.random.default_rng(E * 100 + G * 10 + M)
+    T = 25
+    aff = rng.random((T, E))
+    key = aff + rng.standard_normal((T, E)) * 0.3     # a selection bias reorders the keys
+    idx, gap = O.group_limited_topk(key, aff, k, G, M)
+    for t in range(T):
+        want, want_gap = _group_limited_brute(key[t], aff[t], k, G, M)
+        assert idx[t].tolist() == want
+        assert gap[t] == pytest.approx(want_gap, abs=1e-12) if math.isfinite(want_gap) \
+            else gap[t] == math.inf
+
+
+def test_group_limited_reduces_to_plain_topk():
+    rng = np.random.default_rng(5)
+    l = rng.standard_normal((40, 16))
+    key = O.selection_keys(l, "sigmoid", rng.standard_normal(16) * 0.1)
+    aff = O.routing_affinity(l, "sigmoid")
+    plain_idx, plain_gap = O.select_topk(key, 4)
+    for G, M in [(1, 1), (4, 4), (2, 2)]:     # every group allowed
+        idx, gap = O.group_limited_topk(key, aff, 4, G, M)
+        assert np.array_equal(idx, plain_idx)
+        np.testing.assert_array_equal(gap, plain_gap)
+
+
+def test_group_limited_hand_example():
+    # 8 experts in 4 groups of 2, affinities s; k = 2 over M = 2 groups: each group
+    # is scored by its single best affinity (k/M = 1):
+    #   g0 = {0.90, 0.85} -> 0.90, g1 = {0.10, 0.20} -> 0.20,
+    #   g2 = {0.80, 0.05} -> 0.80, g3 = {0.30, 0.40} -> 0.40.
+    # Groups g0 and g2 are used; the top two keys among experts 0, 1, 4, 5 are 0 and 1.
+    # Group margin 0.80 - 0.40, key margin 0.85 - 0.80.
+    s = np.array([[0.90, 0.85, 0.10, 0.20, 0.80, 0.05, 0.30, 0.40]])
+    idx, gap = O.group_limited_topk(s, s, 2, 4, 2)
+    assert idx.tolist() == [[0, 1]]
+    assert gap[0] == pytest.approx(0.05, abs=1e-15)
+    # a bias that makes expert 7 the largest key does not rescue its group: the group
+    # score uses the unbiased affinity (0.40 < 0.80)
+    key = s + np.array([0, 0, 0, 0, 0, 0, 0, 1.0])
+    idx, _ = O.group_limited_topk(key, s, 2, 4, 2)
+    assert idx.tolist() == [[0, 1]]
+    assert O.select_topk(key, 2)[0].tolist() == [[0, 7]]
+    # k = 4 over M = 2 groups: the two best affinities of a group are summed:
+    #   g0 1.75, g1 0.30, g2 0.85, g3 0.70 -> g0, g2; all four allowed experts are chosen
+    idx, gap = O.group_limited_topk(s, s, 4, 4, 2)
+    assert idx.tolist() == [[0, 1, 4, 5]]
+    assert gap[0] == pytest.approx(0.85 - 0.70, abs=1e-15)
+
+
+def test_group_limited_route_softmax_affinity_is_probability():
+    # for softmax scoring the group score sums probabilities: with 2 experts per group
+    # and k/M = 2 a group's score is the probability mass of the group
+    rng = np.random.default_rng(9)
+    X = rng.standard_normal((30, 8))
+    Wg = rng.standard_normal((8, 8))
+    r = O.route(X, Wg, 4, "softmax", True, n_groups=4, topk_groups=2)
+    p = O.softmax_rows(r["logits"]).reshape(30, 4, 2).sum(2)
+    best2 = np.sort(np.argsort(-p, 1, kind="stable")[:, :2], 1)
+    assert np.array_equal(r["idx"] // 2, np.repeat(best2, 2, axis=1))
+
+
+def test_group_limited_rejects_bad_shapes():
+    key = np.zeros((1, 8))
+    for G, M, k in [(3, 1, 2), (4, 3, 4), (4, 2, 3), (4, 1, 4), (4, 5, 5)]:
+        with pytest.raises(ValueError):
+            O.group_limited_topk(key, key, k, G, M)

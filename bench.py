@@ -15,6 +15,7 @@ forward has no cross-GPU exchange) and the time is the maximum over ranks.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import os
@@ -65,6 +66,8 @@ def workload_config(cfg: K.MoEConfig, cf) -> dict:
     d = {"workload": cfg.name, "T": cfg.T, "H": cfg.H, "E": cfg.E, "I": cfg.I, "k": cfg.k,
          "score": cfg.score, "renorm": cfg.renorm, "shared_expert": cfg.shared,
          "capacity_factor": cf, "router": "fp32", "experts": cfg.dtype}
+    if cfg.n_groups > 1:
+        d["router_groups"] = {"n_groups": cfg.n_groups, "topk_groups": cfg.topk_groups}
     return d
 
 
@@ -205,7 +208,8 @@ def oracle_sample(cfg, d, cf, n_tokens: int, seed: int):
     lb = host(d["logit_bias"]) if "logit_bias" in d else None
     C = None if cf is None else O.capacity(cf, cfg.T, cfg.k, cfg.E)
     t0 = time.perf_counter()
-    r = O.route(X, Wg, cfg.k, cfg.score, cfg.renorm, bias, lb, C)
+    r = O.route(X, Wg, cfg.k, cfg.score, cfg.renorm, bias, lb, C, n_groups=cfg.n_groups,
+                topk_groups=cfg.topk_groups)
     t_route = time.perf_counter() - t0
     tokens = token_subset(cfg.T, n_tokens, seed).numpy()
     need = sorted({int(e) for e in r["idx"][tokens].reshape(-1)})
@@ -428,9 +432,14 @@ def main():
     ap.add_argument("--cpu-tokens", type=int, default=8)
     ap.add_argument("--ref-tokens", type=int, default=2)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--router-groups", default=None, metavar="G:M",
+                    help="group-limited routing: G expert groups, M of them per token")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)     # fewer warm-up steps give no valid number
     cfg = K.BY_NAME[args.config]
+    if args.router_groups:
+        G, M = (int(v) for v in args.router_groups.split(":"))
+        cfg = dataclasses.replace(cfg, n_groups=G, topk_groups=M)
     cf = args.capacity_factor
     if cf is None and cfg.capacity_factors:
         cf = cfg.capacity_factors[0]

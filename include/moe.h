@@ -73,6 +73,17 @@ typedef struct {
   int renorm;  /* 1: gates renormalised over the k chosen (sum to 1); 0: raw softmax
                   probability / raw affinity. */
   int x_dtype; /* dtype of X: MOE_DTYPE_BF16 or MOE_DTYPE_F32 */
+  int n_groups;    /* group-limited routing ("LLM Internals §14.2.3", node-limited routing;
+                      "MoE 03: efficiency frontiers", DeepSeek's hardware-aware design):
+                      the E experts form n_groups groups of E / n_groups consecutive
+                      indices (the experts of one node).  0 or 1: off. */
+  int topk_groups; /* groups a token may use: its topk_groups best groups by the sum of
+                      their k / topk_groups largest unbiased affinities (sigmoid s, or the
+                      softmax probability; ties to the lower group); the k experts are then
+                      the top k keys among those groups' experts.  Needs n_groups <= 32
+                      dividing E, 1 <= topk_groups <= n_groups, k a multiple of topk_groups
+                      and k / topk_groups <= E / n_groups.  topk_groups == n_groups is plain
+                      top-k. */
 } moe_router_desc;
 
 /* Shape of the expert stage (step 5). */
@@ -112,15 +123,19 @@ int moe_capacity(double c, int T, int k, int E);
  *   logit_bias [E] fp32 offset added to every logit before scoring (nullable = 0)
  *   topk_idx   [T, k] int32 out: the k chosen experts of each token, ascending index
  *   topk_gate  [T, k] fp32 out: their gate weights, same order
- *   key_gap    [T] fp32 out (nullable): key_(k) - key_(k+1) of the row (+inf if k == E)
+ *   key_gap    [T] fp32 out (nullable): key_(k) - key_(k+1) of the row (+inf if k == E);
+ *              group-limited: the smaller of the group margin S_(M) - S_(M+1) and the
+ *              key margin among the allowed experts
  *   prob_colsum[E] fp64 out (nullable): sum over tokens of p[t, e] (softmax row, or the
  *              sigmoid affinities normalised over the row); zeroed by the call
  * Selection is exact: the logits are fp32 (bf16 X with E % 8 == 0, H % 64 == 0 and
  * T >= 256: tensor cores over exact bf16 pieces of W_g, accumulation chains of at most
  * 3072 products; otherwise CUDA-core fp32 with 32-term blocks and compensated
- * accumulation), and any row whose k-th/(k+1)-th margin falls inside their error bound
- * is re-decided from dot products carried to ~48 significant bits (error-free products,
- * double-fp32 sums).  Ties go to the lower expert index. */
+ * accumulation), and any row whose k-th/(k+1)-th margin (or group margin) falls inside
+ * their error bound is re-decided from dot products carried to ~48 significant bits
+ * (error-free products, double-fp32 sums).  Ties go to the lower expert index.
+ * Returns MOE_ERR_UNSUPPORTED for n_groups > 32 or not dividing E, MOE_ERR_INVALID_ARG for
+ * the other group-shape violations. */
 int moe_router_topk(moe_ctx* ctx, const moe_router_desc* d, const void* X,
                     const float* Wg, const float* bias, const float* logit_bias,
                     int32_t* topk_idx, float* topk_gate, float* key_gap,

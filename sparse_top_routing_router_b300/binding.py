@@ -41,7 +41,8 @@ EXPORTS = ["moe_ctx_create", "moe_ctx_destroy", "moe_workspace_bytes", "moe_work
 
 class RouterDesc(C.Structure):
     _fields_ = [("T", C.c_int), ("H", C.c_int), ("E", C.c_int), ("k", C.c_int),
-                ("score", C.c_int), ("renorm", C.c_int), ("x_dtype", C.c_int)]
+                ("score", C.c_int), ("renorm", C.c_int), ("x_dtype", C.c_int),
+                ("n_groups", C.c_int), ("topk_groups", C.c_int)]
 
 
 class ExpertDesc(C.Structure):
@@ -184,10 +185,11 @@ def moe_capacity(c: float, T: int, k: int, E: int) -> int:
 
 def moe_router_topk(ctx: Context, X, Wg, k: int, score: int, renorm: bool, topk_idx,
                     topk_gate, ws, bias=None, logit_bias=None, key_gap=None,
-                    prob_colsum=None, stream=None) -> None:
+                    prob_colsum=None, stream=None, n_groups: int = 0,
+                    topk_groups: int = 0) -> None:
     T, H = X.shape
     E = Wg.shape[1]
-    d = RouterDesc(T, H, E, k, score, int(renorm), x_dtype_code(X))
+    d = RouterDesc(T, H, E, k, score, int(renorm), x_dtype_code(X), n_groups, topk_groups)
     _check("moe_router_topk", lib().moe_router_topk(
         ctx.handle, C.byref(d), _p(X), _p(Wg), _p(bias), _p(logit_bias), _p(topk_idx),
         _p(topk_gate), _p(key_gap), _p(prob_colsum), _p(ws), ws.numel() * ws.element_size(),

@@ -119,7 +119,7 @@ int check_shape(int T, int E, int k) {
 
 extern "C" {
 
-int moe_version(void) { return 10000; }
+int moe_version(void) { return 10100; }
 
 const char* moe_status_string(int s) {
   switch (s) {
@@ -231,6 +231,25 @@ int moe_router_topk(moe_ctx* ctx, const moe_router_desc* d, const void* X, const
     return fail(MOE_ERR_INVALID_ARG, "score = %d", d->score);
   if (d->x_dtype != MOE_DTYPE_BF16 && d->x_dtype != MOE_DTYPE_F32)
     return fail(MOE_ERR_INVALID_ARG, "x_dtype = %d", d->x_dtype);
+  // group-limited routing: n_groups <= 1, or every group allowed, is plain top-k
+  int n_groups = d->n_groups, topk_groups = d->topk_groups;
+  if (n_groups < 0 || topk_groups < 0)
+    return fail(MOE_ERR_INVALID_ARG, "n_groups = %d, topk_groups = %d", n_groups, topk_groups);
+  if (n_groups > 1) {
+    if (n_groups > 32 || d->E % n_groups != 0)
+      return fail(MOE_ERR_UNSUPPORTED, "n_groups = %d must divide E = %d and be <= 32",
+                  n_groups, d->E);
+    const int gs = d->E / n_groups;
+    if (topk_groups < 1 || topk_groups > n_groups || d->k % topk_groups != 0 ||
+        d->k / topk_groups > gs)
+      return fail(MOE_ERR_INVALID_ARG,
+                  "topk_groups = %d needs 1 <= topk_groups <= n_groups = %d, k = %d a "
+                  "multiple of it and k / topk_groups <= E / n_groups = %d",
+                  topk_groups, n_groups, d->k, gs);
+    if (topk_groups == n_groups) n_groups = topk_groups = 0;
+  } else {
+    n_groups = topk_groups = 0;
+  }
   if (d->T > 0 && (!X || !Wg || !topk_idx || !topk_gate))
     return fail(MOE_ERR_INVALID_ARG, "X, Wg, topk_idx and topk_gate are required");
   if (!ws) return fail(MOE_ERR_INVALID_ARG, "workspace is null");
@@ -255,6 +274,8 @@ int moe_router_topk(moe_ctx* ctx, const moe_router_desc* d, const void* X, const
   a.score = d->score;
   a.renorm = d->renorm;
   a.x_dtype = d->x_dtype;
+  a.n_groups = n_groups;
+  a.topk_groups = topk_groups;
   a.X = X;
   a.Wg = Wg;
   a.bias = bias;

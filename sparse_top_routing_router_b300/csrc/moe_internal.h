@@ -80,6 +80,7 @@ inline WsLayout ws_layout(int T, int H, int E, int I, int k, int dtype, int has_
 // ---------------------------------------------------------------- launch helpers
 struct RouterArgs {
   int T, H, E, k, score, renorm, x_dtype;
+  int n_groups, topk_groups;   // group-limited routing (n_groups > 1), else 0
   const void* X;
   const float* Wg;
   const float* bias;
@@ -97,7 +98,8 @@ struct RouterArgs {
   double* colsum;
   int* status;
   int* refined;        // counter of rows re-decided from exact dot products
-  int4* refine_list;   // [T] (t, lower band limit, sure limit, 0) of those rows
+  int4* refine_list;   // [T] (t, lower band limit, sure limit, 0) of those rows, or
+                       // (t, candidate group mask, fp32 group margin, 1) when group-limited
 };
 cudaError_t launch_router_logits(const RouterArgs& a, cudaStream_t s);
 // Tensor-core router logits (x bf16, E % 8 == 0, H % 64 == 0, T >= 256): splits W_g into bf16

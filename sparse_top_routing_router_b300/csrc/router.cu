@@ -508,15 +508,16 @@ __device__ __forceinline__ void load_row(const RouterArgs& a, int t, int lane, b
   r.amax = warp_max_f(r.amax);
 }
 
-// Top-(k+1) by repeated warp max: hardware max of the ordered keys, then the lowest
-// expert index holding that key.  Returns the chosen set as a per-lane bitmask.
+// Top-k (and the (k+1)-th key if `next`) by repeated warp max: hardware max of the
+// ordered keys, then the lowest expert index holding that key.  Returns the chosen set as
+// a per-lane bitmask.  Only experts with their `have` bit set take part.
 template <int NJ>
-__device__ __forceinline__ uint32_t topk_row(const RowKeys<NJ>& r, int k, int E, int lane,
+__device__ __forceinline__ uint32_t topk_row(const RowKeys<NJ>& r, int k, bool next, int lane,
                                              float& kth, float& k1th) {
   uint32_t taken = 0;
   kth = 0.f;
   k1th = -INFINITY;
-  const int rounds = (k < E) ? k + 1 : k;
+  const int rounds = next ? k + 1 : k;
   for (int q = 0; q < rounds; ++q) {
     uint32_t mine = 0u;
 #pragma unroll
@@ -591,10 +592,97 @@ __device__ __forceinline__ void finish_row(const RouterArgs& a, int t, int lane,
   }
 }
 
+// ------------------------------------------------------------------ group-limited routing
+// "LLM Internals §14.2.3" (node-limited routing) and "MoE 03: efficiency frontiers"
+// (DeepSeek's hardware-aware design): the experts sit in n_groups groups of consecutive
+// indices; a group's score is the sum of its k / topk_groups largest affinities (the
+// unbiased sigmoid s, or the softmax probability); a token may use only the experts of
+// its topk_groups best groups (ties to the lower group), and takes its top k keys among
+// them.
+
+struct GroupPick {
+  uint32_t sel;    // bit g: group g is used
+  uint32_t cand;   // bit g: group g's score is within 2 err of the M-th (a superset of sel)
+  float gap;       // S_(M) - S_(M+1), +inf if every group is used
+};
+
+// Scores of all groups from fp32 affinities (lane g < G ends up with group g's score),
+// then the M best.  err: error bound of one group score.
+template <int NJ>
+__device__ __forceinline__ GroupPick pick_groups(const RouterArgs& a, uint32_t have,
+                                                 const float (&aff)[NJ], int lane, float err) {
+  const int G = a.n_groups, M = a.topk_groups, gs = a.E / G, n = a.k / M;
+  uint32_t oa[NJ];
+  int grp[NJ];
+#pragma unroll
+  for (int j = 0; j < NJ; ++j) {
+    oa[j] = ordered_key(aff[j]);
+    grp[j] = (lane + 32 * j) / gs;
+  }
+  float my_s = 0.f;
+  for (int g = 0; g < G; ++g) {
+    uint32_t left = 0;
+#pragma unroll
+    for (int j = 0; j < NJ; ++j)
+      if ((have >> j & 1u) && grp[j] == g) left |= 1u << j;
+    float sum = 0.f;
+    for (int q = 0; q < n; ++q) {   // largest first; which of equal values goes is moot
+      uint32_t mine = 0u;
+#pragma unroll
+      for (int j = 0; j < NJ; ++j)
+        if (left >> j & 1u) mine = max(mine, oa[j]);
+      const uint32_t best = __reduce_max_sync(0xffffffffu, mine);
+      uint32_t my_e = 0xffffffffu;
+#pragma unroll
+      for (int j = NJ - 1; j >= 0; --j)
+        if ((left >> j & 1u) && oa[j] == best) my_e = lane + 32 * j;
+      const uint32_t win = __reduce_min_sync(0xffffffffu, my_e);
+      if (win != 0xffffffffu && (int)(win & 31u) == lane) left &= ~(1u << (win >> 5));
+      sum += key_of(best);
+    }
+    if (lane == g) my_s = sum;
+  }
+  GroupPick gp;
+  gp.sel = 0u;
+  const uint32_t os = ordered_key(my_s);
+  bool in = lane < G;
+  float sM = 0.f, sM1 = -INFINITY;
+  const int rounds = M < G ? M + 1 : M;
+  for (int q = 0; q < rounds; ++q) {
+    const uint32_t best = __reduce_max_sync(0xffffffffu, in ? os : 0u);
+    const uint32_t win =
+        __reduce_min_sync(0xffffffffu, (in && os == best) ? (uint32_t)lane : 0xffffffffu);
+    if (q < M) {
+      gp.sel |= 1u << win;
+      sM = key_of(best);
+      if (lane == (int)win) in = false;
+    } else {
+      sM1 = key_of(best);
+    }
+  }
+  gp.gap = M < G ? sM - sM1 : INFINITY;
+  gp.cand = __ballot_sync(0xffffffffu, lane < G && my_s >= sM - 2.f * err);
+  return gp;
+}
+
+// Per-lane mask of the experts (lane + 32 j) that belong to a group of `groups`.
+template <int NJ>
+__device__ __forceinline__ uint32_t experts_of(const RouterArgs& a, uint32_t have,
+                                               uint32_t groups, int lane) {
+  const int gs = a.E / a.n_groups;
+  uint32_t m = 0;
+#pragma unroll
+  for (int j = 0; j < NJ; ++j)
+    if ((have >> j & 1u) && (groups >> ((lane + 32 * j) / gs) & 1u)) m |= 1u << j;
+  return m;
+}
+
 // One warp per token: keys, top-(k+1), gates, key gap, row probabilities.  A row whose
-// margin is within twice the error bound of its fp32 keys is listed, with its band
-// limits, for router_refine_kernel; its outputs here are provisional.
-template <typename TX, int NJ>
+// margin is within twice the error bound of its fp32 keys (or, group-limited, of its group
+// scores) is listed for router_refine_kernel; its outputs here are provisional.
+// GRP: group-limited routing (a separate instantiation: the plain kernel keeps its
+// registers).
+template <typename TX, int NJ, bool GRP>
 __global__ void __launch_bounds__(kSelWarps * 32) router_select_kernel(RouterArgs a,
                                                                       int tok_per_warp) {
   __shared__ float s_col[kSelWarps][NJ * 32];
@@ -611,12 +699,49 @@ __global__ void __launch_bounds__(kSelWarps * 32) router_select_kernel(RouterArg
   for (int t = tbeg; t < min(tbeg + tok_per_warp, a.T); ++t) {
     RowKeys<NJ> r;
     load_row<NJ>(a, t, lane, true, r);
-    float kth, k1th;
-    const uint32_t taken = topk_row<NJ>(r, k, E, lane, kth, k1th);
-    const float gap = (k < E) ? kth - k1th : INFINITY;
     // error bound of the fp32 logits and of the fp32 keys derived from them
     const float eps_l = a.eps_rel * fmaxf(1.f, r.amax) * h_scale;
     const float eps = sigm ? 0.25f * eps_l + ldexpf(1.f, -20) : eps_l;
+    if (GRP) {
+      // affinities: s, or p = exp(l - lmax) / sum (moves by <= 2.01 eps_l p when every
+      // logit moves by eps_l, plus fp32 rounding of exp, the row sum and the quotient)
+      float aff[NJ];
+      float zs = 0.f;
+#pragma unroll
+      for (int j = 0; j < NJ; ++j) {
+        aff[j] = 0.f;
+        if (r.have >> j & 1u) aff[j] = sigm ? r.sg[j] : __expf(r.l[j] - r.lmax);
+        if (aff[j] != aff[j]) aff[j] = 0.f;
+        zs += aff[j];
+      }
+      if (!sigm) {
+        zs = warp_sum_f(zs);
+#pragma unroll
+        for (int j = 0; j < NJ; ++j) aff[j] = __fdividef(aff[j], zs);
+      }
+      const int n = k / a.topk_groups;
+      const float eps_a = sigm ? eps : 2.5f * eps_l + ldexpf(1.f, -18);
+      const float err_g = n * (eps_a + n * ldexpf(1.f, -23));
+      const GroupPick gp = pick_groups<NJ>(a, r.have, aff, lane, err_g);
+      RowKeys<NJ> re = r;
+      re.have = experts_of<NJ>(a, r.have, gp.sel, lane);
+      const bool next = a.topk_groups * (E / a.n_groups) > k;
+      float kth, k1th;
+      const uint32_t taken = topk_row<NJ>(re, k, next, lane, kth, k1th);
+      const float k_gap = next ? kth - k1th : INFINITY;
+      if ((!(gp.gap > 2.f * err_g) || !(k_gap > 2.f * eps)) && lane == 0) {
+        // Exactness guard.  A group whose fp32 score is below S_(M) - 2 err is below the
+        // M groups chosen here in exact arithmetic too, so the exact choice lies among
+        // the candidate groups; the refine kernel re-decides from their exact logits.
+        const int slot = atomicAdd(a.refined, 1);
+        a.refine_list[slot] = make_int4(t, (int)gp.cand, __float_as_int(gp.gap), 1);
+      }
+      finish_row<NJ>(a, t, lane, r, taken, fminf(gp.gap, k_gap), a.colsum ? &col : nullptr);
+      continue;
+    }
+    float kth, k1th;
+    const uint32_t taken = topk_row<NJ>(r, k, k < E, lane, kth, k1th);
+    const float gap = (k < E) ? kth - k1th : INFINITY;
     if (k < E && !(gap > 2.f * eps) && lane == 0) {
       // Exactness guard.  With |approx - exact| <= eps for every key, an expert whose
       // approximate key exceeds k1th + 2 eps beats every expert outside the approximate
@@ -643,10 +768,250 @@ __global__ void __launch_bounds__(kSelWarps * 32) router_select_kernel(RouterArg
   }
 }
 
+// Warp-wide argmax of a double per lane (ties to the lower index); bi = 0x7fffffff if
+// no lane offers a value.
+__device__ __forceinline__ void warp_argmax_d(double& bk, int& bi) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const double k2 = __shfl_xor_sync(0xffffffffu, bk, o);
+    const int i2 = __shfl_xor_sync(0xffffffffu, bi, o);
+    if (k2 > bk || (k2 == bk && i2 < bi)) {
+      bk = k2;
+      bi = i2;
+    }
+  }
+}
+
+// The n-th largest of the ordered values oa[j] over the experts in `members` (per-lane
+// masks), as a float; -inf if there are fewer than n.
+template <int NJ>
+__device__ __forceinline__ float nth_largest(const uint32_t (&oa)[NJ], uint32_t members, int n,
+                                             int lane) {
+  float v = -INFINITY;
+  for (int q = 0; q < n; ++q) {
+    uint32_t mine = 0u;
+#pragma unroll
+    for (int j = 0; j < NJ; ++j)
+      if (members >> j & 1u) mine = max(mine, oa[j]);
+    const uint32_t best = __reduce_max_sync(0xffffffffu, mine);
+    uint32_t my_e = 0xffffffffu;
+#pragma unroll
+    for (int j = NJ - 1; j >= 0; --j)
+      if ((members >> j & 1u) && oa[j] == best) my_e = lane + 32 * j;
+    const uint32_t win = __reduce_min_sync(0xffffffffu, my_e);
+    if (win == 0xffffffffu) return -INFINITY;
+    if ((int)(win & 31u) == lane) members &= ~(1u << (win >> 5));
+    v = key_of(best);
+  }
+  return v;
+}
+
+// Writes the experts of the per-lane masks `m` to s_ce in ascending order; returns the
+// count (all lanes).
+template <int NJ>
+__device__ __forceinline__ int list_experts(uint32_t m, int lane, int* s_ce) {
+  const uint32_t lt_mask = (1u << lane) - 1u;
+  int base = 0;
+#pragma unroll
+  for (int j = 0; j < NJ; ++j) {
+    const uint32_t B = __ballot_sync(0xffffffffu, (m >> j) & 1u);
+    if (m >> j & 1u) s_ce[base + __popc(B & lt_mask)] = lane + 32 * j;
+    base += __popc(B);
+  }
+  return base;
+}
+
+// Reads back into lane registers the exact logits of the experts listed by list_experts(m).
+template <int NJ>
+__device__ __forceinline__ void take_exact(uint32_t m, int lane, const double* s_ex,
+                                           double (&ex)[NJ]) {
+  const uint32_t lt_mask = (1u << lane) - 1u;
+  int base = 0;
+#pragma unroll
+  for (int j = 0; j < NJ; ++j) {
+    const uint32_t B = __ballot_sync(0xffffffffu, (m >> j) & 1u);
+    if (m >> j & 1u) ex[j] = s_ex[base + __popc(B & lt_mask)];
+    base += __popc(B);
+  }
+}
+
+// Group-limited re-decision of row t, in two rounds of exact logits.
+//  1. Group scores.  In a candidate group (cmask), an expert whose fp32 affinity is below
+//     the group's n-th largest minus 2 eps_a is below n others in exact arithmetic too;
+//     the exact top n of the group lies among the rest, so their exact logits give the
+//     exact score.  The M best candidates by exact score are the groups used.
+//  2. Experts.  Among the experts of those groups, the band of the fp32 keys
+//     [kth - 2 eps, k1th + 2 eps] as in the plain re-decision: experts above it are sure
+//     members, the band is ranked on exact keys (computed now unless round 1 did).
+// approx_gap: the fp32 group margin, reported when no other candidate group is left to
+// measure the exact margin against.
+template <typename TX, int NJ>
+__device__ void refine_group_row(const RouterArgs& a, int t, uint32_t cmask, float approx_gap,
+                                 int* s_ce, double* s_ex, float2 (*s_part)[kRefineBatch],
+                                 int* s_nband) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int k = a.k, G = a.n_groups, M = a.topk_groups, n = k / M;
+  const bool sigm = a.score == MOE_SCORE_SIGMOID;
+  const float h_scale = sqrtf(fmaxf(1.f, a.H / 1024.f));
+  RowKeys<NJ> r;
+  float zs = 1.f, eps = 0.f, kth = 0.f, k1th = -INFINITY, g_gap = approx_gap;
+  uint32_t known = 0, cand2 = 0, sure = 0;
+  double ex[NJ];
+  if (w == 0) {
+    load_row<NJ>(a, t, lane, false, r);
+    const float eps_l = a.eps_rel * fmaxf(1.f, r.amax) * h_scale;
+    eps = sigm ? 0.25f * eps_l + ldexpf(1.f, -20) : eps_l;
+    const float eps_a = sigm ? eps : 2.5f * eps_l + ldexpf(1.f, -18);
+    float aff[NJ];
+    float z = 0.f;
+#pragma unroll
+    for (int j = 0; j < NJ; ++j) {
+      aff[j] = 0.f;
+      if (r.have >> j & 1u) aff[j] = sigm ? r.sg[j] : __expf(r.l[j] - r.lmax);
+      if (aff[j] != aff[j]) aff[j] = 0.f;
+      z += aff[j];
+    }
+    if (!sigm) {
+      zs = warp_sum_f(z);
+#pragma unroll
+      for (int j = 0; j < NJ; ++j) aff[j] = __fdividef(aff[j], zs);
+    }
+    uint32_t oa[NJ];
+#pragma unroll
+    for (int j = 0; j < NJ; ++j) oa[j] = ordered_key(aff[j]);
+    // with exactly M candidates the groups are already decided
+    for (int g = 0; g < G && __popc(cmask) > M; ++g) {
+      if (!(cmask >> g & 1u)) continue;
+      const uint32_t mem = experts_of<NJ>(a, r.have, 1u << g, lane);
+      const float lim = nth_largest<NJ>(oa, mem, n, lane) - 2.f * eps_a;
+#pragma unroll
+      for (int j = 0; j < NJ; ++j)
+        if ((mem >> j & 1u) && aff[j] >= lim) known |= 1u << j;
+    }
+    const int nb = list_experts<NJ>(known, lane, s_ce);
+    if (lane == 0) *s_nband = nb;
+  }
+  __syncthreads();
+  int nband = *s_nband;
+  for (int b0 = 0; b0 < nband; b0 += kRefineBatch)
+    exact_logits_cta<TX>(a, t, s_ce + b0, min(kRefineBatch, nband - b0), s_part, s_ex + b0);
+  if (w == 0) {
+#pragma unroll
+    for (int j = 0; j < NJ; ++j) ex[j] = 0.0;
+    take_exact<NJ>(known, lane, s_ex, ex);
+    // exact affinities (softmax: scaled by the row's fp32 maximum and sum, which orders
+    // the groups as the exact probabilities do)
+    double ea[NJ];
+#pragma unroll
+    for (int j = 0; j < NJ; ++j)
+      ea[j] = !(known >> j & 1u) ? 0.0
+              : sigm ? 1.0 / (1.0 + exp(-ex[j])) : exp(ex[j] - (double)r.lmax) / (double)zs;
+    double my_s = -INFINITY;   // lane g: exact score of candidate group g
+    for (int g = 0; g < G && __popc(cmask) > M; ++g) {
+      if (!(cmask >> g & 1u)) continue;
+      uint32_t left = experts_of<NJ>(a, known, 1u << g, lane);
+      double sum = 0.0;
+      for (int q = 0; q < n; ++q) {
+        double bk = -INFINITY;
+        int bi = 0x7fffffff;
+#pragma unroll
+        for (int j = 0; j < NJ; ++j)
+          if ((left >> j & 1u) && (ea[j] > bk || (ea[j] == bk && lane + 32 * j < bi))) {
+            bk = ea[j];
+            bi = lane + 32 * j;
+          }
+        warp_argmax_d(bk, bi);
+        if (bi == 0x7fffffff) break;
+        if ((bi & 31) == lane) left &= ~(1u << (bi >> 5));
+        sum += bk;
+      }
+      if (lane == g) my_s = sum;
+    }
+    uint32_t sel = __popc(cmask) > M ? 0u : cmask;
+    bool in = lane < G && (cmask >> lane & 1u);
+    double sM = 0.0, sM1 = -INFINITY;
+    for (int q = 0; q <= M && __popc(cmask) > M; ++q) {
+      double bk = in ? my_s : -INFINITY;
+      int bi = in ? lane : 0x7fffffff;
+      warp_argmax_d(bk, bi);
+      if (bi == 0x7fffffff) break;
+      if (q < M) {
+        sel |= 1u << bi;
+        sM = bk;
+        if (lane == bi) in = false;
+      } else {
+        sM1 = bk;
+      }
+    }
+    if (sM1 != -INFINITY) g_gap = (float)(sM - sM1);
+    // the key band among the experts of the chosen groups
+    RowKeys<NJ> re = r;
+    re.have = experts_of<NJ>(a, r.have, sel, lane);
+    const bool next = M * (a.E / G) > k;
+    topk_row<NJ>(re, k, next, lane, kth, k1th);
+#pragma unroll
+    for (int j = 0; j < NJ; ++j) {
+      const float kv = key_of(r.ok[j]);
+      if ((re.have >> j & 1u) && kv >= kth - 2.f * eps) {
+        cand2 |= 1u << j;
+        if (kv > k1th + 2.f * eps) sure |= 1u << j;
+      }
+    }
+    const int nb = list_experts<NJ>(cand2 & ~sure & ~known, lane, s_ce);
+    if (lane == 0) *s_nband = nb;
+  }
+  __syncthreads();
+  const int nband2 = *s_nband;
+  for (int b0 = 0; b0 < nband2; b0 += kRefineBatch)
+    exact_logits_cta<TX>(a, t, s_ce + b0, min(kRefineBatch, nband2 - b0), s_part, s_ex + b0);
+  if (w == 0) {
+    take_exact<NJ>(cand2 & ~sure & ~known, lane, s_ex, ex);
+    double ek[NJ];
+#pragma unroll
+    for (int j = 0; j < NJ; ++j) {
+      if (!(cand2 >> j & 1u)) {
+        ek[j] = -INFINITY;
+      } else if (sure >> j & 1u) {
+        ek[j] = INFINITY;
+      } else {
+        ek[j] = sigm ? 1.0 / (1.0 + exp(-ex[j])) + (a.bias ? (double)a.bias[lane + 32 * j] : 0.0)
+                     : ex[j];
+      }
+    }
+    uint32_t tk = 0;
+    double dk = 0.0, dk1 = -INFINITY;
+    for (int q = 0; q <= k; ++q) {
+      double bk = -INFINITY;
+      int bi = 0x7fffffff;
+#pragma unroll
+      for (int j = 0; j < NJ; ++j) {
+        const int e = lane + 32 * j;
+        if ((cand2 >> j & 1u) && !(tk >> j & 1u) && (ek[j] > bk || (ek[j] == bk && e < bi))) {
+          bk = ek[j];
+          bi = e;
+        }
+      }
+      warp_argmax_d(bk, bi);
+      if (bi == 0x7fffffff) break;
+      if (q < k) {
+        if ((bi & 31) == lane) tk |= 1u << (bi >> 5);
+        dk = bk;
+      } else {
+        dk1 = bk;
+      }
+    }
+    // the exact key margin where the band decided it, else the fp32 one
+    const float k_gap = dk1 == -INFINITY ? INFINITY
+                        : (dk == INFINITY || dk1 == INFINITY) ? kth - k1th : (float)(dk - dk1);
+    finish_row<NJ>(a, t, lane, r, tk, fminf(g_gap, k_gap), nullptr);
+  }
+  __syncthreads();   // s_ce / s_ex are reused by the next listed row
+}
+
 // One CTA per listed row (grid-stride over the list): exact logits of the band experts
 // (CTA-wide), then warp 0 re-decides the row among its candidates on the exact keys
 // (ties to the lower index; sure experts rank first) and rewrites its outputs.
-template <typename TX, int NJ>
+template <typename TX, int NJ, bool GRP>
 __global__ void __launch_bounds__(kRefineThreads) router_refine_kernel(RouterArgs a) {
   __shared__ int s_ce[kMaxE];        // band experts, ascending
   __shared__ double s_ex[kMaxE];     // their exact keys
@@ -660,6 +1025,11 @@ __global__ void __launch_bounds__(kRefineThreads) router_refine_kernel(RouterArg
   for (int i = blockIdx.x; i < n; i += gridDim.x) {
     const int4 ent = a.refine_list[i];
     const int t = ent.x;
+    if (GRP) {
+      refine_group_row<TX, NJ>(a, t, (uint32_t)ent.y, __int_as_float(ent.z), s_ce, s_ex,
+                               s_part, &s_nband);
+      continue;
+    }
     const float lim = __int_as_float(ent.y), sure = __int_as_float(ent.z);
     RowKeys<NJ> r;
     uint32_t cand = 0, band = 0;
@@ -737,20 +1107,27 @@ __global__ void __launch_bounds__(kRefineThreads) router_refine_kernel(RouterArg
   }
 }
 
-template <typename TX, int NJ>
-cudaError_t launch_select_nj(const RouterArgs& a, cudaStream_t s) {
+template <typename TX, int NJ, bool GRP>
+cudaError_t launch_select_grp(const RouterArgs& a, cudaStream_t s) {
   // one token per warp up to 2^14 tokens, then more: enough warps to fill the GPU, few
   // enough CTAs that the per-CTA column sums stay cheap
   const int tpw = a.T <= 16384 ? 1 : (a.T + 16383) / 16384;
   const int per_cta = kSelWarps * tpw;
-  router_select_kernel<TX, NJ><<<(a.T + per_cta - 1) / per_cta, kSelWarps * 32, 0, s>>>(a, tpw);
+  router_select_kernel<TX, NJ, GRP>
+      <<<(a.T + per_cta - 1) / per_cta, kSelWarps * 32, 0, s>>>(a, tpw);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   // the listed rows are few; most of these CTAs find nothing to do and exit
   const int sms = a.num_sms > 0 ? a.num_sms : 1;
   const int grid = a.T < 8 * sms ? a.T : 8 * sms;
-  router_refine_kernel<TX, NJ><<<grid, kRefineThreads, 0, s>>>(a);
+  router_refine_kernel<TX, NJ, GRP><<<grid, kRefineThreads, 0, s>>>(a);
   return cudaGetLastError();
+}
+
+template <typename TX, int NJ>
+cudaError_t launch_select_nj(const RouterArgs& a, cudaStream_t s) {
+  return a.n_groups > 1 ? launch_select_grp<TX, NJ, true>(a, s)
+                        : launch_select_grp<TX, NJ, false>(a, s);
 }
 
 template <typename TX>

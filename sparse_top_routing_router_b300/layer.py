@@ -72,7 +72,8 @@ class MoELayer:
         B.moe_router_topk(self.ctx, X, w["Wg"], c.k, self.score, c.renorm, self.idx,
                           self.gate, self.ws, bias=w.get("bias"),
                           logit_bias=w.get("logit_bias"), key_gap=self.gap,
-                          prob_colsum=self.colsum, stream=stream)
+                          prob_colsum=self.colsum, stream=stream,
+                          n_groups=c.n_groups, topk_groups=c.topk_groups)
         B.moe_dispatch(self.ctx, self.idx, c.E, self.capacity, self.counts, self.offsets,
                        self.row_of_slot, self.slot_of_row, self.ws, X=X, Xperm=self.Xperm,
                        stream=stream)

@@ -56,7 +56,7 @@ def oracle_route(run: Run) -> Dict[str, np.ndarray]:
     return O.route(to_np(d["X"]), to_np(d["Wg"]), c.k, c.score, c.renorm,
                    bias=to_np(d["bias"]) if "bias" in d else None,
                    logit_bias=to_np(d["logit_bias"]) if "logit_bias" in d else None,
-                   C=run.capacity)
+                   C=run.capacity, n_groups=c.n_groups, topk_groups=c.topk_groups)
 
 
 def check_routing(run: Run, ref: Dict[str, np.ndarray]) -> Dict[str, object]:

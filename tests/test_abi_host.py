@@ -37,7 +37,7 @@ def test_exports_match_header(L):
 
 
 def test_version_and_strings(L):
-    assert L.moe_version() == 10000
+    assert L.moe_version() == 10100
     assert B.status_string(0) == "ok"
     assert B.status_string(-4) == "device wait timed out"
     for i, n in enumerate(B.KERNEL_NAMES):
@@ -94,6 +94,22 @@ def test_validation_before_device(L):
     r = L.moe_router_topk(None, C.byref(d), fake, fake, None, None, fake, fake, None, None,
                           fake, 64, None)
     assert r == B.MOE_ERR_INVALID_ARG and "workspace" in B.last_error_detail()
+    r = L.moe_router_topk(None, C.byref(d), fake, fake, None, None, fake, fake, None, None,
+                          fake, 1 << 20, None)
+    assert r == B.MOE_ERR_INVALID_ARG and "ctx" in B.last_error_detail()
+    # group-limited routing shapes
+    for G, M, k, code, text in [(3, 1, 2, B.MOE_ERR_UNSUPPORTED, "n_groups = 3"),
+                                (64, 1, 2, B.MOE_ERR_UNSUPPORTED, "n_groups = 64"),
+                                (4, 3, 4, B.MOE_ERR_INVALID_ARG, "topk_groups = 3"),
+                                (4, 5, 5, B.MOE_ERR_INVALID_ARG, "topk_groups = 5"),
+                                (8, 1, 2, B.MOE_ERR_INVALID_ARG, "topk_groups = 1"),
+                                (-1, 0, 2, B.MOE_ERR_INVALID_ARG, "n_groups = -1")]:
+        d = B.RouterDesc(16, 64, 8, k, 0, 1, 0, G, M)
+        r = L.moe_router_topk(None, C.byref(d), fake, fake, None, None, fake, fake, None,
+                              None, fake, 1 << 20, None)
+        assert r == code and text in B.last_error_detail(), (G, M, k, r)
+    # a valid group shape passes the shape checks (and stops at the missing context)
+    d = B.RouterDesc(16, 64, 8, 4, 1, 1, 0, 4, 2)
     r = L.moe_router_topk(None, C.byref(d), fake, fake, None, None, fake, fake, None, None,
                           fake, 1 << 20, None)
     assert r == B.MOE_ERR_INVALID_ARG and "ctx" in B.last_error_detail()

@@ -34,6 +34,9 @@ SMALL = [
     # >= 512 rows per expert on average: the CTA-pair (256-row) tensor-core tiles
     K.scaled(K.MIXTRAL, name="mixtral_small_pairs", T=1100, H=256, E=4, I=384),
     K.scaled(K.DSV3_PREFILL, name="dsv3_small_pairs", T=1100, H=256, E=2, I=256, k=1),
+    # group-limited routing: 8 groups of 8 experts, 4 groups per token
+    K.scaled(K.DSV3_PREFILL, name="dsv3_small_groups", T=300, H=256, E=64, I=128,
+             n_groups=8, topk_groups=4),
     K.scaled(K.SWITCH, name="switch_small_pairs", T=4200, H=128, E=8, I=128),
 ]
 

@@ -67,3 +67,86 @@ def test_logit_error_within_guard(ctx, cfg, eps_rel):
     ratio = float((err / bound).max())
     print(f"{cfg.name}: max |dl| = {err.max():.3e}, max err/eps = {ratio:.4f}")
     assert ratio < 0.25
+
+
+# ---------------------------------------------------------------- group-limited routing
+
+GAP_EXCLUDE = 1e-6
+
+
+def _route_groups(ctx, cfg, d):
+    T, k, E = cfg.T, cfg.k, cfg.E
+    nbytes = B.moe_workspace_bytes(T, cfg.H, E, 64, k, B.x_dtype_code(d["X"]), 0)
+    ws = torch.zeros(nbytes, dtype=torch.uint8, device="cuda")
+    idx = torch.empty(T, k, dtype=torch.int32, device="cuda")
+    gate = torch.empty(T, k, device="cuda")
+    gap = torch.empty(T, device="cuda")
+    score = B.MOE_SCORE_SIGMOID if cfg.score == "sigmoid" else B.MOE_SCORE_SOFTMAX
+    B.moe_router_topk(ctx, d["X"], d["Wg"], k, score, cfg.renorm, idx, gate, ws,
+                      bias=d.get("bias"), logit_bias=d.get("logit_bias"), key_gap=gap,
+                      n_groups=cfg.n_groups, topk_groups=cfg.topk_groups)
+    torch.cuda.synchronize()
+    assert B.moe_get_device_status(ctx, ws) == 0
+    refined = int(ws[4:8].view(torch.int32).item())
+    ref = O.route(d["X"].double().cpu().numpy(), d["Wg"].double().cpu().numpy(), k,
+                  cfg.score, cfg.renorm,
+                  bias=d["bias"].double().cpu().numpy() if "bias" in d else None,
+                  logit_bias=d["logit_bias"].double().cpu().numpy()
+                  if "logit_bias" in d else None,
+                  n_groups=cfg.n_groups, topk_groups=cfg.topk_groups)
+    return (idx.cpu().numpy().astype(np.int64), gate.double().cpu().numpy(),
+            gap.double().cpu().numpy(), refined, ref)
+
+
+GROUP_CASES = [
+    # DSV3 shape: 8 groups of 32, 4 groups per token, tensor-core logits
+    K.scaled(K.DSV3_PREFILL, name="dsv3_groups_tc", T=8192, n_groups=8, topk_groups=4),
+    # CUDA-core logits (T < 256), 8 groups of 8
+    K.scaled(K.DSV3_PREFILL, name="dsv3_groups_cuda", T=200, E=64, n_groups=8,
+             topk_groups=4),
+    # softmax scoring: the group score sums probabilities
+    K.scaled(K.MIXTRAL, name="softmax_groups", T=512, E=16, k=4, n_groups=4, topk_groups=2),
+    # 32 groups of 10 (E = 320, the largest group count), three groups per token
+    K.scaled(K.DSV3_PREFILL, name="e320_groups", T=512, E=320, k=6, n_groups=32,
+             topk_groups=3),
+    # top-1 in one group of 8
+    K.scaled(K.SWITCH, name="switch_groups_k1", T=512, E=64, n_groups=8, topk_groups=1),
+]
+
+
+@pytest.mark.parametrize("cfg", GROUP_CASES, ids=lambda c: c.name)
+def test_group_limited_routing(ctx, cfg):
+    d = make_inputs(cfg, device="cuda", with_experts=False)
+    idx, gate, gap, refined, ref = _route_groups(ctx, cfg, d)
+    ok = ref["gap"] >= GAP_EXCLUDE
+    assert np.array_equal(idx[ok], ref["idx"][ok]), \
+        f"{(idx[ok] != ref['idx'][ok]).any(1).sum()} rows differ"
+    assert np.all(np.diff(idx, axis=1) > 0)
+    # every chosen expert lies in an allowed group count: at most topk_groups groups
+    gs = cfg.E // cfg.n_groups
+    assert max(len(set((row // gs).tolist())) for row in idx) <= cfg.topk_groups
+    g_dev = np.abs(gate - ref["gate"]).max(axis=1)
+    l_scale = np.maximum(1.0, np.abs(ref["logits"]).max(axis=1)) * \
+        math.sqrt(max(1.0, cfg.H / 1024))
+    assert np.all(g_dev[ok] <= 2 * EPS_TENSOR * l_scale[ok] + 2e-6)
+    fin = np.isfinite(ref["gap"]) & ok
+    assert np.abs(gap[fin] - ref["gap"][fin]).max() <= 1e-4
+    print(f"{cfg.name}: excluded {int((~ok).sum())}, re-decided {refined} of {cfg.T}")
+
+
+def test_group_limited_exact_group_ties(ctx):
+    """Groups 0 and 1 hold identical router columns and biases, so their scores tie
+    exactly on every row: the lower group must win wherever the tie decides, which the
+    selection kernel cannot see from fp32 margins alone (margin 0) - every such row is
+    re-decided from exact logits.  All rows must match the oracle."""
+    cfg = K.scaled(K.DSV3_PREFILL, name="tie_groups", T=512, E=64, n_groups=8,
+                   topk_groups=2)
+    d = make_inputs(cfg, device="cuda", with_experts=False)
+    gs = cfg.E // cfg.n_groups
+    d["Wg"][:, gs:2 * gs] = d["Wg"][:, :gs]
+    d["bias"][gs:2 * gs] = d["bias"][:gs]
+    idx, _, _, refined, ref = _route_groups(ctx, cfg, d)
+    tied = ref["gap"] == 0
+    assert tied.sum() > 0 and refined >= tied.sum()
+    assert np.array_equal(idx, ref["idx"]), f"{(idx != ref['idx']).any(1).sum()} rows differ"
+    print(f"tie_groups: {int(tied.sum())} tied rows, re-decided {refined}")

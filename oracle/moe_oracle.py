@@ -299,6 +299,28 @@ def balance_stats(counts: np.ndarray, prob_colsum: np.ndarray, T: int, k: int,
     return dict(f=f, p=p, loss=loss, drop_rate=drop_rate, cv=cv, entropy=entropy)
 
 
+def bias_update(bias: np.ndarray, counts: np.ndarray, T: int, k: int,
+                gamma: float) -> np.ndarray:
+    """The auxiliary-loss-free balancing step  [LI §14.2.3, bias-adjusted selection]:
+    after a step, the load of every expert over the whole batch is compared with the
+    balanced load; an overloaded expert's bias drops by gamma, an underloaded one's
+    rises by gamma, and the bias is not learned by backpropagation.
+
+    Load = m_e, the router's choices before capacity; the balanced load is the mean
+    T*k/E (the page names no threshold), compared exactly as E*m_e against T*k.  An
+    expert at exactly the mean keeps its bias.  Returns the new bias in float64; the
+    inputs are float32 values, so b +- gamma is exact here and rounding it to float32
+    gives the correctly rounded float32 sum.
+    """
+    m = np.asarray(counts, dtype=np.int64)
+    E = m.size
+    b = np.asarray(bias, dtype=f64)
+    g = f64(gamma)
+    over = E * m > T * k
+    under = E * m < T * k
+    return np.where(over, b - g, np.where(under, b + g, b))
+
+
 # ---------------------------------------------------------------------------
 # The whole layer                                  [LI §14.2.1 steps 1-6; KM combine]
 # ---------------------------------------------------------------------------

@@ -431,3 +431,36 @@ def test_group_limited_rejects_bad_shapes():
     for G, M, k in [(3, 1, 2), (4, 3, 4), (4, 2, 3), (4, 1, 4), (4, 5, 5)]:
         with pytest.raises(ValueError):
             O.group_limited_topk(key, key, k, G, M)
+
+
+# ---------------------------------------------------------------- bias update step
+
+def test_bias_update_hand_example():
+    # T*k = 8 slots over E = 4 experts: balanced load 2.  Counts 5, 1, 2, 0: expert 0 is
+    # overloaded (-gamma), experts 1 and 3 underloaded (+gamma), expert 2 unchanged.
+    b = np.array([0.5, -0.25, 0.125, 0.0])
+    out = O.bias_update(b, [5, 1, 2, 0], T=4, k=2, gamma=0.001)
+    np.testing.assert_array_equal(out, [0.5 - 0.001, -0.25 + 0.001, 0.125, 0.001])
+
+
+def test_bias_update_mean_compared_exactly():
+    # T*k/E = 10/3: counts 3 and 4 sit below and above it; no count equals it
+    out = O.bias_update(np.zeros(3), [3, 4, 3], T=10, k=1, gamma=0.5)
+    np.testing.assert_array_equal(out, [0.5, -0.5, 0.5])
+    # gamma = 0 (the rate of the last phase of training on the page) changes nothing
+    b = np.random.default_rng(0).standard_normal(16)
+    np.testing.assert_array_equal(O.bias_update(b, np.arange(16), 30, 4, 0.0), b)
+
+
+def test_bias_update_float32_rounding_is_single():
+    # float32 bias and gamma: the float64 result is the exact sum, so one rounding to
+    # float32 equals a float32 addition (correctly rounded)
+    rng = np.random.default_rng(3)
+    b = (rng.standard_normal(64) * 0.1).astype(np.float32)
+    g = np.float32(0.001)
+    counts = rng.integers(0, 9, 64)
+    out = O.bias_update(b, counts, T=128, k=2, gamma=float(g)).astype(np.float32)
+    over = 64 * counts > 256
+    under = 64 * counts < 256
+    want = np.where(over, b - g, np.where(under, b + g, b)).astype(np.float32)
+    np.testing.assert_array_equal(out, want)

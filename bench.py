@@ -262,7 +262,7 @@ def run_gpu(args, cfg, cf):
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     dev = torch.device("cuda", local)
     d = make_inputs(cfg, device=dev, seed=replica_seed(cfg.seed, rank))
-    layer = MoELayer(cfg, d, device=local, capacity_factor=cf)
+    layer = MoELayer(cfg, d, device=local, capacity_factor=cf, bias_gamma=args.bias_update)
     X = d["X"]
     stream = torch.cuda.current_stream()
 
@@ -396,7 +396,9 @@ def run_gpu(args, cfg, cf):
         if cfg.dtype == "bf16" else "f32",
         "data": "synthetic (seeded N(0,1) tokens, N(0,0.02) random-init weights)",
         "config": dict(workload_config(cfg, cf), l2=l2_note, kept_rows=R,
-                       parallelism=f"replicas x{world}"),
+                       parallelism=f"replicas x{world}",
+                       **({"bias_update_gamma": args.bias_update}
+                          if args.bias_update is not None else {})),
         "tflops": world * layer_flops * args.steps / (ms / 1e3) / 1e12,
         "roofline": roofline,
         "e2e": {"value": world * cfg.T * args.steps / (ms_e2e / 1e3), "unit": "tokens/s",
@@ -432,11 +434,16 @@ def main():
     ap.add_argument("--cpu-tokens", type=int, default=8)
     ap.add_argument("--ref-tokens", type=int, default=2)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--bias-update", type=float, default=None, metavar="GAMMA",
+                    help="end every forward with the bias update step (selection bias "
+                         "-/+ GAMMA for over/underloaded experts)")
     ap.add_argument("--router-groups", default=None, metavar="G:M",
                     help="group-limited routing: G expert groups, M of them per token")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)     # fewer warm-up steps give no valid number
     cfg = K.BY_NAME[args.config]
+    if args.bias_update is not None and cfg.selection_bias_std <= 0:
+        ap.error("--bias-update needs a workload with a selection bias (sigmoid scoring)")
     if args.router_groups:
         G, M = (int(v) for v in args.router_groups.split(":"))
         cfg = dataclasses.replace(cfg, n_groups=G, topk_groups=M)

@@ -227,6 +227,17 @@ int moe_balance_stats(moe_ctx* ctx, int T, int k, int E, const int32_t* counts,
                       const int32_t* offsets, const double* prob_colsum, double alpha,
                       double* f, double* p, double* out, moe_stream_t stream);
 
+/* Auxiliary-loss-free balancing step ("LLM Internals §14.2.3", bias-adjusted selection):
+ * after a batch, every expert whose load is above the balanced load loses gamma from its
+ * selection bias and every expert below it gains gamma; the page gives gamma = 0.001 for
+ * most of training and 0 at the end.  Load = counts[e] from moe_dispatch (router choices
+ * before capacity); balanced load = T k / E, compared exactly (E counts[e] against T k);
+ * an expert exactly at it keeps its bias.  Each updated entry is one float32 addition.
+ *   counts [E] int32 (device), bias [E] fp32 (device, updated in place).
+ * Returns MOE_ERR_INVALID_ARG for a null pointer or a non-finite gamma. */
+int moe_bias_update(moe_ctx* ctx, int T, int k, int E, const int32_t* counts, float gamma,
+                    float* bias, moe_stream_t stream);
+
 /* ------------------------------------------------------------------ diagnostics */
 
 /* Synchronise `stream`, copy the workspace status word into *status (host pointer) and,
@@ -251,6 +262,7 @@ enum moe_kernel_id {
   MOE_K_EXPERT_DOWN,
   MOE_K_COMBINE,
   MOE_K_BALANCE_STATS,
+  MOE_K_BIAS_UPDATE,
   MOE_KERNEL_COUNT
 };
 int moe_ctx_set_tracing(moe_ctx* ctx, int enable);

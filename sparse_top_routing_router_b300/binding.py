@@ -27,13 +27,13 @@ MOE_TEST_HOOK_NONE, MOE_TEST_HOOK_WITHHOLD_LOAD = 0, 1
 
 KERNEL_NAMES = ["router_logits", "router_select", "dispatch_count", "dispatch_scan",
                 "dispatch_scatter", "dispatch_gather", "expert_gate_up", "expert_down",
-                "combine", "balance_stats"]
+                "combine", "balance_stats", "bias_update"]
 MOE_KERNEL_COUNT = len(KERNEL_NAMES)
 
 EXPORTS = ["moe_ctx_create", "moe_ctx_destroy", "moe_workspace_bytes", "moe_workspace_init",
            "moe_capacity", "moe_router_topk", "moe_dispatch", "moe_dispatch_static",
            "moe_grouped_swiglu",
-           "moe_combine", "moe_balance_stats", "moe_get_device_status",
+           "moe_combine", "moe_balance_stats", "moe_bias_update", "moe_get_device_status",
            "moe_ctx_set_tracing", "moe_ctx_trace_read", "moe_ctx_set_test_hook",
            "moe_kernel_name",
            "moe_status_string", "moe_last_error_detail", "moe_version"]
@@ -82,6 +82,7 @@ def lib() -> C.CDLL:
     L.moe_grouped_swiglu.argtypes = [vp, C.POINTER(ExpertDesc)] + [vp] * 12 + [sz, vp]
     L.moe_combine.argtypes = [vp, i, i, i, vp, vp, vp, vp, vp, vp, vp]
     L.moe_balance_stats.argtypes = [vp, i, i, i, vp, vp, vp, d, vp, vp, vp, vp]
+    L.moe_bias_update.argtypes = [vp, i, i, i, vp, C.c_float, vp, vp]
     L.moe_get_device_status.argtypes = [vp, vp, C.POINTER(i), i, vp]
     L.moe_ctx_set_tracing.argtypes = [vp, i]
     L.moe_ctx_set_test_hook.argtypes = [vp, i, i]
@@ -237,6 +238,13 @@ def moe_balance_stats(ctx: Context, T: int, k: int, counts, prob_colsum, alpha: 
     _check("moe_balance_stats", lib().moe_balance_stats(
         ctx.handle, T, k, E, _p(counts), _p(offsets), _p(prob_colsum), float(alpha), _p(f),
         _p(p), _p(out), _stream(stream)))
+
+
+def moe_bias_update(ctx: Context, T: int, k: int, counts, gamma: float, bias,
+                    stream=None) -> None:
+    E = counts.shape[0]
+    _check("moe_bias_update", lib().moe_bias_update(
+        ctx.handle, T, k, E, _p(counts), float(gamma), _p(bias), _stream(stream)))
 
 
 def moe_get_device_status(ctx: Context, ws, reset: bool = True, stream=None) -> int:

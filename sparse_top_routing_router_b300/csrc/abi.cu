@@ -119,7 +119,7 @@ int check_shape(int T, int E, int k) {
 
 extern "C" {
 
-int moe_version(void) { return 10100; }
+int moe_version(void) { return 10200; }
 
 const char* moe_status_string(int s) {
   switch (s) {
@@ -140,7 +140,7 @@ const char* moe_kernel_name(int id) {
   static const char* names[MOE_KERNEL_COUNT] = {
       "router_logits",    "router_select",    "dispatch_count", "dispatch_scan",
       "dispatch_scatter", "dispatch_gather",  "expert_gate_up", "expert_down",
-      "combine",          "balance_stats"};
+      "combine",          "balance_stats",    "bias_update"};
   return (id >= 0 && id < MOE_KERNEL_COUNT) ? names[id] : "unknown";
 }
 
@@ -513,6 +513,20 @@ int moe_balance_stats(moe_ctx* ctx, int T, int k, int E, const int32_t* counts,
   StatsArgs a{T, k, E, counts, offsets, prob_colsum, alpha, f, p, out};
   cudaError_t e = traced(ctx, MOE_K_BALANCE_STATS, s, [&] { return launch_balance_stats(a, s); });
   return e ? cuda_fail(e, "balance_stats launch") : ok();
+}
+
+int moe_bias_update(moe_ctx* ctx, int T, int k, int E, const int32_t* counts, float gamma,
+                    float* bias, moe_stream_t stream) {
+  int r = check_shape(T, E, k);
+  if (r) return r;
+  if (!counts || !bias) return fail(MOE_ERR_INVALID_ARG, "counts and bias are required");
+  if (!(gamma == gamma) || gamma - gamma != 0.f)
+    return fail(MOE_ERR_INVALID_ARG, "gamma must be finite");
+  if ((r = check_ctx(ctx))) return r;
+  cudaStream_t s = (cudaStream_t)stream;
+  BiasArgs a{E, (long long)T * k, counts, gamma, bias};
+  cudaError_t e = traced(ctx, MOE_K_BIAS_UPDATE, s, [&] { return launch_bias_update(a, s); });
+  return e ? cuda_fail(e, "bias_update launch") : ok();
 }
 
 int moe_get_device_status(moe_ctx* ctx, void* ws, int* status, int reset,

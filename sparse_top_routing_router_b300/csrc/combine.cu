@@ -10,6 +10,12 @@
 // balance_stats: §14.2.3 L = alpha * N * sum f_i p_i and the three monitoring signals it
 // names (routing entropy, per-expert load, drop rate), plus the load CV of the
 // "AI Knowledge Map - MoE" page.  One CTA, float64.
+//
+// bias_update: §14.2.3 bias-adjusted selection, the balancing step after a batch: an
+// expert whose load m_e (router choices before capacity) is above the balanced load
+// T k / E loses gamma from its selection bias, one below it gains gamma, one exactly at it
+// keeps its bias.  The comparison is exact in integers (E m_e against T k); the update is
+// one float32 addition.
 #include <math.h>
 
 #include "moe_internal.h"
@@ -120,7 +126,20 @@ __global__ void __launch_bounds__(kMaxE) balance_stats_kernel(StatsArgs a) {
   }
 }
 
+__global__ void __launch_bounds__(256) bias_update_kernel(BiasArgs a) {
+  const int e = blockIdx.x * blockDim.x + threadIdx.x;
+  if (e >= a.E) return;
+  const long long load = (long long)a.counts[e] * a.E;
+  if (load > a.slots) a.bias[e] = a.bias[e] - a.gamma;
+  else if (load < a.slots) a.bias[e] = a.bias[e] + a.gamma;
+}
+
 }  // namespace
+
+cudaError_t launch_bias_update(const BiasArgs& a, cudaStream_t s) {
+  bias_update_kernel<<<(a.E + 255) / 256, 256, 0, s>>>(a);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t s) {
   // CTA per token and column chunk: a small batch is split along H so that the GPU gets

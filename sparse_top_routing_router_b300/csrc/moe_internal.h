@@ -189,4 +189,13 @@ struct StatsArgs {
 };
 cudaError_t launch_balance_stats(const StatsArgs& a, cudaStream_t s);
 
+struct BiasArgs {
+  int E;
+  long long slots;   // T * k
+  const int32_t* counts;
+  float gamma;
+  float* bias;
+};
+cudaError_t launch_bias_update(const BiasArgs& a, cudaStream_t s);
+
 }  // namespace moe

@@ -19,8 +19,11 @@ from .configs import MoEConfig
 class MoELayer:
     def __init__(self, cfg: MoEConfig, weights: Dict[str, torch.Tensor],
                  ctx: Optional[B.Context] = None, device: int = 0,
-                 capacity_factor: Optional[float] = None, gather: bool = True):
+                 capacity_factor: Optional[float] = None, gather: bool = True,
+                 bias_gamma: Optional[float] = None):
         self.cfg = cfg
+        # not None: every forward ends with the bias update step (update_bias)
+        self.bias_gamma = bias_gamma
         self.w = weights
         self.dev = torch.device("cuda", device)
         self.ctx = ctx if ctx is not None else B.Context(device)
@@ -90,9 +93,19 @@ class MoELayer:
                              O_shared=self.O_shared, stream=stream)
         B.moe_combine(self.ctx, self.O, self.row_of_slot, self.gate, Y,
                       O_shared=self.O_shared, Y_bf16=Y_bf16, stream=stream)
+        if self.bias_gamma is not None:
+            self.update_bias(self.bias_gamma, stream=stream)
         if stats:
             stream.wait_event(self._stats_done)   # the forward ends when both streams do
         return Y
+
+    def update_bias(self, gamma: float, stream=None) -> None:
+        """The balancing step after a forward: the selection bias moves by -gamma for
+        every overloaded expert and +gamma for every underloaded one, from this forward's
+        counts (in place on the layer's "bias" weight; enqueued on `stream`)."""
+        stream = torch.cuda.current_stream(self.dev) if stream is None else stream
+        B.moe_bias_update(self.ctx, self.T, self.cfg.k, self.counts, gamma, self.w["bias"],
+                          stream=stream)
 
     def forward_host(self, X_host: torch.Tensor, Y_host: torch.Tensor,
                      X_dev: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:

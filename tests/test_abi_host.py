@@ -37,7 +37,7 @@ def test_exports_match_header(L):
 
 
 def test_version_and_strings(L):
-    assert L.moe_version() == 10100
+    assert L.moe_version() == 10200
     assert B.status_string(0) == "ok"
     assert B.status_string(-4) == "device wait timed out"
     for i, n in enumerate(B.KERNEL_NAMES):
@@ -112,6 +112,15 @@ def test_validation_before_device(L):
     d = B.RouterDesc(16, 64, 8, 4, 1, 1, 0, 4, 2)
     r = L.moe_router_topk(None, C.byref(d), fake, fake, None, None, fake, fake, None, None,
                           fake, 1 << 20, None)
+    assert r == B.MOE_ERR_INVALID_ARG and "ctx" in B.last_error_detail()
+    # bias update: gamma must be finite; null pointers rejected
+    r = L.moe_bias_update(None, 16, 2, 8, fake, float("nan"), fake, None)
+    assert r == B.MOE_ERR_INVALID_ARG and "gamma" in B.last_error_detail()
+    r = L.moe_bias_update(None, 16, 2, 8, fake, float("inf"), fake, None)
+    assert r == B.MOE_ERR_INVALID_ARG and "gamma" in B.last_error_detail()
+    r = L.moe_bias_update(None, 16, 2, 8, None, 0.001, fake, None)
+    assert r == B.MOE_ERR_INVALID_ARG and "required" in B.last_error_detail()
+    r = L.moe_bias_update(None, 16, 2, 8, fake, 0.001, fake, None)
     assert r == B.MOE_ERR_INVALID_ARG and "ctx" in B.last_error_detail()
     # dispatch: X without Xperm
     r = L.moe_dispatch(None, 16, 2, 8, 64, 0, -1, fake, fake, fake, fake, fake, fake, None,

@@ -344,6 +344,59 @@ def route(X, Wg, k: int, score: str, renorm: bool, bias=None, logit_bias=None,
     return d
 
 
+def expert_choice(S: np.ndarray, C: int) -> Dict[str, np.ndarray]:
+    """Expert-choice routing  [LI §14.2, the two selection paradigms: expert-choice; P1,
+    "Expert Choice Routing"]: every expert takes the C tokens of the batch with the
+    largest affinity S[t, e]; ties go to the lower token index.  A token may be taken
+    by several experts or by none.
+
+    In the slot layout of token-choice routing with k = E: slot s = t*E + e is the pair
+    (token t, expert e).  Returns chosen[E, C] (each expert's tokens, ascending), the
+    rows ordered by (expert, token) - offsets[e] = e*C, row_of_slot[T*E] (-1 = not
+    taken), slot_of_row[E*C] - the gates gate[T, E] (S where taken, 0 elsewhere), idx[T, E]
+    = e in slot (t, e), and gap[E] = S_(C) - S_(C+1) down each expert's column (+inf
+    when C == T).
+    """
+    S = np.asarray(S, dtype=f64)
+    T, E = S.shape
+    if not 0 <= C <= T:
+        raise ValueError("expert-choice capacity outside [0, T]")
+    order = np.argsort(-S, axis=0, kind="stable")          # per column: descending
+    chosen = np.sort(order[:C, :].T, axis=1)
+    cols = np.arange(E)
+    if 0 < C < T:
+        gap = S[order[C - 1, cols], cols] - S[order[C, cols], cols]
+    else:
+        gap = np.full(E, np.inf)
+    row_of_slot = np.full(T * E, -1, dtype=np.int64)
+    slot_of_row = np.zeros(E * C, dtype=np.int64)
+    gate = np.zeros((T, E), dtype=f64)
+    for e in range(E):
+        rows = e * C + np.arange(C)
+        slots = chosen[e] * E + e
+        row_of_slot[slots] = rows
+        slot_of_row[rows] = slots
+        gate[chosen[e], e] = S[chosen[e], e]
+    return dict(chosen=chosen, offsets=np.arange(E + 1, dtype=np.int64) * C,
+                row_of_slot=row_of_slot, slot_of_row=slot_of_row, gate=gate,
+                idx=np.tile(np.arange(E, dtype=np.int64), (T, 1)), gap=gap)
+
+
+def route_expert_choice(X, Wg, k: int, score: str, logit_bias=None) -> Dict[str, np.ndarray]:
+    """Scoring and expert-choice selection on every token.  Each expert takes the
+    balanced load C = T*k/E (the average number of experts per token is k), which must
+    be an integer; S is the unbiased affinity (routing_affinity), since a per-expert
+    selection bias would shift a whole column and change no expert's choice."""
+    l = router_logits(X, Wg, logit_bias)
+    T, E = l.shape
+    if (T * k) % E:
+        raise ValueError("expert-choice needs E to divide T*k")
+    S = routing_affinity(l, score)
+    d = expert_choice(S, T * k // E)
+    d.update(logits=l, S=S)
+    return d
+
+
 ExpertFn = Callable[[int], Tuple[np.ndarray, np.ndarray, np.ndarray]]
 
 

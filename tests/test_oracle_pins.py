@@ -464,3 +464,66 @@ def test_bias_update_float32_rounding_is_single():
     under = 64 * counts < 256
     want = np.where(over, b - g, np.where(under, b + g, b)).astype(np.float32)
     np.testing.assert_array_equal(out, want)
+
+
+# ---------------------------------------------------------------- expert-choice routing
+
+def test_expert_choice_brute_force():
+    rng = np.random.default_rng(11)
+    T, E, C = 8, 3, 3
+    S = rng.random((T, E))
+    r = O.expert_choice(S, C)
+    for e in range(E):
+        col = S[:, e]
+        best = max(itertools.combinations(range(T), C), key=lambda c: sum(col[t] for t in c))
+        assert r["chosen"][e].tolist() == list(best)
+        rest = [col[t] for t in range(T) if t not in best]
+        assert r["gap"][e] == pytest.approx(min(col[list(best)]) - max(rest), abs=1e-15)
+
+
+def test_expert_choice_hand_examples():
+    # T = 4 tokens, E = 2 experts, k = 1: C = T*k/E = 2 tokens per expert
+    S = np.array([[0.9, 0.1], [0.6, 0.4], [0.3, 0.7], [0.2, 0.8]])
+    r = O.expert_choice(S, 2)
+    assert r["chosen"].tolist() == [[0, 1], [2, 3]]
+    np.testing.assert_allclose(r["gap"], [0.6 - 0.3, 0.7 - 0.4], atol=1e-15)
+    # tokens 0 and 1 are taken twice, tokens 2 and 3 by nobody (the page's caveat)
+    S = np.array([[0.9, 0.8], [0.6, 0.7], [0.1, 0.2], [0.3, 0.05]])
+    r = O.expert_choice(S, 2)
+    assert r["chosen"].tolist() == [[0, 1], [0, 1]]
+    assert r["row_of_slot"].tolist() == [0, 2, 1, 3, -1, -1, -1, -1]
+    assert r["slot_of_row"].tolist() == [0, 2, 1, 3]
+    np.testing.assert_array_equal(r["gate"], [[0.9, 0.8], [0.6, 0.7], [0, 0], [0, 0]])
+
+
+def test_expert_choice_ties_and_balance():
+    S = np.full((6, 3), 0.5)
+    r = O.expert_choice(S, 4)
+    assert r["chosen"].tolist() == [[0, 1, 2, 3]] * 3      # ties: lowest token indices
+    assert np.all(r["gap"] == 0)
+    rng = np.random.default_rng(4)
+    S = rng.random((40, 5))
+    r = O.expert_choice(S, 16)
+    # every expert takes exactly C; the rows are the inverse permutation of their slots
+    assert np.all((r["row_of_slot"].reshape(40, 5) >= 0).sum(0) == 16)
+    assert np.array_equal(r["row_of_slot"][r["slot_of_row"]], np.arange(80))
+    assert np.array_equal(r["slot_of_row"] % 5, np.repeat(np.arange(5), 16))
+
+
+def test_expert_choice_single_expert_is_dense():
+    # E = 1, k = 1: the expert takes every token with softmax affinity 1
+    rng = np.random.default_rng(6)
+    X = rng.standard_normal((7, 4))
+    Wg = rng.standard_normal((4, 1))
+    r = O.route_expert_choice(X, Wg, 1, "softmax")
+    assert r["chosen"].tolist() == [list(range(7))]
+    np.testing.assert_array_equal(r["gate"], np.ones((7, 1)))
+    Wgt, Wup, Wdn = (rng.standard_normal((3, 4)), rng.standard_normal((3, 4)),
+                     rng.standard_normal((4, 3)))
+    Y = O.combine_subset(X, r, lambda e: (Wgt, Wup, Wdn), np.arange(7))
+    np.testing.assert_allclose(Y, O.swiglu_expert(X, Wgt, Wup, Wdn), rtol=1e-14)
+
+
+def test_expert_choice_needs_integer_capacity():
+    with pytest.raises(ValueError):
+        O.route_expert_choice(np.zeros((5, 2)), np.zeros((2, 2)), 1, "softmax")

@@ -68,6 +68,8 @@ def workload_config(cfg: K.MoEConfig, cf) -> dict:
          "capacity_factor": cf, "router": "fp32", "experts": cfg.dtype}
     if cfg.n_groups > 1:
         d["router_groups"] = {"n_groups": cfg.n_groups, "topk_groups": cfg.topk_groups}
+    if cfg.expert_choice:
+        d["routing"] = f"expert choice: each expert takes its C = T*k/E = {cfg.T * cfg.k // cfg.E} best tokens"
     return d
 
 
@@ -208,11 +210,16 @@ def oracle_sample(cfg, d, cf, n_tokens: int, seed: int):
     lb = host(d["logit_bias"]) if "logit_bias" in d else None
     C = None if cf is None else O.capacity(cf, cfg.T, cfg.k, cfg.E)
     t0 = time.perf_counter()
-    r = O.route(X, Wg, cfg.k, cfg.score, cfg.renorm, bias, lb, C, n_groups=cfg.n_groups,
-                topk_groups=cfg.topk_groups)
+    if cfg.expert_choice:
+        r = O.route_expert_choice(X, Wg, cfg.k, cfg.score, lb)
+    else:
+        r = O.route(X, Wg, cfg.k, cfg.score, cfg.renorm, bias, lb, C, n_groups=cfg.n_groups,
+                    topk_groups=cfg.topk_groups)
     t_route = time.perf_counter() - t0
     tokens = token_subset(cfg.T, n_tokens, seed).numpy()
-    need = sorted({int(e) for e in r["idx"][tokens].reshape(-1)})
+    ks = r["idx"].shape[1]
+    taken = r["row_of_slot"].reshape(cfg.T, ks)[tokens] >= 0
+    need = sorted({int(e) for e in r["idx"][tokens][taken]})
     W = {e: (host(d["W_gate"][e]), host(d["W_up"][e]), host(d["W_down"][e])) for e in need}
     shared = (host(d["Ws_gate"]), host(d["Ws_up"]), host(d["Ws_down"])) if cfg.shared else None
     t0 = time.perf_counter()
@@ -337,7 +344,8 @@ def run_gpu(args, cfg, cf):
     gu_flops = 2.0 * rows * cfg.H * 2 * cfg.I
     dn_flops = 2.0 * rows * cfg.I * cfg.H
     elt = 2 if cfg.dtype == "bf16" else 4
-    n_touched = int((layer.counts > 0).sum().item()) + (1 if cfg.shared else 0)
+    # experts with at least one kept row (expert-choice routing fills every expert)
+    n_touched = int((torch.diff(layer.offsets) > 0).sum().item()) + (1 if cfg.shared else 0)
     w_touched = n_touched * 3 * cfg.H * cfg.I * elt
     # algorithmic bytes of the gate/up launch: its touched weights once, A rows in, h out
     gu_bytes = n_touched * 2 * cfg.H * cfg.I * elt + rows * cfg.H * elt + rows * cfg.I * 2
@@ -437,6 +445,8 @@ def main():
     ap.add_argument("--bias-update", type=float, default=None, metavar="GAMMA",
                     help="end every forward with the bias update step (selection bias "
                          "-/+ GAMMA for over/underloaded experts)")
+    ap.add_argument("--expert-choice", action="store_true",
+                    help="expert-choice routing: every expert takes its C = T*k/E best tokens")
     ap.add_argument("--router-groups", default=None, metavar="G:M",
                     help="group-limited routing: G expert groups, M of them per token")
     args = ap.parse_args()
@@ -447,6 +457,10 @@ def main():
     if args.router_groups:
         G, M = (int(v) for v in args.router_groups.split(":"))
         cfg = dataclasses.replace(cfg, n_groups=G, topk_groups=M)
+    if args.expert_choice:
+        if args.router_groups or args.capacity_factor is not None or args.bias_update is not None:
+            ap.error("--expert-choice takes no groups, capacity factor or bias update")
+        cfg = dataclasses.replace(cfg, expert_choice=True, capacity_factors=())
     cf = args.capacity_factor
     if cf is None and cfg.capacity_factors:
         cf = cfg.capacity_factors[0]

@@ -19,8 +19,8 @@
  *    library allocates no device memory: scratch lives in a caller-provided workspace
  *    of moe_workspace_bytes() bytes whose first 256 bytes hold a device status word
  *    (int32 at byte 0) and must be zeroed once (moe_workspace_init) before first use.
- *    The int32 at byte 4 counts the rows the last moe_router_topk call re-decided from
- *    exact dot products (a diagnostic).
+ *    The int32 at byte 4 counts the rows the last moe_router_topk call (the experts the
+ *    last moe_expert_choice call) re-decided from exact dot products (a diagnostic).
  *  - Every call is asynchronous on `stream`, performs no host synchronisation (except
  *    moe_get_device_status and moe_ctx_trace_read, which say so) and returns an int
  *    status: MOE_OK (0) or a negative MOE_ERR_*.  Argument checks run before anything is
@@ -141,6 +141,40 @@ int moe_router_topk(moe_ctx* ctx, const moe_router_desc* d, const void* X,
                     int32_t* topk_idx, float* topk_gate, float* key_gap,
                     double* prob_colsum, void* ws, size_t ws_bytes, moe_stream_t stream);
 
+/* Expert-choice routing ("LLM Internals §14.2", the two selection paradigms: expert-
+ * choice; "MoE 03: efficiency frontiers", Expert Choice Routing).  Instead of every token
+ * choosing k experts, every expert takes the C = T*k/E tokens of the batch with the
+ * largest affinity S[t, e]: the softmax probability over the experts (MOE_SCORE_SOFTMAX)
+ * or the sigmoid s (MOE_SCORE_SIGMOID).  Ties go to the lower token index.  Every expert
+ * carries exactly C rows and nothing is dropped, but a token may be taken by several
+ * experts or by none.  Slots are (token, expert) pairs s = t*E + e, so steps 5-6 run
+ * unchanged with E slots per token:
+ *   offsets     [E+1] int32 out: e*C
+ *   row_of_slot [T*E] int32 out: permuted row of slot t*E+e, -1 if e did not take t
+ *   slot_of_row [T*k] int32 out: the slot of each row (rows by expert, then token)
+ *   slot_gate   [T*E] fp32 out: S[t, e] where e took t, 0 elsewhere (moe_combine's gate)
+ *   col_gap     [E] fp32 out (nullable): S_(C) - S_(C+1) down each expert's column
+ *               (+inf if C is 0 or T)
+ * d: T <= 32768, H, E, k (the average experts per token; E must divide T*k), score,
+ * x_dtype.  renorm does not apply and there is no selection bias: a per-expert bias shifts
+ * a whole column and changes no choice.  n_groups must be 0 or 1.  Exactness as for
+ * moe_router_topk: a column whose C-th/(C+1)-th margin lies inside the error bound of its
+ * fp32 affinities is re-decided from the exact affinities of its band tokens.
+ * Then moe_gather_rows (R = T*k, k = E), moe_grouped_swiglu (k) and moe_combine (k = E,
+ * row_of_slot, slot_gate). */
+int moe_expert_choice(moe_ctx* ctx, const moe_router_desc* d, const void* X,
+                      const float* Wg, const float* logit_bias, int32_t* offsets,
+                      int32_t* row_of_slot, int32_t* slot_of_row, float* slot_gate,
+                      float* col_gap, void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* Xperm[r] = X[slot_of_row[r] / k] for r < R: the row gather of a slot layout in which a
+ * token may fill any number of rows (expert-choice routing, k = E).  X has T rows; a slot
+ * outside [0, T*k) is recorded in the workspace status word (MOE_ERR_DEVICE_INDEX) and
+ * its row left untouched.  The row size H * element size must be a multiple of 16 B. */
+int moe_gather_rows(moe_ctx* ctx, int R, int k, int H, int x_dtype,
+                    const int32_t* slot_of_row, const void* X, int T, void* Xperm, void* ws,
+                    moe_stream_t stream);
+
 /* ------------------------------------------------------------------ step 4 */
 
 /* Group the T*k (token, choice) slots by expert (§14.2.1 step 4) under an optional
@@ -207,7 +241,8 @@ int moe_grouped_swiglu(moe_ctx* ctx, const moe_expert_desc* d, const void* X,
 /* Y[t] = sum over kept j of topk_gate[t, j] * O[row_of_slot[t*k+j]]  (+ O_shared[t])
  * (§14.2.1 step 6; "AI Knowledge Map - MoE" final weighted sum).  A dropped slot adds
  * nothing and the remaining gates are not renormalised.
- *   O_shared nullable; Y [T, H] fp32 out; Y_bf16 [T, H] nullable bf16 copy of Y. */
+ *   O_shared nullable; Y [T, H] fp32 out; Y_bf16 [T, H] nullable bf16 copy of Y.
+ *   k: slots per token, at most 512 (E for expert-choice routing). */
 int moe_combine(moe_ctx* ctx, int T, int k, int H, const float* O, const float* O_shared,
                 const int32_t* row_of_slot, const float* topk_gate, float* Y,
                 void* Y_bf16, moe_stream_t stream);

@@ -34,6 +34,7 @@ EXPORTS = ["moe_ctx_create", "moe_ctx_destroy", "moe_workspace_bytes", "moe_work
            "moe_capacity", "moe_router_topk", "moe_dispatch", "moe_dispatch_static",
            "moe_grouped_swiglu",
            "moe_combine", "moe_balance_stats", "moe_bias_update", "moe_get_device_status",
+           "moe_expert_choice", "moe_gather_rows",
            "moe_ctx_set_tracing", "moe_ctx_trace_read", "moe_ctx_set_test_hook",
            "moe_kernel_name",
            "moe_status_string", "moe_last_error_detail", "moe_version"]
@@ -83,6 +84,9 @@ def lib() -> C.CDLL:
     L.moe_combine.argtypes = [vp, i, i, i, vp, vp, vp, vp, vp, vp, vp]
     L.moe_balance_stats.argtypes = [vp, i, i, i, vp, vp, vp, d, vp, vp, vp, vp]
     L.moe_bias_update.argtypes = [vp, i, i, i, vp, C.c_float, vp, vp]
+    L.moe_expert_choice.argtypes = [vp, C.POINTER(RouterDesc), vp, vp, vp, vp, vp, vp, vp,
+                                    vp, vp, sz, vp]
+    L.moe_gather_rows.argtypes = [vp, i, i, i, i, vp, vp, i, vp, vp, vp]
     L.moe_get_device_status.argtypes = [vp, vp, C.POINTER(i), i, vp]
     L.moe_ctx_set_tracing.argtypes = [vp, i]
     L.moe_ctx_set_test_hook.argtypes = [vp, i, i]
@@ -194,6 +198,26 @@ def moe_router_topk(ctx: Context, X, Wg, k: int, score: int, renorm: bool, topk_
     _check("moe_router_topk", lib().moe_router_topk(
         ctx.handle, C.byref(d), _p(X), _p(Wg), _p(bias), _p(logit_bias), _p(topk_idx),
         _p(topk_gate), _p(key_gap), _p(prob_colsum), _p(ws), ws.numel() * ws.element_size(),
+        _stream(stream)))
+
+
+def moe_expert_choice(ctx: Context, X, Wg, k: int, score: int, offsets, row_of_slot,
+                      slot_of_row, slot_gate, ws, logit_bias=None, col_gap=None,
+                      stream=None) -> None:
+    T, H = X.shape
+    E = Wg.shape[1]
+    d = RouterDesc(T, H, E, k, score, 0, x_dtype_code(X), 0, 0)
+    _check("moe_expert_choice", lib().moe_expert_choice(
+        ctx.handle, C.byref(d), _p(X), _p(Wg), _p(logit_bias), _p(offsets), _p(row_of_slot),
+        _p(slot_of_row), _p(slot_gate), _p(col_gap), _p(ws), ws.numel() * ws.element_size(),
+        _stream(stream)))
+
+
+def moe_gather_rows(ctx: Context, slot_of_row, k: int, X, Xperm, ws, stream=None) -> None:
+    R = slot_of_row.shape[0]
+    T, H = X.shape
+    _check("moe_gather_rows", lib().moe_gather_rows(
+        ctx.handle, R, k, H, x_dtype_code(X), _p(slot_of_row), _p(X), T, _p(Xperm), _p(ws),
         _stream(stream)))
 
 

@@ -32,6 +32,7 @@ class MoEConfig:
     selection_bias_std: float = 0.0            # sigmoid: per-expert bias for selection only
     zipf_s: float = 0.0                        # >0: logit offset -s*ln(e+1) per expert
     alpha: float = 0.0                         # balance-loss coefficient
+    expert_choice: bool = False                # every expert takes its C = T*k/E best tokens
     n_groups: int = 0                          # group-limited routing: expert groups
     topk_groups: int = 0                       # ... and the groups a token may use
     x_std: float = 1.0

@@ -115,11 +115,87 @@ int check_shape(int T, int E, int k) {
   return MOE_OK;
 }
 
+// Router scoring shared by token-choice and expert-choice routing: fills the logits part
+// of `a` (shapes, inputs, workspace pointers, split-K choice, error bound) and launches the
+// logit kernels (traced as router_logits).  The caller has validated d and the buffers.
+int router_logits_stage(moe_ctx* ctx, const moe_router_desc* d, const void* X,
+                        const float* Wg, const float* logit_bias, void* ws, size_t ws_bytes,
+                        const WsLayout& L, RouterArgs& a, cudaStream_t s) {
+  // the tensor-core router also needs the W_g pieces; the fp32 CUDA-core one does not
+  const bool use_tc = d->x_dtype == MOE_DTYPE_BF16 && d->E % 8 == 0 &&
+                      d->H % 64 == 0 && d->T >= 256 && ws_bytes >= L.chunk_counts;
+  a = RouterArgs{};
+  a.T = d->T;
+  a.H = d->H;
+  a.E = d->E;
+  a.k = d->k;
+  a.score = d->score;
+  a.renorm = d->renorm;
+  a.x_dtype = d->x_dtype;
+  a.X = X;
+  a.Wg = Wg;
+  a.logit_bias = logit_bias;
+  a.logits = reinterpret_cast<float2*>(static_cast<char*>(ws) + L.logits);
+  a.num_sms = ctx->num_sms;
+  a.wait_limit_ns = ctx->wait_limit_ns;
+  a.wsplit = use_tc ? reinterpret_cast<__nv_bfloat16*>(static_cast<char*>(ws) + L.wsplit)
+                    : nullptr;
+  a.logits_part = nullptr;
+  if (use_tc) {
+    // Every slice at most kRouterTcMaxK products long.  Among the slice counts the
+    // workspace holds, take the one with the least time per slice-wave: tiles * S work
+    // units over num_sms CTAs take ceil(tiles * S / num_sms) rounds of 1/S of a tile each.
+    const int tiles = ((d->T + 127) / 128) * ((d->E + 255) / 256);
+    const bool fused = router_tc_fused(d->E);
+    const int nkb = (fused ? 1 : 3) * d->H / 64;
+    const int kb_chain = kRouterTcMaxK / (fused ? 3 * 64 : 64);   // k-blocks per chain
+    const int need = (nkb + kb_chain - 1) / kb_chain;
+    const int cap = router_split_cap(d->T, d->H);
+    int hi = cap >= 2 ? 2 * (cap - 1) : 1;   // fp32 partials behind slice 0
+    if (hi > nkb) hi = nkb;
+    const int sms = ctx->num_sms > 0 ? ctx->num_sms : 1;
+    int best = need > hi ? hi : need;
+    double best_t = 1e30;
+    for (int sp = best; sp <= hi; ++sp) {
+      const double t = (double)((tiles * sp + sms - 1) / sms) / sp;
+      if (t < best_t - 1e-12) {
+        best_t = t;
+        best = sp;
+      }
+    }
+    a.splits = best;
+    if (best > 1)
+      a.logits_part = reinterpret_cast<float*>(a.logits + (size_t)d->T * d->E);
+    a.eps_rel = kRouterEpsTensor;
+  } else {
+    a.splits = router_splits(d->T, d->H);
+    a.eps_rel = kRouterEpsCuda;
+  }
+  a.status = static_cast<int*>(ws);
+  a.refined = static_cast<int*>(ws) + 1;
+  a.refine_list = reinterpret_cast<int4*>(static_cast<char*>(ws) + L.refine);
+  cudaError_t e;
+  if ((e = cudaMemsetAsync(a.refined, 0, sizeof(int), s))) return cuda_fail(e, "cudaMemsetAsync");
+  if (use_tc) {
+    bool bad = false;
+    e = traced(ctx, MOE_K_ROUTER_LOGITS, s, [&] {
+      cudaError_t r = launch_router_split(a, s);
+      return r != cudaSuccess ? r : launch_router_tc(a, ctx->encode, &bad, s);
+    }, 2);
+    if (bad) return fail(MOE_ERR_INVALID_ARG, "tensor map encoding failed (router)");
+    if (e) return cuda_fail(e, "router_logits launch");
+  } else if ((e = traced(ctx, MOE_K_ROUTER_LOGITS, s,
+                         [&] { return launch_router_logits(a, s); }))) {
+    return cuda_fail(e, "router_logits launch");
+  }
+  return MOE_OK;
+}
+
 }  // namespace
 
 extern "C" {
 
-int moe_version(void) { return 10200; }
+int moe_version(void) { return 10300; }
 
 const char* moe_status_string(int s) {
   switch (s) {
@@ -256,9 +332,6 @@ int moe_router_topk(moe_ctx* ctx, const moe_router_desc* d, const void* X, const
   if (!aligned16(X) || !aligned16(Wg) || !aligned16(ws))
     return fail(MOE_ERR_INVALID_ARG, "X, Wg and ws must be 16-byte aligned");
   const WsLayout L = ws_layout(d->T, d->H, d->E, 0, d->k, d->x_dtype, 0);
-  // the tensor-core router also needs the W_g pieces; the fp32 CUDA-core one does not
-  const bool use_tc = d->x_dtype == MOE_DTYPE_BF16 && d->E % 8 == 0 &&
-                      d->H % 64 == 0 && d->T >= 256 && ws_bytes >= L.chunk_counts;
   if (ws_bytes < L.wsplit) return fail(MOE_ERR_INVALID_ARG, "workspace too small");
   if ((r = check_ctx(ctx))) return r;
   cudaStream_t s = (cudaStream_t)stream;
@@ -267,80 +340,115 @@ int moe_router_topk(moe_ctx* ctx, const moe_router_desc* d, const void* X, const
     return cuda_fail(e, "cudaMemsetAsync");
   if (d->T == 0) return ok();
   RouterArgs a;
-  a.T = d->T;
-  a.H = d->H;
-  a.E = d->E;
-  a.k = d->k;
-  a.score = d->score;
-  a.renorm = d->renorm;
-  a.x_dtype = d->x_dtype;
+  if ((r = router_logits_stage(ctx, d, X, Wg, logit_bias, ws, ws_bytes, L, a, s))) return r;
+  a.bias = bias;
   a.n_groups = n_groups;
   a.topk_groups = topk_groups;
-  a.X = X;
-  a.Wg = Wg;
-  a.bias = bias;
-  a.logit_bias = logit_bias;
-  a.logits = reinterpret_cast<float2*>(static_cast<char*>(ws) + L.logits);
-  a.num_sms = ctx->num_sms;
-  a.wait_limit_ns = ctx->wait_limit_ns;
-  a.wsplit = use_tc ? reinterpret_cast<__nv_bfloat16*>(static_cast<char*>(ws) + L.wsplit)
-                    : nullptr;
-  a.logits_part = nullptr;
-  if (use_tc) {
-    // Every slice at most kRouterTcMaxK products long.  Among the slice counts the
-    // workspace holds, take the one with the least time per slice-wave: tiles * S work
-    // units over num_sms CTAs take ceil(tiles * S / num_sms) rounds of 1/S of a tile each.
-    const int tiles = ((d->T + 127) / 128) * ((d->E + 255) / 256);
-    const bool fused = router_tc_fused(d->E);
-    const int nkb = (fused ? 1 : 3) * d->H / 64;
-    const int kb_chain = kRouterTcMaxK / (fused ? 3 * 64 : 64);   // k-blocks per chain
-    const int need = (nkb + kb_chain - 1) / kb_chain;
-    const int cap = router_split_cap(d->T, d->H);
-    int hi = cap >= 2 ? 2 * (cap - 1) : 1;   // fp32 partials behind slice 0
-    if (hi > nkb) hi = nkb;
-    const int sms = ctx->num_sms > 0 ? ctx->num_sms : 1;
-    int best = need > hi ? hi : need;
-    double best_t = 1e30;
-    for (int sp = best; sp <= hi; ++sp) {
-      const double t = (double)((tiles * sp + sms - 1) / sms) / sp;
-      if (t < best_t - 1e-12) {
-        best_t = t;
-        best = sp;
-      }
-    }
-    a.splits = best;
-    if (best > 1)
-      a.logits_part = reinterpret_cast<float*>(a.logits + (size_t)d->T * d->E);
-    a.eps_rel = kRouterEpsTensor;
-  } else {
-    a.splits = router_splits(d->T, d->H);
-    a.eps_rel = kRouterEpsCuda;
-  }
   a.idx = topk_idx;
   a.gate = topk_gate;
   a.gap = key_gap;
   a.colsum = prob_colsum;
-  a.status = static_cast<int*>(ws);
-  a.refined = static_cast<int*>(ws) + 1;
-  a.refine_list = reinterpret_cast<int4*>(static_cast<char*>(ws) + L.refine);
-  if ((e = cudaMemsetAsync(a.refined, 0, sizeof(int), s))) return cuda_fail(e, "cudaMemsetAsync");
-  if (use_tc) {
-    bool bad = false;
-    e = traced(ctx, MOE_K_ROUTER_LOGITS, s, [&] {
-      cudaError_t r = launch_router_split(a, s);
-      return r != cudaSuccess ? r : launch_router_tc(a, ctx->encode, &bad, s);
-    }, 2);
-    if (bad) return fail(MOE_ERR_INVALID_ARG, "tensor map encoding failed (router)");
-    if (e) return cuda_fail(e, "router_logits launch");
-  } else if ((e = traced(ctx, MOE_K_ROUTER_LOGITS, s,
-                         [&] { return launch_router_logits(a, s); }))) {
-    return cuda_fail(e, "router_logits launch");
-  }
   // selection and exact re-decision, after a reduce kernel that sums split-K partials
   if ((e = traced(ctx, MOE_K_ROUTER_SELECT, s, [&] { return launch_router_select(a, s); },
                   a.splits > 1 ? 3 : 2)))
     return cuda_fail(e, "router_select launch");
   return ok();
+}
+
+int moe_expert_choice(moe_ctx* ctx, const moe_router_desc* d, const void* X, const float* Wg,
+                      const float* logit_bias, int32_t* offsets, int32_t* row_of_slot,
+                      int32_t* slot_of_row, float* slot_gate, float* col_gap, void* ws,
+                      size_t ws_bytes, moe_stream_t stream) {
+  if (!d) return fail(MOE_ERR_INVALID_ARG, "desc is null");
+  int r = check_shape(d->T, d->E, d->k);
+  if (r) return r;
+  if (d->H < 1) return fail(MOE_ERR_INVALID_ARG, "H = %d", d->H);
+  if (d->score != MOE_SCORE_SOFTMAX && d->score != MOE_SCORE_SIGMOID)
+    return fail(MOE_ERR_INVALID_ARG, "score = %d", d->score);
+  if (d->x_dtype != MOE_DTYPE_BF16 && d->x_dtype != MOE_DTYPE_F32)
+    return fail(MOE_ERR_INVALID_ARG, "x_dtype = %d", d->x_dtype);
+  if (d->n_groups > 1)
+    return fail(MOE_ERR_UNSUPPORTED, "expert-choice routing takes no expert groups");
+  if (((long long)d->T * d->k) % d->E != 0)
+    return fail(MOE_ERR_INVALID_ARG, "E = %d must divide T*k = %lld (C = T*k/E)", d->E,
+                (long long)d->T * d->k);
+  if (d->T > kEcMaxT)
+    return fail(MOE_ERR_UNSUPPORTED, "expert-choice routing takes T <= %d tokens", kEcMaxT);
+  if ((long long)d->T * d->E > 0x7fffffffLL)
+    return fail(MOE_ERR_UNSUPPORTED, "T*E exceeds int32");
+  if (d->T > 0 && (!X || !Wg || !offsets || !row_of_slot || !slot_of_row || !slot_gate))
+    return fail(MOE_ERR_INVALID_ARG,
+                "X, Wg, offsets, row_of_slot, slot_of_row and slot_gate are required");
+  if (!ws) return fail(MOE_ERR_INVALID_ARG, "workspace is null");
+  if (!aligned16(X) || !aligned16(Wg) || !aligned16(ws))
+    return fail(MOE_ERR_INVALID_ARG, "X, Wg and ws must be 16-byte aligned");
+  const WsLayout L = ws_layout(d->T, d->H, d->E, 0, d->k, d->x_dtype, 0);
+  if (ws_bytes < L.h) return fail(MOE_ERR_INVALID_ARG, "workspace too small");
+  if ((r = check_ctx(ctx))) return r;
+  cudaStream_t s = (cudaStream_t)stream;
+  cudaError_t e;
+  const int C = (int)((long long)d->T * d->k / d->E);
+  if (d->T == 0) {
+    if (offsets && (e = cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (d->E + 1), s)))
+      return cuda_fail(e, "cudaMemsetAsync");
+    return ok();
+  }
+  ExpertChoiceArgs a;
+  if ((r = router_logits_stage(ctx, d, X, Wg, logit_bias, ws, ws_bytes, L, a.r, s))) return r;
+  char* w = static_cast<char*>(ws);
+  a.C = C;
+  a.St = reinterpret_cast<float*>(w + L.ec_st);
+  a.exS = reinterpret_cast<double*>(w + L.ec_exs);
+  a.need = reinterpret_cast<int*>(w + L.ec_need);
+  a.tok_list = reinterpret_cast<int*>(w + L.ec_tok);
+  a.col_list = reinterpret_cast<int*>(w + L.ec_col);
+  a.col_info = reinterpret_cast<int4*>(w + L.ec_info);
+  a.ctr = reinterpret_cast<int*>(w + L.ec_ctr);
+  a.offsets = offsets;
+  a.row_of_slot = row_of_slot;
+  a.slot_of_row = slot_of_row;
+  a.gate = slot_gate;
+  a.gap = col_gap;
+  const size_t slots = (size_t)d->T * d->E;
+  if ((e = cudaMemsetAsync(a.ctr, 0, 16, s)) ||
+      (e = cudaMemsetAsync(a.need, 0, sizeof(int) * d->T, s)) ||
+      (e = cudaMemsetAsync(row_of_slot, 0xff, sizeof(int32_t) * slots, s)) ||
+      (e = cudaMemsetAsync(slot_gate, 0, sizeof(float) * slots, s)))
+    return cuda_fail(e, "cudaMemsetAsync");
+  // the split-K reduce, affinities, per-expert selection, exact rows, fix-up
+  if ((e = traced(ctx, MOE_K_ROUTER_SELECT, s, [&] {
+         cudaError_t q = launch_router_reduce(a.r, s);
+         return q != cudaSuccess ? q : launch_expert_choice(a, s);
+       }, a.r.splits > 1 ? 5 : 4)))
+    return cuda_fail(e, "expert-choice launch");
+  // the diagnostic counter: experts re-decided from exact affinities
+  if ((e = cudaMemcpyAsync(static_cast<int*>(ws) + 1, a.ctr + 1, sizeof(int),
+                           cudaMemcpyDeviceToDevice, s)))
+    return cuda_fail(e, "cudaMemcpyAsync");
+  return ok();
+}
+
+int moe_gather_rows(moe_ctx* ctx, int R, int k, int H, int x_dtype, const int32_t* slot_of_row,
+                    const void* X, int T, void* Xperm, void* ws, moe_stream_t stream) {
+  if (R < 0 || k < 1 || k > kMaxE || T < 0)
+    return fail(MOE_ERR_INVALID_ARG, "R = %d, k = %d, T = %d", R, k, T);
+  if (x_dtype != MOE_DTYPE_BF16 && x_dtype != MOE_DTYPE_F32)
+    return fail(MOE_ERR_INVALID_ARG, "x_dtype = %d", x_dtype);
+  if (H < 1 || (H * (x_dtype == MOE_DTYPE_BF16 ? 2 : 4)) % 16 != 0)
+    return fail(MOE_ERR_UNSUPPORTED, "row of H = %d elements is not a multiple of 16 B", H);
+  if (R > 0 && (!slot_of_row || !X || !Xperm || !ws))
+    return fail(MOE_ERR_INVALID_ARG, "slot_of_row, X, Xperm and ws are required");
+  if (!aligned16(X) || !aligned16(Xperm))
+    return fail(MOE_ERR_INVALID_ARG, "X and Xperm must be 16-byte aligned");
+  int r = check_ctx(ctx);
+  if (r) return r;
+  cudaStream_t s = (cudaStream_t)stream;
+  const int row_bytes = H * (x_dtype == MOE_DTYPE_BF16 ? 2 : 4);
+  cudaError_t e = traced(ctx, MOE_K_DISPATCH_GATHER, s, [&] {
+    return launch_gather_rows(R, k, row_bytes, slot_of_row, X, Xperm, static_cast<int*>(ws),
+                              T, s);
+  });
+  return e ? cuda_fail(e, "gather launch") : ok();
 }
 
 int moe_dispatch(moe_ctx* ctx, int T, int k, int E, int H, int x_dtype, int capacity,
@@ -486,7 +594,7 @@ int moe_grouped_swiglu(moe_ctx* ctx, const moe_expert_desc* d, const void* X,
 int moe_combine(moe_ctx* ctx, int T, int k, int H, const float* O, const float* O_shared,
                 const int32_t* row_of_slot, const float* topk_gate, float* Y, void* Y_bf16,
                 moe_stream_t stream) {
-  if (T < 0 || k < 1 || k > kMaxK) return fail(MOE_ERR_INVALID_ARG, "T = %d, k = %d", T, k);
+  if (T < 0 || k < 1 || k > kMaxE) return fail(MOE_ERR_INVALID_ARG, "T = %d, k = %d", T, k);
   if (H < 4 || H % 4) return fail(MOE_ERR_UNSUPPORTED, "combine needs H %% 4 == 0");
   if (T > 0 && (!O || !row_of_slot || !topk_gate || !Y))
     return fail(MOE_ERR_INVALID_ARG, "O, row_of_slot, topk_gate and Y are required");

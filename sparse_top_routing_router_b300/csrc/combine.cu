@@ -26,22 +26,37 @@ namespace {
 
 __global__ void __launch_bounds__(256) combine_kernel(CombineArgs a) {
   const int t = blockIdx.x;
-  __shared__ int s_row[kMaxK];
-  __shared__ float s_g[kMaxK];
-  if (threadIdx.x < a.k) {
-    s_row[threadIdx.x] = a.row_of_slot[(size_t)t * a.k + threadIdx.x];
-    s_g[threadIdx.x] = a.gate[(size_t)t * a.k + threadIdx.x];
+  // the token's live slots (row >= 0) in ascending slot order: k is at most kMaxK for
+  // token-choice routing and E for expert-choice routing, where most slots are empty
+  __shared__ int s_row[kMaxE];
+  __shared__ float s_g[kMaxE];
+  __shared__ int s_n;
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    int n = 0;
+    for (int base = 0; base < a.k; base += 32) {
+      const int j = base + lane;
+      const int r = j < a.k ? a.row_of_slot[(size_t)t * a.k + j] : -1;
+      const uint32_t live = __ballot_sync(0xffffffffu, r >= 0);
+      if (r >= 0) {
+        const int pos = n + __popc(live & ((1u << lane) - 1u));
+        s_row[pos] = r;
+        s_g[pos] = a.gate[(size_t)t * a.k + j];
+      }
+      n += __popc(live);
+    }
+    if (lane == 0) s_n = n;
   }
   __syncthreads();
+  const int nlive = s_n;
   const int nv = a.H / 4;
   const int per = (nv + gridDim.y - 1) / gridDim.y;   // column chunk of this CTA
   const int v0 = blockIdx.y * per, v1 = min(nv, v0 + per);
   float4* Y = reinterpret_cast<float4*>(a.Y + (size_t)t * a.H);
   for (int v = v0 + threadIdx.x; v < v1; v += blockDim.x) {
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int j = 0; j < a.k; ++j) {
+    for (int j = 0; j < nlive; ++j) {
       const int r = s_row[j];
-      if (r < 0) continue;
       const float g = s_g[j];
       const float4 o = reinterpret_cast<const float4*>(a.O + (size_t)r * a.H)[v];
       acc.x = fmaf(g, o.x, acc.x);

@@ -150,7 +150,38 @@ __global__ void __launch_bounds__(256) dispatch_gather_kernel(DispatchArgs a,
   }
 }
 
+// Warp per permuted row: Xperm[r] = X[slot_of_row[r] / k] (expert-choice routing, where
+// a token may fill any number of rows).  A slot outside [0, T*k) is reported and its
+// row left untouched.
+__global__ void __launch_bounds__(256) gather_rows_kernel(int R, int k, int T, int row_bytes,
+                                                          const int32_t* slot_of_row,
+                                                          const void* X, void* Xperm,
+                                                          int* status) {
+  const int lane = threadIdx.x & 31;
+  const int r = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (r >= R) return;
+  const int slot = slot_of_row[r];
+  if (slot < 0 || (long long)slot >= (long long)T * k) {
+    if (lane == 0) set_status(status, MOE_ERR_DEVICE_INDEX);
+    return;
+  }
+  const int t = slot / k;
+  const uint4* src = reinterpret_cast<const uint4*>(static_cast<const char*>(X) +
+                                                    (size_t)t * row_bytes);
+  uint4* dst = reinterpret_cast<uint4*>(static_cast<char*>(Xperm) + (size_t)r * row_bytes);
+  for (int v = lane; v < row_bytes / 16; v += 32) dst[v] = src[v];
+}
+
 }  // namespace
+
+cudaError_t launch_gather_rows(int R, int k, int row_bytes, const int32_t* slot_of_row,
+                               const void* X, void* Xperm, int* status, int T,
+                               cudaStream_t s) {
+  if (R <= 0) return cudaSuccess;
+  gather_rows_kernel<<<(R + 7) / 8, 256, 0, s>>>(R, k, T, row_bytes, slot_of_row, X, Xperm,
+                                                 status);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_dispatch_count(const DispatchArgs& a, cudaStream_t s) {
   const int nchunks = (a.T + kChunk - 1) / kChunk;

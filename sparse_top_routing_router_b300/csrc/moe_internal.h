@@ -53,7 +53,11 @@ inline int router_splits(int T, int H) {          // CUDA-core logits
 //   dispatch chunk table  2 * nchunks * E int32
 //   expert activations h  (T*k + T) * I elements (bf16, or fp32 for the fp32 path)
 struct WsLayout {
-  size_t logits, refine, wsplit, chunk_counts, chunk_base, h, total;
+  size_t logits, refine, wsplit, chunk_counts, chunk_base, h;
+  // expert-choice routing: affinities by column, exact affinities of listed tokens,
+  // token flags and lists, column list and limits, counters
+  size_t ec_st, ec_exs, ec_need, ec_tok, ec_col, ec_info, ec_ctr;
+  size_t total;
 };
 
 inline WsLayout ws_layout(int T, int H, int E, int I, int k, int dtype, int has_shared) {
@@ -70,7 +74,21 @@ inline WsLayout ws_layout(int T, int H, int E, int I, int k, int dtype, int has_
   off = align_up(off + nchunks * E * 4, 256);
   L.chunk_base = off;
   off = align_up(off + nchunks * E * 4, 256);
-  L.h = off;
+  L.ec_st = off;
+  off = align_up(off + (size_t)T * E * 4, 256);
+  L.ec_exs = off;
+  off = align_up(off + (size_t)T * E * 8, 256);
+  L.ec_need = off;
+  off = align_up(off + (size_t)T * 4, 256);
+  L.ec_tok = off;
+  off = align_up(off + (size_t)T * 4, 256);
+  L.ec_col = off;
+  off = align_up(off + (size_t)E * 4, 256);
+  L.ec_info = off;
+  off = align_up(off + (size_t)E * 16, 256);
+  L.ec_ctr = off;
+  off = align_up(off + 16, 256);
+  L.h = off;   // last: the only region whose size depends on I
   const size_t rows = (size_t)T * k + (has_shared ? (size_t)T : 0);
   off = align_up(off + rows * I * (dtype == MOE_DTYPE_BF16 ? 2 : 4), 256);
   L.total = off;
@@ -113,6 +131,28 @@ cudaError_t launch_router_split(const RouterArgs& a, cudaStream_t s);
 cudaError_t launch_router_tc(const RouterArgs& a, EncodeTiledFnR enc, bool* encode_failed,
                              cudaStream_t s);
 cudaError_t launch_router_select(const RouterArgs& a, cudaStream_t s);
+// sums split-K partial logits into slot 0 (a.splits > 1); returns the args with splits = 1
+cudaError_t launch_router_reduce(RouterArgs& a, cudaStream_t s);
+
+// Expert-choice routing: every expert takes the C tokens of largest affinity.
+constexpr int kEcMaxT = 32768;   // one expert's column of keys sits in shared memory
+struct ExpertChoiceArgs {
+  RouterArgs r;        // logits (reduced), shapes, X, W_g, logit offset, error bound
+  int C;
+  float* St;           // [E][T] fp32 affinities, one column per expert
+  double* exS;         // [T][E] exact affinities of the listed tokens
+  int* need;           // [T] 1 = the token's exact affinities are needed
+  int* tok_list;       // [T] those tokens
+  int* col_list;       // [E] experts whose choice waits for exact affinities
+  int4* col_info;      // [E] (band low, band high, fp32 margin, 0) of those experts
+  int* ctr;            // [0] listed tokens, [1] listed experts, [2] max rel err, [3] max abs err
+  int32_t* offsets;    // [E+1]
+  int32_t* row_of_slot;  // [T*E], slot t*E + e
+  int32_t* slot_of_row;  // [E*C]
+  float* gate;         // [T*E]
+  float* gap;          // [E] nullable
+};
+cudaError_t launch_expert_choice(const ExpertChoiceArgs& a, cudaStream_t s);
 
 struct DispatchArgs {
   int T, k, E, H, x_dtype, capacity;
@@ -131,6 +171,10 @@ cudaError_t launch_dispatch_count(const DispatchArgs& a, cudaStream_t s);
 cudaError_t launch_dispatch_scan(const DispatchArgs& a, cudaStream_t s);
 cudaError_t launch_dispatch_scatter(const DispatchArgs& a, cudaStream_t s);
 cudaError_t launch_dispatch_gather(const DispatchArgs& a, cudaStream_t s);
+// Xperm[r] = X[slot_of_row[r] / k] for r < R (one warp per row)
+cudaError_t launch_gather_rows(int R, int k, int row_bytes, const int32_t* slot_of_row,
+                               const void* X, void* Xperm, int* status, int T,
+                               cudaStream_t s);
 
 struct ExpertArgs {
   int T, H, E, I, k, has_shared, num_sms;

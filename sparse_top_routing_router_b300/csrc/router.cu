@@ -1107,6 +1107,401 @@ __global__ void __launch_bounds__(kRefineThreads) router_refine_kernel(RouterArg
   }
 }
 
+// ------------------------------------------------------------------ expert-choice routing
+// "LLM Internals §14.2" (the two selection paradigms: expert-choice) and "MoE 03:
+// efficiency frontiers" (Expert Choice Routing): every expert takes the C tokens of the
+// batch with the largest affinity S[t, e] - the softmax probability over the experts, or
+// the sigmoid s - with ties to the lower token index.  Exactness as for token choice: a
+// column whose C-th/(C+1)-th margin lies within twice the error bound of its fp32
+// affinities waits for the exact affinities of the tokens in its band.
+
+constexpr int kEcThreads = 1024;
+
+__device__ __forceinline__ uint64_t ordered_key64(double d) {
+  const uint64_t u = (uint64_t)__double_as_longlong(d + 0.0);
+  return (u >> 63) ? ~u : (u | 0x8000000000000000ull);
+}
+__device__ __forceinline__ double key_of64(uint64_t o) {
+  return __longlong_as_double((long long)((o >> 63) ? (o & 0x7fffffffffffffffull) : ~o));
+}
+
+// Exclusive prefix sum of one int per thread over a block of kEcThreads (32 warps).
+__device__ __forceinline__ int block_excl_scan(int v, int* s_w) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) s_w[w] = x;
+  __syncthreads();
+  if (w == 0) {
+    const int y = s_w[lane];
+    int z = y;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int q = __shfl_up_sync(0xffffffffu, z, o);
+      if (lane >= o) z += q;
+    }
+    s_w[lane] = z - y;
+  }
+  __syncthreads();
+  const int res = s_w[w] + x - v;
+  __syncthreads();
+  return res;
+}
+
+// The rank-th largest key (rank >= 1, at most the number of active items) among the
+// items i < n for which get(i, key) is true: most significant byte first, one 256-bin
+// histogram per byte.  Affinities crowd into a few bins (their leading bytes agree), so
+// the lanes of a warp that fall into the same bin add to it once, with their count.
+template <typename K, typename Get>
+__device__ K block_radix_select(int n, int rank, Get get, int* hist, K* s_pre, int* s_rem) {
+  K prefix = 0, mask = 0;
+  int remaining = rank;
+  const int lane = threadIdx.x & 31;
+  for (int shift = (int)sizeof(K) * 8 - 8; shift >= 0; shift -= 8) {
+    for (int i = threadIdx.x; i < 256; i += blockDim.x) hist[i] = 0;
+    __syncthreads();
+    for (int base = 0; base < n; base += blockDim.x) {   // the same trip count for all
+      const int i = base + threadIdx.x;
+      K key = 0;
+      const bool act = i < n && get(i, key) && (key & mask) == prefix;
+      const int digit = act ? (int)((key >> shift) & 255) : -1;
+      const unsigned grp = __match_any_sync(0xffffffffu, digit);
+      if (act && __ffs(grp) - 1 == lane) atomicAdd(&hist[digit], __popc(grp));
+    }
+    __syncthreads();
+    if (threadIdx.x < 32) {
+      // the bin holding the rank-th largest: lane i sums bins 255 - 8i down to 248 - 8i,
+      // a warp scan finds the lane where the count from the top reaches `remaining`,
+      // and that lane walks its eight bins
+      int c8 = 0;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) c8 += hist[255 - 8 * lane - q];
+      int incl = c8;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      const unsigned hit = __ballot_sync(0xffffffffu, incl >= remaining);
+      const int src = hit ? __ffs(hit) - 1 : 31;
+      if (lane == src) {
+        int cum = incl - c8, d = 255 - 8 * lane;
+        for (int q = 0; q < 7; ++q, --d) {
+          if (cum + hist[d] >= remaining) break;
+          cum += hist[d];
+        }
+        *s_pre = prefix | ((K)d << shift);
+        *s_rem = remaining - cum;
+      }
+    }
+    __syncthreads();
+    prefix = *s_pre;
+    remaining = *s_rem;
+    mask |= (K)255 << shift;
+    __syncthreads();
+  }
+  return prefix;
+}
+
+// fp32 affinities of token t (one warp per token), stored by column; the row's error
+// bound |dS| <= abs + rel * S goes into the running maxima.  Softmax: S moves by at most
+// (e^{2 eps} - 1) S when every logit moves by eps, plus the rounding of exp, the row sum
+// and the quotient; sigmoid: by 0.25 eps plus the rounding of exp and the quotient.
+template <int NJ>
+__global__ void __launch_bounds__(256) ec_scores_kernel(ExpertChoiceArgs a) {
+  const RouterArgs& r = a.r;
+  const int lane = threadIdx.x & 31;
+  // a warp past the last token takes the last token again (same values, same stores) so
+  // that every warp reaches the block's barriers
+  const int t = min(blockIdx.x * 8 + (threadIdx.x >> 5), r.T - 1);
+  const bool sigm = r.score == MOE_SCORE_SIGMOID;
+  float l[NJ];
+  float lmax = -INFINITY, amax = 0.f;
+#pragma unroll
+  for (int j = 0; j < NJ; ++j) {
+    const int e = lane + 32 * j;
+    l[j] = -INFINITY;
+    if (e < r.E) {
+      const float2 pz = r.logits[(size_t)t * r.E + e];
+      float hs = pz.x, ls = pz.y;
+      if (r.logit_bias) two_sum(hs, ls, r.logit_bias[e]);
+      l[j] = hs + ls;
+      lmax = fmaxf(lmax, l[j]);
+      amax = fmaxf(amax, fabsf(l[j]));
+    }
+  }
+  lmax = warp_max_f(lmax);
+  amax = warp_max_f(amax);
+  const float eps_l = r.eps_rel * fmaxf(1.f, amax) * sqrtf(fmaxf(1.f, r.H / 1024.f));
+  float S[NJ];
+  float z = 0.f;
+#pragma unroll
+  for (int j = 0; j < NJ; ++j) {
+    S[j] = 0.f;
+    if (lane + 32 * j < r.E)
+      S[j] = sigm ? __fdividef(1.f, 1.f + __expf(-l[j])) : __expf(l[j] - lmax);
+    z += S[j];
+  }
+  if (!sigm) {
+    z = warp_sum_f(z);
+#pragma unroll
+    for (int j = 0; j < NJ; ++j) S[j] = __fdividef(S[j], z);
+  }
+#pragma unroll
+  for (int j = 0; j < NJ; ++j) {
+    const int e = lane + 32 * j;
+    if (e < r.E) a.St[(size_t)e * r.T + t] = S[j] == S[j] ? S[j] : 0.f;
+  }
+  // the block's largest bounds, then one update of the running maxima per block
+  // (non-negative floats order as their bit patterns)
+  __shared__ int s_rel, s_abs;
+  if (threadIdx.x == 0) s_rel = s_abs = 0;
+  __syncthreads();
+  if (lane == 0) {
+    const float rel = sigm ? 0.f : 2.1f * eps_l + ldexpf(1.f, -18);
+    const float ab = sigm ? 0.25f * eps_l + ldexpf(1.f, -20) : ldexpf(1.f, -24);
+    atomicMax(&s_rel, __float_as_int(rel));
+    atomicMax(&s_abs, __float_as_int(ab));
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    atomicMax(&a.ctr[2], s_rel);
+    atomicMax(&a.ctr[3], s_abs);
+  }
+}
+
+struct EcShared {
+  int hist[256];
+  int w[32];
+  int cnt[3];
+  unsigned long long mx;
+  uint64_t pre;
+  int rem;
+};
+
+// Writes expert e's column from the membership flags s_in[t]: its rows e*C + i hold its
+// tokens in ascending order.
+__device__ void ec_write_column(const ExpertChoiceArgs& a, int e, const uint8_t* s_in,
+                                const uint32_t* s_key, EcShared& sh) {
+  const int T = a.r.T, E = a.r.E, C = a.C;
+  const int per = (T + kEcThreads - 1) / kEcThreads;
+  const int t0 = threadIdx.x * per, t1 = min(T, t0 + per);
+  int c = 0;
+  for (int t = t0; t < t1; ++t) c += s_in[t];
+  int pos = block_excl_scan(c, sh.w);
+  for (int t = t0; t < t1; ++t) {
+    if (!s_in[t]) continue;
+    if (pos >= C) break;   // cannot happen: exactly C members
+    const int row = e * C + pos++;
+    const int slot = t * E + e;
+    a.slot_of_row[row] = slot;
+    a.row_of_slot[slot] = row;
+    a.gate[slot] = key_of(s_key[t]);
+  }
+}
+
+// One CTA per expert: the C-th largest fp32 affinity of its column by radix select, the
+// (C+1)-th, and either the column's tokens (margin above twice the error bound) or a
+// listing of the column and of its band tokens for the exact path.
+__global__ void __launch_bounds__(kEcThreads) ec_select_kernel(ExpertChoiceArgs a) {
+  extern __shared__ uint32_t s_key[];
+  uint8_t* s_in = reinterpret_cast<uint8_t*>(s_key + a.r.T);
+  __shared__ EcShared sh;
+  const int e = blockIdx.x, T = a.r.T, C = a.C, tid = threadIdx.x;
+  for (int t = tid; t < T; t += kEcThreads) s_key[t] = ordered_key(a.St[(size_t)e * T + t]);
+  if (tid == 0) {
+    a.offsets[e] = e * C;
+    if (e == 0) a.offsets[a.r.E] = a.r.E * C;
+    sh.cnt[0] = sh.cnt[1] = 0;
+    sh.mx = 0ull;
+  }
+  __syncthreads();
+  if (C == 0 || C >= T) {
+    for (int t = tid; t < T; t += kEcThreads) s_in[t] = C > 0;
+    __syncthreads();
+    if (C > 0) ec_write_column(a, e, s_in, s_key, sh);
+    if (tid == 0 && a.gap) a.gap[e] = INFINITY;
+    return;
+  }
+  __shared__ uint32_t s_pre32;
+  const uint32_t tau = block_radix_select<uint32_t>(
+      T, C, [&](int i, uint32_t& k) { k = s_key[i]; return true; }, sh.hist, &s_pre32,
+      &sh.rem);
+  int gt = 0, eq = 0;
+  uint32_t below = 0u;
+  for (int t = tid; t < T; t += kEcThreads) {
+    const uint32_t k = s_key[t];
+    gt += k > tau;
+    eq += k == tau;
+    if (k < tau) below = max(below, k);
+  }
+  gt = __reduce_add_sync(0xffffffffu, gt);
+  eq = __reduce_add_sync(0xffffffffu, eq);
+  below = __reduce_max_sync(0xffffffffu, below);
+  if ((tid & 31) == 0) {
+    atomicAdd(&sh.cnt[0], gt);
+    atomicAdd(&sh.cnt[1], eq);
+    atomicMax(&sh.mx, (unsigned long long)below);
+  }
+  __syncthreads();
+  gt = sh.cnt[0];
+  eq = sh.cnt[1];
+  const uint32_t next = gt + eq > C ? tau : (uint32_t)sh.mx;   // the (C+1)-th largest
+  const float ftau = key_of(tau), fnext = key_of(next);
+  const float err = __int_as_float(a.ctr[3]) + __int_as_float(a.ctr[2]) * ftau;
+  const float gapf = ftau - fnext;
+  if (!(gapf > 2.f * err)) {
+    // Exactness guard.  With |dS| <= err near the boundary, a token above fnext + 2 err
+    // is in the exact top C and one below ftau - 2 err is not; the band between needs
+    // exact affinities.
+    const float lo = ftau - 2.f * err, hi = fnext + 2.f * err;
+    for (int t = tid; t < T; t += kEcThreads) {
+      const float v = key_of(s_key[t]);
+      if (v >= lo && !(v > hi) && atomicExch(&a.need[t], 1) == 0)
+        a.tok_list[atomicAdd(&a.ctr[0], 1)] = t;
+    }
+    if (tid == 0) {
+      a.col_list[atomicAdd(&a.ctr[1], 1)] = e;
+      // the band limits themselves, so that the fix-up sees the very same band
+      a.col_info[e] = make_int4(__float_as_int(lo), __float_as_int(hi), __float_as_int(gapf), 0);
+    }
+    return;
+  }
+  // members: every key above tau, then the C - gt lowest tokens whose key equals tau
+  const int per = (T + kEcThreads - 1) / kEcThreads;
+  const int t0 = tid * per, t1 = min(T, t0 + per);
+  int ce = 0;
+  for (int t = t0; t < t1; ++t) ce += s_key[t] == tau;
+  int rank = block_excl_scan(ce, sh.w);
+  for (int t = t0; t < t1; ++t) {
+    const uint32_t k = s_key[t];
+    s_in[t] = k > tau || (k == tau && rank++ < C - gt);
+  }
+  __syncthreads();
+  ec_write_column(a, e, s_in, s_key, sh);
+  if (tid == 0 && a.gap) a.gap[e] = gapf;
+}
+
+// One CTA per listed token: exact logits of all its experts, then its exact affinities.
+template <typename TX>
+__global__ void __launch_bounds__(kRefineThreads) ec_exact_rows_kernel(ExpertChoiceArgs a) {
+  __shared__ int s_ce[kMaxE];
+  __shared__ double s_ex[kMaxE];
+  __shared__ float2 s_part[kRefineWarps][kRefineBatch];
+  const int n = a.ctr[0], E = a.r.E;
+  const bool sigm = a.r.score == MOE_SCORE_SIGMOID;
+  for (int c = threadIdx.x; c < E; c += blockDim.x) s_ce[c] = c;
+  __syncthreads();
+  for (int i = blockIdx.x; i < n; i += gridDim.x) {
+    const int t = a.tok_list[i];
+    for (int b0 = 0; b0 < E; b0 += kRefineBatch)
+      exact_logits_cta<TX>(a.r, t, s_ce + b0, min(kRefineBatch, E - b0), s_part, s_ex + b0);
+    if (threadIdx.x == 0) {
+      double* out = a.exS + (size_t)t * E;
+      if (sigm) {
+        for (int c = 0; c < E; ++c) out[c] = 1.0 / (1.0 + exp(-s_ex[c]));
+      } else {
+        double m = -INFINITY, z = 0.0;
+        for (int c = 0; c < E; ++c) m = fmax(m, s_ex[c]);
+        for (int c = 0; c < E; ++c) z += exp(s_ex[c] - m);
+        for (int c = 0; c < E; ++c) out[c] = exp(s_ex[c] - m) / z;
+      }
+    }
+    __syncthreads();
+  }
+}
+
+// One CTA per listed expert: its sure members, then the best of its band tokens by exact
+// affinity (ties to the lower token) up to C.
+__global__ void __launch_bounds__(kEcThreads) ec_fix_kernel(ExpertChoiceArgs a) {
+  extern __shared__ uint32_t s_key[];
+  uint8_t* s_in = reinterpret_cast<uint8_t*>(s_key + a.r.T);
+  __shared__ EcShared sh;
+  const int n = a.ctr[1], T = a.r.T, E = a.r.E, C = a.C, tid = threadIdx.x;
+  for (int i = blockIdx.x; i < n; i += gridDim.x) {
+    const int e = a.col_list[i];
+    const int4 info = a.col_info[e];
+    const float lo = __int_as_float(info.x), hi = __int_as_float(info.y);
+    for (int t = tid; t < T; t += kEcThreads) s_key[t] = ordered_key(a.St[(size_t)e * T + t]);
+    if (tid == 0) {
+      sh.cnt[0] = sh.cnt[1] = sh.cnt[2] = 0;
+      sh.mx = 0ull;
+    }
+    __syncthreads();
+    // 1 = sure member, 2 = band
+    int nsure = 0, nband = 0;
+    for (int t = tid; t < T; t += kEcThreads) {
+      const float v = key_of(s_key[t]);
+      const uint8_t f = v > hi ? 1 : (v >= lo ? 2 : 0);
+      s_in[t] = f;
+      nsure += f == 1;
+      nband += f == 2;
+    }
+    nsure = __reduce_add_sync(0xffffffffu, nsure);
+    nband = __reduce_add_sync(0xffffffffu, nband);
+    if ((tid & 31) == 0) {
+      atomicAdd(&sh.cnt[0], nsure);
+      atomicAdd(&sh.cnt[1], nband);
+    }
+    __syncthreads();
+    const int need = C - sh.cnt[0];
+    const int band_n = sh.cnt[1];
+    auto exkey = [&](int t) { return ordered_key64(a.exS[(size_t)t * E + e]); };
+    uint64_t etau = 0ull;
+    if (need > 0 && need <= band_n)
+      etau = block_radix_select<uint64_t>(
+          T, need,
+          [&](int t, uint64_t& k) {
+            if (s_in[t] != 2) return false;
+            k = exkey(t);
+            return true;
+          },
+          sh.hist, &sh.pre, &sh.rem);
+    int gt = 0;
+    for (int t = tid; t < T; t += kEcThreads)
+      if (s_in[t] == 2 && exkey(t) > etau) ++gt;
+    gt = __reduce_add_sync(0xffffffffu, gt);
+    if ((tid & 31) == 0) atomicAdd(&sh.cnt[2], gt);
+    __syncthreads();
+    const int take_eq = need - sh.cnt[2];
+    const int per = (T + kEcThreads - 1) / kEcThreads;
+    const int t0 = tid * per, t1 = min(T, t0 + per);
+    int ce = 0;
+    for (int t = t0; t < t1; ++t) ce += s_in[t] == 2 && exkey(t) == etau;
+    int rank = block_excl_scan(ce, sh.w);
+    unsigned long long best_out = 0ull;   // largest exact key of the band left out
+    for (int t = t0; t < t1; ++t) {
+      const uint8_t f = s_in[t];
+      bool in = f == 1;
+      if (f == 2 && need > 0) {
+        const uint64_t k = exkey(t);
+        in = k > etau || (k == etau && rank++ < take_eq);
+      }
+      if (f == 2 && !in) best_out = max(best_out, (unsigned long long)exkey(t));
+      s_in[t] = in;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) best_out = max(best_out, __shfl_xor_sync(0xffffffffu, best_out, o));
+    if ((tid & 31) == 0) atomicMax(&sh.mx, best_out);
+    __syncthreads();
+    ec_write_column(a, e, s_in, s_key, sh);
+    if (tid == 0 && a.gap)
+      a.gap[e] = (need > 0 && sh.mx) ? (float)(key_of64(etau) - key_of64(sh.mx))
+                                     : __int_as_float(info.z);
+    __syncthreads();   // shared memory is reused by the next listed expert
+  }
+}
+
+template <int NJ>
+cudaError_t launch_ec_scores(const ExpertChoiceArgs& a, cudaStream_t s) {
+  ec_scores_kernel<NJ><<<(a.r.T + 7) / 8, 256, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
 template <typename TX, int NJ, bool GRP>
 cudaError_t launch_select_grp(const RouterArgs& a, cudaStream_t s) {
   // one token per warp up to 2^14 tokens, then more: enough warps to fill the GPU, few
@@ -1165,6 +1560,55 @@ cudaError_t launch_router_logits(const RouterArgs& a, cudaStream_t s) {
 cudaError_t launch_router_split(const RouterArgs& a, cudaStream_t s) {
   const dim3 grid((a.H + 31) / 32, (a.E + 31) / 32);
   router_split_kernel<<<grid, 256, 0, s>>>(a.Wg, a.H, a.E, a.wsplit);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_expert_choice(const ExpertChoiceArgs& a, cudaStream_t s) {
+  const int E = a.r.E;
+  cudaError_t e = E <= 32 ? launch_ec_scores<1>(a, s)
+                  : E <= 64 ? launch_ec_scores<2>(a, s)
+                  : E <= 128 ? launch_ec_scores<4>(a, s)
+                  : E <= 256 ? launch_ec_scores<8>(a, s)
+                             : launch_ec_scores<16>(a, s);
+  if (e != cudaSuccess) return e;
+  const size_t smem = (size_t)a.r.T * 5 + 16;
+  for (const void* fn : {reinterpret_cast<const void*>(ec_select_kernel),
+                         reinterpret_cast<const void*>(ec_fix_kernel)}) {
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  ec_select_kernel<<<E, kEcThreads, smem, s>>>(a);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  // the listed tokens are few; most of these CTAs find nothing to do
+  const int sms = a.r.num_sms > 0 ? a.r.num_sms : 1;
+  const int grid = a.r.T < 2 * sms ? a.r.T : 2 * sms;
+  if (a.r.x_dtype == MOE_DTYPE_BF16)
+    ec_exact_rows_kernel<__nv_bfloat16><<<grid, kRefineThreads, 0, s>>>(a);
+  else
+    ec_exact_rows_kernel<float><<<grid, kRefineThreads, 0, s>>>(a);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  ec_fix_kernel<<<E, kEcThreads, smem, s>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_router_reduce(RouterArgs& a, cudaStream_t s) {
+  if (a.splits <= 1) return cudaSuccess;
+  const size_t n = (size_t)a.T * a.E;
+  const size_t want = (size_t)2 * 2048 * (a.num_sms > 0 ? a.num_sms : 1);
+  int G = 1;
+  while (G < 8 && G < a.splits && n * G < want) G <<= 1;
+  const unsigned blocks = (unsigned)((n * G + 255) / 256);
+  const bool f32 = a.logits_part != nullptr;
+#define MOE_REDUCE(GG)                                                                      \
+  (f32 ? router_reduce_kernel<true, GG><<<blocks, 256, 0, s>>>(a.logits, a.logits_part, n,   \
+                                                                a.splits)                   \
+       : router_reduce_kernel<false, GG><<<blocks, 256, 0, s>>>(a.logits, nullptr, n, a.splits))
+  if (G == 1) MOE_REDUCE(1);
+  else if (G == 2) MOE_REDUCE(2);
+  else if (G == 4) MOE_REDUCE(4);
+  else MOE_REDUCE(8);
+#undef MOE_REDUCE
+  a.splits = 1;
   return cudaGetLastError();
 }
 

@@ -41,12 +41,15 @@ class MoELayer:
         self.ws = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=dev)
         B.moe_workspace_init(self.ws)
         self.idx = torch.empty(T, c.k, dtype=i32, device=dev)
-        self.gate = torch.empty(T, c.k, dtype=f32, device=dev)
+        # expert-choice routing: E slots (token, expert) per token
+        ks = c.E if c.expert_choice else c.k
+        self.gate = torch.empty(T, ks, dtype=f32, device=dev)
+        self.col_gap = torch.empty(c.E, dtype=f32, device=dev) if c.expert_choice else None
         self.gap = torch.empty(T, dtype=f32, device=dev)
         self.colsum = torch.empty(c.E, dtype=torch.float64, device=dev)
         self.counts = torch.empty(c.E, dtype=i32, device=dev)
         self.offsets = torch.empty(c.E + 1, dtype=i32, device=dev)
-        self.row_of_slot = torch.empty(T * c.k, dtype=i32, device=dev)
+        self.row_of_slot = torch.empty(T * ks, dtype=i32, device=dev)
         self.slot_of_row = torch.empty(T * c.k, dtype=i32, device=dev)
         self.Xperm = torch.empty(T * c.k, c.H, dtype=xdt, device=dev)
         self.O = torch.empty(T * c.k, c.H, dtype=f32, device=dev)
@@ -72,6 +75,8 @@ class MoELayer:
         assert X.shape == (self.T, c.H)
         Y = self.Y if Y is None else Y
         stream = torch.cuda.current_stream(self.dev) if stream is None else stream
+        if c.expert_choice:
+            return self._forward_expert_choice(X, Y, Y_bf16, stream)
         B.moe_router_topk(self.ctx, X, w["Wg"], c.k, self.score, c.renorm, self.idx,
                           self.gate, self.ws, bias=w.get("bias"),
                           logit_bias=w.get("logit_bias"), key_gap=self.gap,
@@ -97,6 +102,24 @@ class MoELayer:
             self.update_bias(self.bias_gamma, stream=stream)
         if stats:
             stream.wait_event(self._stats_done)   # the forward ends when both streams do
+        return Y
+
+    def _forward_expert_choice(self, X, Y, Y_bf16, stream) -> torch.Tensor:
+        """Expert-choice routing: every expert takes its C = T*k/E best tokens; the expert
+        stage is unchanged, the combine sums over the E (token, expert) slots."""
+        c, w = self.cfg, self.w
+        B.moe_expert_choice(self.ctx, X, w["Wg"], c.k, self.score, self.offsets,
+                            self.row_of_slot, self.slot_of_row, self.gate, self.ws,
+                            logit_bias=w.get("logit_bias"), col_gap=self.col_gap,
+                            stream=stream)
+        B.moe_gather_rows(self.ctx, self.slot_of_row, c.E, X, self.Xperm, self.ws,
+                          stream=stream)
+        B.moe_grouped_swiglu(self.ctx, X, self.Xperm, self.offsets, w["W_gate"], w["W_up"],
+                             w["W_down"], self.O, self.ws, c.k, Ws_gate=w.get("Ws_gate"),
+                             Ws_up=w.get("Ws_up"), Ws_down=w.get("Ws_down"),
+                             O_shared=self.O_shared, stream=stream)
+        B.moe_combine(self.ctx, self.O, self.row_of_slot, self.gate, Y,
+                      O_shared=self.O_shared, Y_bf16=Y_bf16, stream=stream)
         return Y
 
     def update_bias(self, gamma: float, stream=None) -> None:

@@ -37,7 +37,7 @@ def test_exports_match_header(L):
 
 
 def test_version_and_strings(L):
-    assert L.moe_version() == 10200
+    assert L.moe_version() == 10300
     assert B.status_string(0) == "ok"
     assert B.status_string(-4) == "device wait timed out"
     for i, n in enumerate(B.KERNEL_NAMES):
@@ -66,7 +66,8 @@ def test_workspace_bytes(L):
     logits = 7 * 8192 * 256 * 8          # up to 7 split-K slices of (hi, lo) partial logits
     wsplit = 256 * 3 * 7168 * 2          # W_g as bf16 pieces for the tensor-core router
     refine = 8192 * 16                   # rows listed for exact re-decision
-    assert h + wsplit < ws < h + wsplit + logits + refine + 2 * 32 * 256 * 4 + 4096
+    ec = 8192 * 256 * 12 + 8192 * 8 + 256 * 20   # expert-choice columns and exact rows
+    assert h + wsplit + ec < ws < h + wsplit + ec + logits + refine + 2 * 32 * 256 * 4 + 8192
     assert B.moe_workspace_bytes(-1, 1, 1, 1, 1, 0, 0) == 0
     assert B.moe_workspace_bytes(0, 64, 8, 64, 2, 0, 0) >= 256
 
@@ -121,6 +122,27 @@ def test_validation_before_device(L):
     r = L.moe_bias_update(None, 16, 2, 8, None, 0.001, fake, None)
     assert r == B.MOE_ERR_INVALID_ARG and "required" in B.last_error_detail()
     r = L.moe_bias_update(None, 16, 2, 8, fake, 0.001, fake, None)
+    assert r == B.MOE_ERR_INVALID_ARG and "ctx" in B.last_error_detail()
+    # expert choice: E must divide T*k; at most 32768 tokens; no expert groups
+    d = B.RouterDesc(10, 64, 4, 1, 0, 0, 0)
+    r = L.moe_expert_choice(None, C.byref(d), fake, fake, None, fake, fake, fake, fake, None,
+                            fake, 1 << 30, None)
+    assert r == B.MOE_ERR_INVALID_ARG and "divide" in B.last_error_detail()
+    d = B.RouterDesc(40000, 64, 8, 2, 0, 0, 0)
+    r = L.moe_expert_choice(None, C.byref(d), fake, fake, None, fake, fake, fake, fake, None,
+                            fake, 1 << 30, None)
+    assert r == B.MOE_ERR_UNSUPPORTED and "32768" in B.last_error_detail()
+    d = B.RouterDesc(16, 64, 8, 2, 0, 0, 0, 4, 2)
+    r = L.moe_expert_choice(None, C.byref(d), fake, fake, None, fake, fake, fake, fake, None,
+                            fake, 1 << 30, None)
+    assert r == B.MOE_ERR_UNSUPPORTED and "groups" in B.last_error_detail()
+    d = B.RouterDesc(16, 64, 8, 2, 0, 0, 0)
+    r = L.moe_expert_choice(None, C.byref(d), fake, fake, None, fake, fake, fake, fake, None,
+                            fake, 1 << 30, None)
+    assert r == B.MOE_ERR_INVALID_ARG and "ctx" in B.last_error_detail()
+    r = L.moe_gather_rows(None, 8, 4, 100, 0, fake, fake, 4, fake, fake, None)
+    assert r == B.MOE_ERR_UNSUPPORTED and "16 B" in B.last_error_detail()
+    r = L.moe_gather_rows(None, 8, 4, 64, 0, fake, fake, 4, fake, fake, None)
     assert r == B.MOE_ERR_INVALID_ARG and "ctx" in B.last_error_detail()
     # dispatch: X without Xperm
     r = L.moe_dispatch(None, 16, 2, 8, 64, 0, -1, fake, fake, fake, fake, fake, fake, None,

@@ -251,6 +251,66 @@ def dispatch(idx: np.ndarray, E: int, C: Optional[int] = None) -> Dict[str, np.n
 
 
 # ---------------------------------------------------------------------------
+# FP8 expert weights                        [LI §14.2.5: one expert = 44 MB in FP8]
+# ---------------------------------------------------------------------------
+
+E4M3_MAX = 448.0
+
+
+def e4m3_encode(v: np.ndarray) -> np.ndarray:
+    """FP8 E4M3 codes of float values: 1 sign bit, 4 exponent bits (bias 7) and 3
+    mantissa bits; normals 2^(e-7) * (1 + m/8) for e = 1..15 (e = 15 with m = 7 is NaN,
+    so 448 is the largest finite value), subnormals 2^-6 * m/8.  Round to nearest, ties
+    to even; magnitudes above 448 saturate to 448.  The page states the FP8 size of an
+    expert and no format details: E4M3 is the FP8 format whose range holds weights."""
+    v = np.asarray(v, dtype=f64)
+    neg = np.signbit(v)
+    a = np.abs(v)
+    _, ex = np.frexp(np.where(a > 0, a, 1.0))       # a = f * 2^ex, f in [0.5, 1)
+    E = np.clip(ex - 1, -6, 8)                      # binade; below 2^-6 the subnormal step
+    step = np.ldexp(1.0, E - 3)                     # spacing of E4M3 values in the binade
+    r = np.round(a / step) * step                   # a / step is exact; ties to even
+    r = np.minimum(r, E4M3_MAX)
+    _, rex = np.frexp(np.where(r > 0, r, 1.0))
+    rE = rex - 1
+    normal = r >= 2.0 ** -6
+    e = np.where(normal, rE + 7, 0)
+    m = np.where(normal, r / np.ldexp(1.0, rE) * 8 - 8, r / 2.0 ** -9)
+    code = (neg.astype(np.int64) << 7) | (e.astype(np.int64) << 3) | m.astype(np.int64)
+    return code.astype(np.uint8)
+
+
+def e4m3_decode(code: np.ndarray) -> np.ndarray:
+    """The value of every finite E4M3 code (see e4m3_encode), in float64."""
+    c = np.asarray(code, dtype=np.int64)
+    s = np.where(c & 0x80, -1.0, 1.0)
+    e = (c >> 3) & 0xF
+    m = c & 7
+    return s * np.where(e > 0, np.ldexp(1.0 + m / 8.0, e - 7), m * 2.0 ** -9)
+
+
+def quantize_fp8_rows(W: np.ndarray) -> Tuple[np.ndarray, np.ndarray]:
+    """Per-output-channel FP8 weights: W[..., r, :] ~= scale[..., r] * e4m3(q[..., r, :]).
+
+    The page gives one byte per parameter and no scale convention; this takes one fp32
+    scale per row of the output-major weight (per output channel), scale = amax / 448
+    (1 for an all-zero row), and q = E4M3(w / scale), every step in float32 (division
+    correctly rounded), so that the codes are a deterministic function of the weights.
+    """
+    W32 = np.asarray(W, dtype=np.float32)
+    amax = np.abs(W32).max(axis=-1)
+    scale = np.where(amax > 0, (amax / np.float32(E4M3_MAX)).astype(np.float32),
+                     np.float32(1.0)).astype(np.float32)
+    v = (W32 / scale[..., None]).astype(np.float32)
+    return e4m3_encode(v.astype(f64)), scale
+
+
+def dequantize_fp8_rows(q: np.ndarray, scale: np.ndarray) -> np.ndarray:
+    """scale[r] * value(q[r, :]) in float64 (exact: a 4-bit significand times an fp32)."""
+    return np.asarray(scale, dtype=f64)[..., None] * e4m3_decode(q)
+
+
+# ---------------------------------------------------------------------------
 # Step 5: one SwiGLU expert                                  [LI §14.2.1 step 5, §14.2.2]
 # ---------------------------------------------------------------------------
 

@@ -527,3 +527,50 @@ def test_expert_choice_single_expert_is_dense():
 def test_expert_choice_needs_integer_capacity():
     with pytest.raises(ValueError):
         O.route_expert_choice(np.zeros((5, 2)), np.zeros((2, 2)), 1, "softmax")
+
+
+# ---------------------------------------------------------------- FP8 (E4M3) weights
+
+def test_e4m3_codes_from_the_format():
+    # 1.0 = 2^0: e = 7, m = 0; 448 = 2^8 * 1.75: e = 15, m = 6; 2^-6 smallest normal;
+    # 2^-9 smallest subnormal; -0 keeps its sign
+    v = [1.0, 448.0, 2.0 ** -6, 2.0 ** -9, 7 * 2.0 ** -9, -0.0, -2.5, 0.0]
+    assert O.e4m3_encode(np.array(v)).tolist() == [0x38, 0x7E, 0x08, 0x01, 0x07, 0x80,
+                                                   0xC2, 0x00]
+    # ties to even: 1.0625 lies between 1.0 (m = 0) and 1.125 (m = 1) -> 1.0; 1.1875
+    # between 1.125 and 1.25 (m = 2) -> 1.25; 2^-10 between 0 and 2^-9 -> 0
+    assert O.e4m3_encode(np.array([1.0625, 1.1875, 2.0 ** -10])).tolist() == [0x38, 0x3A, 0]
+    # saturation above the largest finite value
+    assert O.e4m3_encode(np.array([464.0, 1e6, -500.0])).tolist() == [0x7E, 0x7E, 0xFE]
+
+
+def test_e4m3_round_trip_and_library_cast():
+    codes = np.array([c for c in range(256) if (c & 0x7F) != 0x7F], dtype=np.uint8)
+    vals = O.e4m3_decode(codes)
+    back = O.e4m3_encode(vals)
+    assert np.array_equal(back[vals != 0], codes[vals != 0])
+    # in range, the codes equal torch's round-to-nearest-even float8_e4m3fn cast
+    import torch
+    rng = np.random.default_rng(8)
+    x = (rng.standard_normal(4000) * 40).astype(np.float32)
+    x = x[np.abs(x) <= 448]
+    want = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(O.e4m3_encode(x.astype(np.float64)), want)
+
+
+def test_quantize_fp8_rows_scale_and_error():
+    rng = np.random.default_rng(12)
+    W = (rng.standard_normal((6, 300)) * 0.02).astype(np.float32)
+    W[2] = 0.0
+    q, s = O.quantize_fp8_rows(W)
+    assert q.dtype == np.uint8 and s.dtype == np.float32
+    assert s[2] == 1.0 and np.all(q[2] == 0)
+    # the largest magnitude of every non-zero row maps to +-448
+    for r in (0, 1, 3, 4, 5):
+        assert np.abs(O.e4m3_decode(q[r])).max() == 448.0
+    D = O.dequantize_fp8_rows(q, s)
+    # relative error at most half a step: 2^-4 of the magnitude for normals, plus the
+    # subnormal step 2^-9 * scale near zero
+    err = np.abs(D - W)
+    # (plus the rounding of w / scale in float32)
+    assert np.all(err <= np.abs(W) * (2.0 ** -4 + 2.0 ** -20) + s[:, None] * 2.0 ** -10)

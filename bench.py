@@ -68,6 +68,8 @@ def workload_config(cfg: K.MoEConfig, cf) -> dict:
          "capacity_factor": cf, "router": "fp32", "experts": cfg.dtype}
     if cfg.n_groups > 1:
         d["router_groups"] = {"n_groups": cfg.n_groups, "topk_groups": cfg.topk_groups}
+    if cfg.fp8_experts:
+        d["experts"] = "fp8 e4m3, per-output-channel fp32 scales; bf16 activations"
     if cfg.expert_choice:
         d["routing"] = f"expert choice: each expert takes its C = T*k/E = {cfg.T * cfg.k // cfg.E} best tokens"
     return d
@@ -344,11 +346,15 @@ def run_gpu(args, cfg, cf):
     gu_flops = 2.0 * rows * cfg.H * 2 * cfg.I
     dn_flops = 2.0 * rows * cfg.I * cfg.H
     elt = 2 if cfg.dtype == "bf16" else 4
+    welt = 1 if cfg.fp8_experts else elt     # bytes per expert weight
     # experts with at least one kept row (expert-choice routing fills every expert)
     n_touched = int((torch.diff(layer.offsets) > 0).sum().item()) + (1 if cfg.shared else 0)
-    w_touched = n_touched * 3 * cfg.H * cfg.I * elt
+    # FP8 weights carry one fp32 scale per output channel: 2I + H per expert
+    w_scales = 4 * (2 * cfg.I + cfg.H) if cfg.fp8_experts else 0
+    w_touched = n_touched * (3 * cfg.H * cfg.I * welt + w_scales)
     # algorithmic bytes of the gate/up launch: its touched weights once, A rows in, h out
-    gu_bytes = n_touched * 2 * cfg.H * cfg.I * elt + rows * cfg.H * elt + rows * cfg.I * 2
+    gu_bytes = (n_touched * (2 * cfg.H * cfg.I * welt + (8 * cfg.I if cfg.fp8_experts else 0))
+                + rows * cfg.H * elt + rows * cfg.I * 2)
     prof = traffic_from_profile() if cfg.name == K.MIXTRAL.name else None
     # A kernel timed inside a long back-to-back run (>= 0.5 s) is compared with the
     # sustained bf16 peak, a short burst with the burst peak.
@@ -445,6 +451,8 @@ def main():
     ap.add_argument("--bias-update", type=float, default=None, metavar="GAMMA",
                     help="end every forward with the bias update step (selection bias "
                          "-/+ GAMMA for over/underloaded experts)")
+    ap.add_argument("--fp8-experts", action="store_true",
+                    help="expert weights as FP8 E4M3 codes with per-channel scales")
     ap.add_argument("--expert-choice", action="store_true",
                     help="expert-choice routing: every expert takes its C = T*k/E best tokens")
     ap.add_argument("--router-groups", default=None, metavar="G:M",
@@ -457,6 +465,10 @@ def main():
     if args.router_groups:
         G, M = (int(v) for v in args.router_groups.split(":"))
         cfg = dataclasses.replace(cfg, n_groups=G, topk_groups=M)
+    if args.fp8_experts:
+        if cfg.dtype != "bf16":
+            ap.error("--fp8-experts needs a bf16 workload")
+        cfg = dataclasses.replace(cfg, fp8_experts=True)
     if args.expert_choice:
         if args.router_groups or args.capacity_factor is not None or args.bias_update is not None:
             ap.error("--expert-choice takes no groups, capacity factor or bias update")

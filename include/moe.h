@@ -236,6 +236,38 @@ int moe_grouped_swiglu(moe_ctx* ctx, const moe_expert_desc* d, const void* X,
                        const void* Ws_up, const void* Ws_down, float* O, float* O_shared,
                        void* ws, size_t ws_bytes, moe_stream_t stream);
 
+/* FP8 expert weights ("LLM Internals §14.2.5": one expert's three matrices are 44 MB in
+ * FP8, and decode-sized batches read every touched expert's weights for a few rows).
+ * The pages fix one byte per weight and no scale convention; this library stores E4M3
+ * codes (1 sign, 4 exponent bits with bias 7, 3 mantissa bits, largest finite 448)
+ * with one fp32 scale per output channel (row of the output-major weight):
+ *   scale[r] = amax_r / 448 (1 for an all-zero row), q[r][c] = E4M3(W[r][c] / scale[r]),
+ * both divisions correctly rounded in fp32, the code rounded to nearest even and
+ * saturated at 448.  The dequantized weight is scale[r] * value(q[r][c]).
+ *
+ * moe_quantize_fp8: W [rows, cols] (bf16 or fp32, w_dtype; cols even) -> q [rows, cols]
+ * uint8 codes and scale [rows] fp32, all device memory.  For the expert weights call it
+ * on W_gate / W_up as [E*I, H] and W_down as [E*H, I]. */
+int moe_quantize_fp8(moe_ctx* ctx, int rows, int cols, int w_dtype, const void* W,
+                     uint8_t* q, float* scale, moe_stream_t stream);
+
+/* Step 5 with FP8 expert weights: as moe_grouped_swiglu (same X, Xperm, offsets, O,
+ * O_shared, workspace and h rounding), the weights given as codes and scales:
+ *   Q_gate, Q_up [E][I][H], S_gate, S_up [E][I]; Q_down [E][H][I], S_down [E][H];
+ *   Qs_* / Ss_* the shared expert's ([I][H], [I]; [H][I], [H]; nullable without it).
+ * h = SiLU(s_g (x . q_g)) * (s_u (x . q_u)), o = s_d (h . q_d): the codes decode exactly
+ * and every dot product accumulates in fp32 on CUDA cores, a GEMV per weight row for up
+ * to 8 rows of an expert at a time - the form of decode-sized batches (a few rows per
+ * expert), where the step streams the touched weights once.  Needs bf16 activations and
+ * H % 64 == 0, I % 64 == 0. */
+int moe_grouped_swiglu_fp8(moe_ctx* ctx, const moe_expert_desc* d, const void* X,
+                           const void* Xperm, const int32_t* offsets, const uint8_t* Q_gate,
+                           const float* S_gate, const uint8_t* Q_up, const float* S_up,
+                           const uint8_t* Q_down, const float* S_down, const uint8_t* Qs_gate,
+                           const float* Ss_gate, const uint8_t* Qs_up, const float* Ss_up,
+                           const uint8_t* Qs_down, const float* Ss_down, float* O,
+                           float* O_shared, void* ws, size_t ws_bytes, moe_stream_t stream);
+
 /* ------------------------------------------------------------------ step 6 */
 
 /* Y[t] = sum over kept j of topk_gate[t, j] * O[row_of_slot[t*k+j]]  (+ O_shared[t])

@@ -34,7 +34,8 @@ EXPORTS = ["moe_ctx_create", "moe_ctx_destroy", "moe_workspace_bytes", "moe_work
            "moe_capacity", "moe_router_topk", "moe_dispatch", "moe_dispatch_static",
            "moe_grouped_swiglu",
            "moe_combine", "moe_balance_stats", "moe_bias_update", "moe_get_device_status",
-           "moe_expert_choice", "moe_gather_rows",
+           "moe_expert_choice", "moe_gather_rows", "moe_quantize_fp8",
+           "moe_grouped_swiglu_fp8",
            "moe_ctx_set_tracing", "moe_ctx_trace_read", "moe_ctx_set_test_hook",
            "moe_kernel_name",
            "moe_status_string", "moe_last_error_detail", "moe_version"]
@@ -87,6 +88,8 @@ def lib() -> C.CDLL:
     L.moe_expert_choice.argtypes = [vp, C.POINTER(RouterDesc), vp, vp, vp, vp, vp, vp, vp,
                                     vp, vp, sz, vp]
     L.moe_gather_rows.argtypes = [vp, i, i, i, i, vp, vp, i, vp, vp, vp]
+    L.moe_quantize_fp8.argtypes = [vp, i, i, i, vp, vp, vp, vp]
+    L.moe_grouped_swiglu_fp8.argtypes = [vp, C.POINTER(ExpertDesc)] + [vp] * 18 + [sz, vp]
     L.moe_get_device_status.argtypes = [vp, vp, C.POINTER(i), i, vp]
     L.moe_ctx_set_tracing.argtypes = [vp, i]
     L.moe_ctx_set_test_hook.argtypes = [vp, i, i]
@@ -244,6 +247,30 @@ def moe_grouped_swiglu(ctx: Context, X, Xperm, offsets, W_gate, W_up, W_down, O,
     _check("moe_grouped_swiglu", lib().moe_grouped_swiglu(
         ctx.handle, C.byref(d), _p(X), _p(Xperm), _p(offsets), _p(W_gate), _p(W_up),
         _p(W_down), _p(Ws_gate), _p(Ws_up), _p(Ws_down), _p(O), _p(O_shared), _p(ws),
+        ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def moe_quantize_fp8(ctx: Context, W, q, scale, stream=None) -> None:
+    """W [..., cols] -> q (uint8, same shape) and scale [...]: one scale per row."""
+    cols = W.shape[-1]
+    rows = W.numel() // cols
+    _check("moe_quantize_fp8", lib().moe_quantize_fp8(
+        ctx.handle, rows, cols, x_dtype_code(W), _p(W), _p(q), _p(scale), _stream(stream)))
+
+
+def moe_grouped_swiglu_fp8(ctx: Context, X, Xperm, offsets, fp8, O, ws, k: int,
+                           O_shared=None, stream=None) -> None:
+    """fp8: dict of codes and scales Q_gate, S_gate, Q_up, S_up, Q_down, S_down (and
+    Qs_* / Ss_* for a shared expert)."""
+    T, H = X.shape
+    E, I, _ = fp8["Q_gate"].shape
+    has_shared = "Qs_gate" in fp8
+    d = ExpertDesc(T, H, E, I, k, MOE_DTYPE_BF16, int(has_shared))
+    names = ["Q_gate", "S_gate", "Q_up", "S_up", "Q_down", "S_down",
+             "Qs_gate", "Ss_gate", "Qs_up", "Ss_up", "Qs_down", "Ss_down"]
+    _check("moe_grouped_swiglu_fp8", lib().moe_grouped_swiglu_fp8(
+        ctx.handle, C.byref(d), _p(X), _p(Xperm), _p(offsets),
+        *[_p(fp8.get(n)) for n in names], _p(O), _p(O_shared), _p(ws),
         ws.numel() * ws.element_size(), _stream(stream)))
 
 

@@ -33,6 +33,7 @@ class MoEConfig:
     zipf_s: float = 0.0                        # >0: logit offset -s*ln(e+1) per expert
     alpha: float = 0.0                         # balance-loss coefficient
     expert_choice: bool = False                # every expert takes its C = T*k/E best tokens
+    fp8_experts: bool = False                  # expert weights as FP8 E4M3 + channel scales
     n_groups: int = 0                          # group-limited routing: expert groups
     topk_groups: int = 0                       # ... and the groups a token may use
     x_std: float = 1.0

@@ -195,7 +195,7 @@ int router_logits_stage(moe_ctx* ctx, const moe_router_desc* d, const void* X,
 
 extern "C" {
 
-int moe_version(void) { return 10300; }
+int moe_version(void) { return 10400; }
 
 const char* moe_status_string(int s) {
   switch (s) {
@@ -588,6 +588,83 @@ int moe_grouped_swiglu(moe_ctx* ctx, const moe_expert_desc* d, const void* X,
     if ((e = traced(ctx, MOE_K_EXPERT_DOWN, s, [&] { return launch_expert_down_f32(a, s); })))
       return cuda_fail(e, "expert_down launch");
   }
+  return ok();
+}
+
+int moe_quantize_fp8(moe_ctx* ctx, int rows, int cols, int w_dtype, const void* W,
+                     uint8_t* q, float* scale, moe_stream_t stream) {
+  if (rows < 0 || cols < 2 || cols % 2)
+    return fail(MOE_ERR_INVALID_ARG, "rows = %d, cols = %d (cols even and >= 2)", rows, cols);
+  if (w_dtype != MOE_DTYPE_BF16 && w_dtype != MOE_DTYPE_F32)
+    return fail(MOE_ERR_INVALID_ARG, "w_dtype = %d", w_dtype);
+  if (rows > 0 && (!W || !q || !scale))
+    return fail(MOE_ERR_INVALID_ARG, "W, q and scale are required");
+  int r = check_ctx(ctx);
+  if (r) return r;
+  cudaError_t e = launch_quantize_fp8_rows(rows, cols, w_dtype, W, q, scale,
+                                           (cudaStream_t)stream);
+  return e ? cuda_fail(e, "quantize_fp8 launch") : ok();
+}
+
+int moe_grouped_swiglu_fp8(moe_ctx* ctx, const moe_expert_desc* d, const void* X,
+                           const void* Xperm, const int32_t* offsets, const uint8_t* Q_gate,
+                           const float* S_gate, const uint8_t* Q_up, const float* S_up,
+                           const uint8_t* Q_down, const float* S_down, const uint8_t* Qs_gate,
+                           const float* Ss_gate, const uint8_t* Qs_up, const float* Ss_up,
+                           const uint8_t* Qs_down, const float* Ss_down, float* O,
+                           float* O_shared, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  if (!d) return fail(MOE_ERR_INVALID_ARG, "desc is null");
+  int r = check_shape(d->T, d->E, d->k);
+  if (r) return r;
+  if (d->dtype != MOE_DTYPE_BF16)
+    return fail(MOE_ERR_UNSUPPORTED, "FP8 expert weights take bf16 activations");
+  if (d->H < 64 || d->I < 64 || d->H % 64 || d->I % 64)
+    return fail(MOE_ERR_UNSUPPORTED, "FP8 experts need H %% 64 == 0 and I %% 64 == 0");
+  if (d->T > 0 && (!offsets || !Q_gate || !S_gate || !Q_up || !S_up || !Q_down || !S_down ||
+                   !O || !Xperm || !ws))
+    return fail(MOE_ERR_INVALID_ARG, "offsets, codes, scales, Xperm, O and ws are required");
+  if (d->T > 0 && d->has_shared &&
+      (!X || !Qs_gate || !Ss_gate || !Qs_up || !Ss_up || !Qs_down || !Ss_down || !O_shared))
+    return fail(MOE_ERR_INVALID_ARG, "the shared expert needs X, its codes, scales and O_shared");
+  const void* ptrs[] = {X, Xperm, Q_gate, Q_up, Q_down, Qs_gate, Qs_up, Qs_down, O, O_shared, ws};
+  for (const void* q : ptrs)
+    if (!aligned16(q)) return fail(MOE_ERR_INVALID_ARG, "pointers must be 16-byte aligned");
+  const WsLayout L = ws_layout(d->T, d->H, d->E, d->I, d->k, d->dtype, d->has_shared);
+  if (ws_bytes < L.total) return fail(MOE_ERR_INVALID_ARG, "workspace too small");
+  if ((r = check_ctx(ctx))) return r;
+  if (d->T == 0) return ok();
+  cudaStream_t s = (cudaStream_t)stream;
+  Fp8Args a;
+  a.T = d->T;
+  a.H = d->H;
+  a.E = d->E;
+  a.I = d->I;
+  a.k = d->k;
+  a.has_shared = d->has_shared ? 1 : 0;
+  a.X = X;
+  a.Xperm = Xperm;
+  a.offsets = offsets;
+  a.Q_gate = Q_gate;
+  a.Q_up = Q_up;
+  a.Q_down = Q_down;
+  a.S_gate = S_gate;
+  a.S_up = S_up;
+  a.S_down = S_down;
+  a.Qs_gate = Qs_gate;
+  a.Qs_up = Qs_up;
+  a.Qs_down = Qs_down;
+  a.Ss_gate = Ss_gate;
+  a.Ss_up = Ss_up;
+  a.Ss_down = Ss_down;
+  a.h = static_cast<char*>(ws) + L.h;
+  a.O = O;
+  a.O_shared = O_shared;
+  a.status = static_cast<int*>(ws);
+  cudaError_t e;
+  if ((e = traced(ctx, MOE_K_EXPERT_GATE_UP, s, [&] { return launch_expert_gate_up_fp8(a, s); })))
+    return cuda_fail(e, "expert_gate_up (fp8) launch");
+  if ((e = traced(ctx, MOE_K_EXPERT_DOWN, s, [&] { return launch_expert_down_fp8(a, s); })))
+    return cuda_fail(e, "expert_down (fp8) launch");
   return ok();
 }
 

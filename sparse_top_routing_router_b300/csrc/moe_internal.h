@@ -206,6 +206,26 @@ cudaError_t launch_expert_gate_up_tc(const ExpertArgs& a, EncodeTiledFn encode,
                                      bool* encode_failed, cudaStream_t s);
 cudaError_t launch_expert_down_tc(const ExpertArgs& a, EncodeTiledFn encode,
                                   bool* encode_failed, cudaStream_t s);
+// FP8 (E4M3) weights with per-output-channel fp32 scales: CUDA-core GEMVs for
+// decode-sized batches (bf16 activations).
+struct Fp8Args {
+  int T, H, E, I, k, has_shared;
+  const void* X;
+  const void* Xperm;
+  const int32_t* offsets;
+  const uint8_t *Q_gate, *Q_up, *Q_down;      // [E][I][H], [E][I][H], [E][H][I] codes
+  const float *S_gate, *S_up, *S_down;        // [E][I], [E][I], [E][H] scales
+  const uint8_t *Qs_gate, *Qs_up, *Qs_down;   // shared expert
+  const float *Ss_gate, *Ss_up, *Ss_down;
+  void* h;
+  float* O;
+  float* O_shared;
+  int* status;
+};
+cudaError_t launch_quantize_fp8_rows(int rows, int cols, int w_dtype, const void* W,
+                                     uint8_t* q, float* scale, cudaStream_t s);
+cudaError_t launch_expert_gate_up_fp8(const Fp8Args& a, cudaStream_t s);
+cudaError_t launch_expert_down_fp8(const Fp8Args& a, cudaStream_t s);
 // fp32 CUDA-core path.
 cudaError_t launch_expert_gate_up_f32(const ExpertArgs& a, cudaStream_t s);
 cudaError_t launch_expert_down_f32(const ExpertArgs& a, cudaStream_t s);

@@ -32,6 +32,25 @@ class MoELayer:
                          else B.moe_capacity(capacity_factor, cfg.T, cfg.k, cfg.E))
         self.dtype_code = B.MOE_DTYPE_BF16 if cfg.dtype == "bf16" else B.MOE_DTYPE_F32
         self._alloc(cfg.T)
+        self.fp8 = self._quantize_fp8() if cfg.fp8_experts else None
+
+    def _quantize_fp8(self) -> Dict[str, torch.Tensor]:
+        """FP8 E4M3 codes and per-output-channel scales of every expert weight (once)."""
+        q = {}
+        for name in ("gate", "up", "down", "s_gate", "s_up", "s_down"):
+            shared = name.startswith("s_")
+            src = ("Ws_" + name[2:]) if shared else ("W_" + name)
+            if src not in self.w:
+                continue
+            W = self.w[src]
+            codes = torch.empty(W.shape, dtype=torch.uint8, device=self.dev)
+            scale = torch.empty(W.shape[:-1], dtype=torch.float32, device=self.dev)
+            B.moe_quantize_fp8(self.ctx, W, codes, scale)
+            tag = name[2:] if shared else name
+            q[("Qs_" if shared else "Q_") + tag] = codes
+            q[("Ss_" if shared else "S_") + tag] = scale
+        torch.cuda.synchronize(self.dev)
+        return q
 
     def _alloc(self, T: int) -> None:
         c, dev = self.cfg, self.dev
@@ -92,10 +111,7 @@ class MoELayer:
                                 self.f, self.p, self.stats, offsets=self.offsets,
                                 stream=self._side)
             self._stats_done.record(self._side)
-        B.moe_grouped_swiglu(self.ctx, X, self.Xperm, self.offsets, w["W_gate"], w["W_up"],
-                             w["W_down"], self.O, self.ws, c.k, Ws_gate=w.get("Ws_gate"),
-                             Ws_up=w.get("Ws_up"), Ws_down=w.get("Ws_down"),
-                             O_shared=self.O_shared, stream=stream)
+        self._experts(X, stream)
         B.moe_combine(self.ctx, self.O, self.row_of_slot, self.gate, Y,
                       O_shared=self.O_shared, Y_bf16=Y_bf16, stream=stream)
         if self.bias_gamma is not None:
@@ -114,13 +130,22 @@ class MoELayer:
                             stream=stream)
         B.moe_gather_rows(self.ctx, self.slot_of_row, c.E, X, self.Xperm, self.ws,
                           stream=stream)
+        self._experts(X, stream)
+        B.moe_combine(self.ctx, self.O, self.row_of_slot, self.gate, Y,
+                      O_shared=self.O_shared, Y_bf16=Y_bf16, stream=stream)
+        return Y
+
+    def _experts(self, X, stream) -> None:
+        """Step 5: the grouped SwiGLU experts, from bf16/fp32 or FP8 weights."""
+        c, w = self.cfg, self.w
+        if self.fp8 is not None:
+            B.moe_grouped_swiglu_fp8(self.ctx, X, self.Xperm, self.offsets, self.fp8, self.O,
+                                     self.ws, c.k, O_shared=self.O_shared, stream=stream)
+            return
         B.moe_grouped_swiglu(self.ctx, X, self.Xperm, self.offsets, w["W_gate"], w["W_up"],
                              w["W_down"], self.O, self.ws, c.k, Ws_gate=w.get("Ws_gate"),
                              Ws_up=w.get("Ws_up"), Ws_down=w.get("Ws_down"),
                              O_shared=self.O_shared, stream=stream)
-        B.moe_combine(self.ctx, self.O, self.row_of_slot, self.gate, Y,
-                      O_shared=self.O_shared, Y_bf16=Y_bf16, stream=stream)
-        return Y
 
     def update_bias(self, gamma: float, stream=None) -> None:
         """The balancing step after a forward: the selection bias moves by -gamma for

@@ -37,7 +37,7 @@ def test_exports_match_header(L):
 
 
 def test_version_and_strings(L):
-    assert L.moe_version() == 10300
+    assert L.moe_version() == 10400
     assert B.status_string(0) == "ok"
     assert B.status_string(-4) == "device wait timed out"
     for i, n in enumerate(B.KERNEL_NAMES):
@@ -144,6 +144,12 @@ def test_validation_before_device(L):
     assert r == B.MOE_ERR_UNSUPPORTED and "16 B" in B.last_error_detail()
     r = L.moe_gather_rows(None, 8, 4, 64, 0, fake, fake, 4, fake, fake, None)
     assert r == B.MOE_ERR_INVALID_ARG and "ctx" in B.last_error_detail()
+    # FP8 weights: odd column counts, fp32 activations
+    r = L.moe_quantize_fp8(None, 4, 63, 0, fake, fake, fake, None)
+    assert r == B.MOE_ERR_INVALID_ARG and "cols" in B.last_error_detail()
+    e8 = B.ExpertDesc(16, 128, 8, 128, 2, B.MOE_DTYPE_F32, 0)
+    r = L.moe_grouped_swiglu_fp8(None, C.byref(e8), *([fake] * 18), 1 << 30, None)
+    assert r == B.MOE_ERR_UNSUPPORTED and "bf16" in B.last_error_detail()
     # dispatch: X without Xperm
     r = L.moe_dispatch(None, 16, 2, 8, 64, 0, -1, fake, fake, fake, fake, fake, fake, None,
                        fake, 1 << 20, None)

@@ -218,3 +218,63 @@ def test_forward_host_matches_device(ctx):
     s.synchronize()
     assert torch.equal(Y_host, Y_dev.cpu())
     assert layer.device_status() == 0
+
+
+# ---------------------------------------------------------------- the further entry points
+
+@pytest.mark.parametrize("kw", [dict(expert_choice=True), dict(fp8_experts=True),
+                                dict(score="sigmoid", selection_bias_std=0.1, n_groups=4,
+                                     topk_groups=2)],
+                         ids=["expert_choice", "fp8", "groups"])
+def test_empty_batch_other_paths(ctx, kw):
+    cfg = _small(T=0, shared=True, **kw)
+    d = make_inputs(cfg, device="cuda")
+    layer = MoELayer(cfg, d, ctx=ctx)
+    layer.forward(d["X"])
+    torch.cuda.synchronize()
+    assert layer.device_status() == 0
+    assert layer.offsets.tolist() == [0] * (cfg.E + 1)
+
+
+def test_group_limited_single_token_and_whole_groups(ctx):
+    # one token; k = topk_groups * (E / n_groups): every expert of the chosen groups
+    cfg = _small(T=1, E=16, k=8, score="sigmoid", selection_bias_std=0.1, n_groups=4,
+                 topk_groups=2)
+    run = P.run_gpu(cfg, ctx=ctx)
+    assert run.status == 0
+    ref = P.oracle_route(run)
+    assert np.array_equal(P.to_np(run.layer.idx).astype(np.int64), ref["idx"])
+    groups = set((ref["idx"][0] // 4).tolist())
+    assert len(groups) == 2
+
+
+def test_expert_choice_ragged_shapes(ctx):
+    # C = T*k/E = 3 tokens per expert out of 12; E = 8 experts of a 64-wide layer
+    cfg = _small(T=12, k=2, expert_choice=True, shared=True)
+    run = P.run_gpu(cfg, ctx=ctx)
+    assert run.status == 0
+    c, L = run.cfg, run.layer
+    ref = O.route_expert_choice(P.to_np(run.inputs["X"]), P.to_np(run.inputs["Wg"]), c.k,
+                                c.score)
+    sor = P.to_np(L.slot_of_row).astype(np.int64)
+    ok = ref["gap"] >= P.GAP_EXCLUDE
+    assert np.array_equal((sor.reshape(c.E, 3) // c.E)[ok], ref["chosen"][ok])
+
+
+def test_fp8_many_rows_per_expert(ctx):
+    # 40 tokens, top-2 of 2 experts: 40 rows per expert, five 8-row passes each
+    cfg = _small(T=40, E=2, k=2, fp8_experts=True, shared=True)
+    run = P.run_gpu(cfg, ctx=ctx)
+    assert run.status == 0
+    d, L = run.inputs, run.layer
+    ref = P.oracle_route(run)
+
+    def fetch(e):
+        return tuple(O.dequantize_fp8_rows(*O.quantize_fp8_rows(
+            P.to_np(d[n][e]).astype(np.float32))) for n in ("W_gate", "W_up", "W_down"))
+    shared = tuple(O.dequantize_fp8_rows(*O.quantize_fp8_rows(
+        P.to_np(d[n]).astype(np.float32))) for n in ("Ws_gate", "Ws_up", "Ws_down"))
+    Yref = O.combine_subset(P.to_np(d["X"]), ref, fetch, np.arange(cfg.T), shared)
+    Y = P.to_np(L.Y)
+    rms = float(np.sqrt(np.mean(Yref ** 2)))
+    assert float(np.abs(Y - Yref).max()) <= P.Y_TOL["bf16"] * rms

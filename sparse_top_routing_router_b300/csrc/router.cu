@@ -842,7 +842,7 @@ __device__ __forceinline__ void take_exact(uint32_t m, int lane, const double* s
 //     exact score.  The M best candidates by exact score are the groups used.
 //  2. Experts.  Among the experts of those groups, the band of the fp32 keys
 //     [kth - 2 eps, k1th + 2 eps] as in the plain re-decision: experts above it are sure
-//     members, the band is ranked on exact keys (computed now unless round 1 did).
+//     members, the band is ranked on exact keys (computed now unless step 1 did).
 // approx_gap: the fp32 group margin, reported when no other candidate group is left to
 // measure the exact margin against.
 template <typename TX, int NJ>

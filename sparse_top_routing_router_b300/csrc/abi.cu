@@ -283,7 +283,10 @@ int moe_capacity(double c, int T, int k, int E) {
   u128 num = (u128)mant * (u128)(unsigned)T * (u128)(unsigned)k;
   u128 q;
   if (ex >= 0) {
-    if (ex > 30) return fail(MOE_ERR_INVALID_ARG, "capacity overflows");
+    // q = num * 2^ex.  E < 2^31, so any q >= 2^64 makes C > INT32_MAX: reject it before
+    // the shift, which could otherwise wrap past 2^128 to a small (wrong) capacity.
+    if (ex > 30 || (num >> (64 - ex)) != 0)
+      return fail(MOE_ERR_INVALID_ARG, "capacity overflows");
     q = num << ex;
   } else {
     const int s = -ex;

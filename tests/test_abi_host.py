@@ -55,7 +55,9 @@ def test_capacity_matches_oracle(L, c, T, k, E):
 
 def test_capacity_rejects(L):
     for bad in [(-1.0, 4, 1, 2), (math.inf, 4, 1, 2), (math.nan, 4, 1, 2), (1.0, -1, 1, 2),
-                (1.0, 4, 0, 2), (1.0, 4, 1, 0), (1e30, 4, 1, 1)]:
+                (1.0, 4, 0, 2), (1.0, 4, 1, 0), (1e30, 4, 1, 1),
+                # c * T * k = 2^128 exactly: must not wrap to a capacity of 0
+                (2.0 ** 82, 2 ** 23, 2 ** 23, 1), (2.0 ** 60, 2 ** 31 - 1, 2 ** 31 - 1, 2 ** 30)]:
         with pytest.raises(B.MoEError):
             B.moe_capacity(*bad)
 
@@ -174,3 +176,11 @@ def test_validation_before_device(L):
 def test_test_hook_validation(L):
     assert L.moe_ctx_set_test_hook(None, 1, 10) == B.MOE_ERR_INVALID_ARG
     assert L.moe_ctx_set_tracing(None, 1) == B.MOE_ERR_INVALID_ARG
+
+
+def test_capacity_huge_factor_exact(L):
+    # factors of 2^52 and above (an integer mantissa shifted left) still evaluate exactly
+    assert B.moe_capacity(2.0 ** 52, 1, 1, 2 ** 30) == 2 ** 22
+    assert B.moe_capacity(2.0 ** 60, 1, 1, 2 ** 30 + 1) == -(-(2 ** 60) // (2 ** 30 + 1))
+    assert B.moe_capacity(3.0 * 2.0 ** 55, 5, 1, 2 ** 31 - 1) == \
+        -(-(15 * 2 ** 55) // (2 ** 31 - 1))

@@ -1,0 +1,102 @@
+"""Host-side logic of bench.py on CPU: the clock samples kept for the timed region and
+the throttle reasons read from them, the source-hash gate on the committed DRAM-traffic
+figure, and the workload description of the JSON line."""
+
+import datetime
+import hashlib
+import json
+import os
+import sys
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+from sparse_top_routing_router_b300 import configs as K  # noqa: E402
+
+
+class _FakeSmi:
+    def __init__(self, text):
+        self.text = text
+
+    def terminate(self):
+        pass
+
+    def communicate(self, timeout=None):
+        return self.text, ""
+
+
+def _row(ts, sm, mx, power, reasons=("Not Active",) * 4):
+    stamp = datetime.datetime.fromtimestamp(ts).strftime("%Y/%m/%d %H:%M:%S.%f")[:-3]
+    return ", ".join([stamp, "0", str(sm), str(mx), str(power), "0x0", *reasons])
+
+
+def test_clock_samples_inside_the_timed_window_only(monkeypatch):
+    t0 = 1_800_000_000.0
+    rows = [
+        _row(t0 - 1.0, 2032, 2032, 200.0),                       # idle, before the region
+        _row(t0 + 0.1, 1200, 2032, 1090.0,
+             ("Not Active", "Not Active", "Not Active", "Active")),
+        _row(t0 + 0.3, 1250, 2032, 1095.0),
+        _row(t0 + 0.5, 1300, 2032, 1099.0),
+        _row(t0 + 2.0, 2032, 2032, 210.0,
+             ("Active", "Not Active", "Not Active", "Not Active")),   # after the region
+        "garbage line",
+    ]
+    s = bench.ClockSampler(0)
+    s.proc = _FakeSmi("\n".join(rows) + "\n")
+    s.t0, s.t1 = t0, t0 + 0.6
+    monkeypatch.setattr(bench.time, "sleep", lambda _: None)   # stop() waits for a last sample
+    out = s.stop()
+    assert out["samples"] == 3 and out["samples_total"] == 5
+    assert out["sm_mhz"] == 1250 and out["sm_max_mhz"] == 2032
+    # only reasons seen inside the window: the later hw_slowdown sample is not ours
+    assert out["reasons"] == ["sw_power_cap"]
+    assert abs(out["window_s"] - 0.6) < 1e-6
+
+
+def test_clock_sampler_without_nvidia_smi():
+    s = bench.ClockSampler(0)
+    s.proc = None
+    out = s.stop()
+    assert out["sm_mhz"] is None and out["reasons"] == ["nvidia-smi unavailable"]
+
+
+def test_traffic_figure_only_for_the_profiled_source(tmp_path, monkeypatch):
+    src = tmp_path / "kernel.cu"
+    src.write_bytes(b"// kernel source\n")
+    sha = hashlib.sha256(src.read_bytes()).hexdigest()[:16]
+    prof = tmp_path / "traffic.txt"
+    prof.write_text(json.dumps({"kernel_sha": sha, "dram_bytes_per_launch": 123}))
+    monkeypatch.setattr(bench, "KERNEL_SRC", str(src))
+    monkeypatch.setattr(bench, "PROFILE_TRAFFIC", str(prof))
+    assert bench.traffic_from_profile()["dram_bytes_per_launch"] == 123
+    src.write_bytes(b"// kernel source, changed\n")
+    assert bench.traffic_from_profile() is None
+    monkeypatch.setattr(bench, "PROFILE_TRAFFIC", str(tmp_path / "missing.txt"))
+    assert bench.traffic_from_profile() is None
+
+
+def test_committed_traffic_profile_is_well_formed():
+    with open(bench.PROFILE_TRAFFIC) as fh:
+        j = json.load(fh)
+    assert j["dram_bytes_per_launch"] == j["dram_bytes_read"] + j["dram_bytes_write"]
+    assert len(j["kernel_sha"]) == 16 and "--clock-control none" in j["command"]
+
+
+def test_workload_config_names_the_workload():
+    d = bench.workload_config(K.SWITCH, 1.25)
+    assert d["workload"] == "switch_capacity_bf16" and d["capacity_factor"] == 1.25
+    assert (d["T"], d["H"], d["E"], d["I"], d["k"]) == (16384, 4096, 64, 8192, 1)
+    assert "model" not in d
+    g = bench.workload_config(K.scaled(K.DSV3_PREFILL, n_groups=8, topk_groups=4), None)
+    assert g["router_groups"] == {"n_groups": 8, "topk_groups": 4}
+
+
+def test_peaks_are_read_from_the_measured_file():
+    p = bench.peaks()
+    if os.path.exists(os.path.join(ROOT, "MEASURED_PEAKS.json")):
+        assert p["source"] == "measured" and p["hbm_gbs"] > 1000
+    else:
+        assert p == {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0,
+                     "bf16_tflops_sustained": 1400.0, "source": "fallback"}

@@ -184,3 +184,51 @@ def test_capacity_huge_factor_exact(L):
     assert B.moe_capacity(2.0 ** 60, 1, 1, 2 ** 30 + 1) == -(-(2 ** 60) // (2 ** 30 + 1))
     assert B.moe_capacity(3.0 * 2.0 ** 55, 5, 1, 2 ** 31 - 1) == \
         -(-(15 * 2 ** 55) // (2 ** 31 - 1))
+
+
+C_CLIENT = r"""
+#include <stdio.h>
+#include <string.h>
+#include "moe.h"
+
+int main(void) {
+  /* host-only calls: no device is touched */
+  if (moe_version() != 10400) return 1;
+  if (strcmp(moe_status_string(MOE_ERR_TIMEOUT), "device wait timed out") != 0) return 2;
+  if (moe_capacity(1.0, 6, 2, 4) != 3 || moe_capacity(2.0, 6, 2, 4) != 6) return 3;
+  if (moe_capacity(-1.0, 6, 2, 4) != MOE_ERR_INVALID_ARG) return 4;
+  if (strlen(moe_last_error_detail()) == 0) return 5;
+  if (moe_workspace_bytes(64, 128, 8, 256, 2, MOE_DTYPE_F32, 0) == 0) return 6;
+  if (strcmp(moe_kernel_name(MOE_K_EXPERT_GATE_UP), "expert_gate_up") != 0) return 7;
+  /* argument checks run before any device work */
+  moe_router_desc d;
+  memset(&d, 0, sizeof d);
+  d.T = 4; d.H = 64; d.E = 8; d.k = 9;
+  if (moe_router_topk(NULL, &d, NULL, NULL, NULL, NULL, NULL, NULL, NULL, NULL, NULL, 0,
+                      NULL) != MOE_ERR_UNSUPPORTED) return 8;
+  printf("ok %d\n", moe_capacity(1.25, 16384, 1, 64));
+  return 0;
+}
+"""
+
+
+def test_header_is_plain_c_and_links(L, tmp_path):
+    """include/moe.h compiles as C99 with warnings as errors, and a C program linked
+    against libmoe.so calls its host-only entry points."""
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no C compiler")
+    src = tmp_path / "client.c"
+    src.write_text(C_CLIENT)
+    exe = tmp_path / "client"
+    libdir = os.path.dirname(B.LIB_PATH)
+    r = subprocess.run([gcc, "-std=c99", "-Wall", "-Wextra", "-Werror", "-pedantic",
+                        "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe),
+                        "-L", libdir, "-lmoe", f"-Wl,-rpath,{libdir}"],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
+    assert r.returncode == 0, (r.returncode, r.stderr)
+    assert r.stdout.strip() == "ok 320"

@@ -230,6 +230,30 @@ def oracle_sample(cfg, d, cf, n_tokens: int, seed: int):
     return t_route, t_ffn, int(tokens.size), blas_threads()
 
 
+def cpu_baseline_sample(cfg, d, cf, first_tokens: int, min_seconds: float,
+                        mem_bytes: int = _HOST_CACHE_LIMIT):
+    """The oracle's bounded sample for the cpu_baseline figure: routing of all T tokens,
+    then experts + combine of a seeded token sample that doubles (from first_tokens)
+    until the expert stage alone takes min_seconds, the sample is the whole batch, or the
+    next sample's float64 expert weights could exceed mem_bytes.  A few tokens would
+    time the oracle reading its weights rather than computing: per token it touches k
+    whole experts."""
+    per_expert = 3 * cfg.H * cfg.I * 8
+    slots = cfg.E if cfg.expert_choice else cfg.k
+    n = max(1, min(first_tokens, cfg.T))
+    res = oracle_sample(cfg, d, cf, n, seed=1)
+    while res[1] < min_seconds and res[2] < cfg.T:
+        n = min(2 * n, cfg.T)
+        touched = min(cfg.E, n * slots) + (1 if cfg.shared else 0)
+        if touched * per_expert > mem_bytes:
+            break
+        try:
+            res = oracle_sample(cfg, d, cf, n, seed=1)
+        except MemoryError:
+            break            # keep the last sample that fitted
+    return res
+
+
 def run_reference(args, cfg, cf):
     rank, world, _ = dist_env()
     if rank != 0:
@@ -426,12 +450,17 @@ def run_gpu(args, cfg, cf):
         "clocks": clk,
     }
     if world == 1 and not args.no_cpu_baseline:
-        tr, tf, n, threads = oracle_sample(cfg, d, cf, args.cpu_tokens, seed=1)
+        tr, tf, n, threads = cpu_baseline_sample(cfg, d, cf, args.cpu_tokens,
+                                                 args.cpu_seconds)
         v = cfg.T / (tr + tf * cfg.T / n)
         line["cpu_baseline"] = {
             "value": v, "unit": "tokens/s", "cores": threads, "kind": "oracle",
             "sample": f"fp64 oracle: routing of all {cfg.T} tokens ({tr:.2f} s) + experts and "
-                      f"combine of {n} seeded tokens ({tf:.2f} s), extrapolated to {cfg.T} tokens"}
+                      + (f"combine of all {cfg.T} tokens ({tf:.2f} s)" if n >= cfg.T else
+                         f"combine of {n} seeded tokens ({tf:.2f} s), extrapolated to "
+                         f"{cfg.T} tokens")
+                      + f"; the token sample doubles from {args.cpu_tokens} until the expert "
+                        f"stage takes {args.cpu_seconds:g} s or covers the batch"}
     print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
@@ -445,7 +474,10 @@ def main():
     ap.add_argument("--config", default=DEFAULT_CONFIG, choices=sorted(K.BY_NAME))
     ap.add_argument("--capacity-factor", type=float, default=None)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
-    ap.add_argument("--cpu-tokens", type=int, default=8)
+    ap.add_argument("--cpu-tokens", type=int, default=8,
+                    help="first token sample of the cpu_baseline oracle (it doubles)")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="grow the cpu_baseline sample until its expert stage takes this long")
     ap.add_argument("--ref-tokens", type=int, default=2)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--bias-update", type=float, default=None, metavar="GAMMA",

@@ -100,3 +100,28 @@ def test_peaks_are_read_from_the_measured_file():
     else:
         assert p == {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0,
                      "bf16_tflops_sustained": 1400.0, "source": "fallback"}
+
+
+def test_cpu_baseline_sample_grows_to_the_batch_or_the_memory_cap(monkeypatch):
+    from sparse_top_routing_router_b300.inputs import make_inputs
+    cfg = K.TINY_F32                       # T=64, E=8, k=2
+    d = make_inputs(cfg, device="cpu")
+    sizes = []
+    real = bench.oracle_sample
+
+    def spy(cfg_, d_, cf_, n, seed):
+        sizes.append(n)
+        return real(cfg_, d_, cf_, n, seed)
+    monkeypatch.setattr(bench, "oracle_sample", spy)
+    # a time floor it never reaches: doubles from 5 up to the whole batch
+    tr, tf, n, threads = bench.cpu_baseline_sample(cfg, d, None, 5, min_seconds=1e9)
+    assert sizes == [5, 10, 20, 40, 64] and n == 64 and threads >= 1
+    # a floor the first sample meets: one sample
+    sizes.clear()
+    bench.cpu_baseline_sample(cfg, d, None, 5, min_seconds=0.0)
+    assert sizes == [5]
+    # memory: 3 experts' float64 weights allowed, so 2 tokens (4 slots) are not
+    sizes.clear()
+    per_expert = 3 * cfg.H * cfg.I * 8
+    bench.cpu_baseline_sample(cfg, d, None, 1, min_seconds=1e9, mem_bytes=3 * per_expert)
+    assert sizes == [1]

@@ -254,12 +254,39 @@ def cpu_baseline_sample(cfg, d, cf, first_tokens: int, min_seconds: float,
     return res
 
 
+def reference_sample_tokens(cfg, d, cf, step_budget_s: float,
+                            mem_bytes: int = _HOST_CACHE_LIMIT) -> int:
+    """Tokens per step of the reference arm: the sample doubles from 2 while one step,
+    by the wall clock and with its weight staging, stays within step_budget_s and its
+    float64 expert weights within mem_bytes.  Each size runs twice on seeds of its own
+    and the second run is timed: the first stages the experts a small layer then keeps
+    cached (as the timed steps find them), while a large layer stages fresh experts on
+    both, as its timed steps do."""
+    per_expert = 3 * cfg.H * cfg.I * 8
+    slots = cfg.E if cfg.expert_choice else cfg.k
+    n, seed = min(2, cfg.T), 10_000
+    oracle_sample(cfg, d, cf, n, seed)      # stages the inputs
+    while n < cfg.T:
+        n2 = min(2 * n, cfg.T)
+        if (min(cfg.E, n2 * slots) + (1 if cfg.shared else 0)) * per_expert > mem_bytes:
+            break
+        oracle_sample(cfg, d, cf, n2, seed + 1)
+        t0 = time.perf_counter()
+        oracle_sample(cfg, d, cf, n2, seed + 2)
+        seed += 2
+        if time.perf_counter() - t0 > step_budget_s:
+            break
+        n = n2
+    return n
+
+
 def run_reference(args, cfg, cf):
     rank, world, _ = dist_env()
     if rank != 0:
         return
     d = make_inputs(cfg, device="cpu")
-    n_tok = args.ref_tokens
+    step_budget = args.ref_budget / (args.warmup + args.steps)
+    n_tok = args.ref_tokens or reference_sample_tokens(cfg, d, cf, step_budget)
     times = []
     threads = 1
     for i in range(args.warmup + args.steps):
@@ -269,7 +296,11 @@ def run_reference(args, cfg, cf):
         log(f"reference step {i}: route {tr:.2f}s ffn({n} tok) {tf:.2f}s")
     v = statistics.mean(times)
     sample = (f"routing of all {cfg.T} tokens + experts/combine of {n_tok} seeded tokens "
-              f"per step, throughput extrapolated to {cfg.T} tokens")
+              f"per step, throughput extrapolated to {cfg.T} tokens"
+              + ("" if args.ref_tokens else
+                 f"; {n_tok} = the largest doubling of 2 tokens whose step fits "
+                 f"{step_budget:.2f} s, so the {args.warmup + args.steps} steps take about "
+                 f"{args.ref_budget:g} s"))
     line = {"metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * cfg.T / v,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
@@ -478,7 +509,10 @@ def main():
                     help="first token sample of the cpu_baseline oracle (it doubles)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="grow the cpu_baseline sample until its expert stage takes this long")
-    ap.add_argument("--ref-tokens", type=int, default=2)
+    ap.add_argument("--ref-tokens", type=int, default=0,
+                    help="tokens per reference step (0: the largest that fits --ref-budget)")
+    ap.add_argument("--ref-budget", type=float, default=150.0,
+                    help="seconds the reference arm's warm-up and timed steps may take")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--bias-update", type=float, default=None, metavar="GAMMA",
                     help="end every forward with the bias update step (selection bias "

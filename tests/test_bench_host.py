@@ -125,3 +125,14 @@ def test_cpu_baseline_sample_grows_to_the_batch_or_the_memory_cap(monkeypatch):
     per_expert = 3 * cfg.H * cfg.I * 8
     bench.cpu_baseline_sample(cfg, d, None, 1, min_seconds=1e9, mem_bytes=3 * per_expert)
     assert sizes == [1]
+
+
+def test_reference_sample_fits_the_step_budget():
+    from sparse_top_routing_router_b300.inputs import make_inputs
+    cfg = K.TINY_F32                       # T=64
+    d = make_inputs(cfg, device="cpu")
+    assert bench.reference_sample_tokens(cfg, d, None, step_budget_s=1e9) == 64
+    assert bench.reference_sample_tokens(cfg, d, None, step_budget_s=0.0) == 2
+    per_expert = 3 * cfg.H * cfg.I * 8
+    # 4 tokens (8 slots) would need all 8 experts: capped at 2 tokens by memory
+    assert bench.reference_sample_tokens(cfg, d, None, 1e9, mem_bytes=7 * per_expert) == 2

@@ -123,7 +123,16 @@ def _check(fn: str, s: int) -> None:
 
 
 def _p(t: Optional[torch.Tensor]):
-    return None if t is None else C.c_void_p(t.data_ptr())
+    """Device pointer of a contiguous CUDA tensor (None stays None).  A host tensor or a
+    strided view is refused here: the kernels would read its address as device memory
+    laid out row-major."""
+    if t is None:
+        return None
+    if t.device.type != "cuda":
+        raise TypeError(f"expected a CUDA tensor, got one on {t.device}")
+    if not t.is_contiguous():
+        raise ValueError(f"expected a contiguous tensor, got strides {t.stride()}")
+    return C.c_void_p(t.data_ptr())
 
 
 def _stream(stream) -> C.c_void_p:

@@ -232,3 +232,23 @@ def test_header_is_plain_c_and_links(L, tmp_path):
     r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
     assert r.returncode == 0, (r.returncode, r.stderr)
     assert r.stdout.strip() == "ok 320"
+
+
+def test_binding_refuses_host_and_strided_tensors(L):
+    """A host tensor or a strided view never reaches the library as a device pointer."""
+    import torch
+
+    class _Ctx:
+        handle = None
+    O = torch.zeros(8, 4)
+    ros = torch.zeros(4, dtype=torch.int32)
+    gate = torch.ones(4, 1)
+    with pytest.raises(TypeError, match="CUDA tensor"):
+        B.moe_combine(_Ctx(), O, ros, gate, torch.zeros(4, 4))
+    with pytest.raises(TypeError, match="CUDA tensor"):
+        B.moe_bias_update(_Ctx(), 4, 1, ros, 0.001, torch.zeros(4))
+    if torch.cuda.is_available():
+        strided = torch.zeros(4, 8, device="cuda")[:, ::2]
+        with pytest.raises(ValueError, match="contiguous"):
+            B.moe_combine(_Ctx(), O.cuda(), ros.cuda(), gate.cuda(), strided)
+    assert B._p(None) is None

@@ -135,6 +135,17 @@ def _p(t: Optional[torch.Tensor]):
     return C.c_void_p(t.data_ptr())
 
 
+def _req(t: Optional[torch.Tensor], name: str, dtype: torch.dtype, numel: int) -> None:
+    """`t` (if given) holds `dtype` elements, at least `numel` of them: the library takes
+    its sizes from the shapes passed beside the pointers and cannot check the buffers."""
+    if t is None:
+        return
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
+    if t.numel() < numel:
+        raise ValueError(f"{name}: {t.numel()} elements, the call needs {numel}")
+
+
 def _stream(stream) -> C.c_void_p:
     if stream is None:
         stream = torch.cuda.current_stream()
@@ -206,6 +217,13 @@ def moe_router_topk(ctx: Context, X, Wg, k: int, score: int, renorm: bool, topk_
                     topk_groups: int = 0) -> None:
     T, H = X.shape
     E = Wg.shape[1]
+    _req(Wg, "Wg", torch.float32, H * E)
+    _req(bias, "bias", torch.float32, E)
+    _req(logit_bias, "logit_bias", torch.float32, E)
+    _req(topk_idx, "topk_idx", torch.int32, T * k)
+    _req(topk_gate, "topk_gate", torch.float32, T * k)
+    _req(key_gap, "key_gap", torch.float32, T)
+    _req(prob_colsum, "prob_colsum", torch.float64, E)
     d = RouterDesc(T, H, E, k, score, int(renorm), x_dtype_code(X), n_groups, topk_groups)
     _check("moe_router_topk", lib().moe_router_topk(
         ctx.handle, C.byref(d), _p(X), _p(Wg), _p(bias), _p(logit_bias), _p(topk_idx),
@@ -218,6 +236,13 @@ def moe_expert_choice(ctx: Context, X, Wg, k: int, score: int, offsets, row_of_s
                       stream=None) -> None:
     T, H = X.shape
     E = Wg.shape[1]
+    _req(Wg, "Wg", torch.float32, H * E)
+    _req(logit_bias, "logit_bias", torch.float32, E)
+    _req(offsets, "offsets", torch.int32, E + 1)
+    _req(row_of_slot, "row_of_slot", torch.int32, T * E)
+    _req(slot_of_row, "slot_of_row", torch.int32, T * k)
+    _req(slot_gate, "slot_gate", torch.float32, T * E)
+    _req(col_gap, "col_gap", torch.float32, E)
     d = RouterDesc(T, H, E, k, score, 0, x_dtype_code(X), 0, 0)
     _check("moe_expert_choice", lib().moe_expert_choice(
         ctx.handle, C.byref(d), _p(X), _p(Wg), _p(logit_bias), _p(offsets), _p(row_of_slot),
@@ -228,6 +253,8 @@ def moe_expert_choice(ctx: Context, X, Wg, k: int, score: int, offsets, row_of_s
 def moe_gather_rows(ctx: Context, slot_of_row, k: int, X, Xperm, ws, stream=None) -> None:
     R = slot_of_row.shape[0]
     T, H = X.shape
+    _req(slot_of_row, "slot_of_row", torch.int32, R)
+    _req(Xperm, "Xperm", X.dtype, R * H)
     _check("moe_gather_rows", lib().moe_gather_rows(
         ctx.handle, R, k, H, x_dtype_code(X), _p(slot_of_row), _p(X), T, _p(Xperm), _p(ws),
         _stream(stream)))
@@ -240,6 +267,14 @@ def moe_dispatch(ctx: Context, topk_idx, E: int, capacity: int, counts, offsets,
     if H is None:
         H = X.shape[1] if X is not None else 0
     xd = x_dtype_code(X) if X is not None else MOE_DTYPE_BF16
+    _req(topk_idx, "topk_idx", torch.int32, T * k)
+    _req(counts, "counts", torch.int32, E)
+    _req(offsets, "offsets", torch.int32, E + 1)
+    _req(row_of_slot, "row_of_slot", torch.int32, T * k)
+    _req(slot_of_row, "slot_of_row", torch.int32, T * k)
+    if X is not None:
+        _req(X, "X", X.dtype, T * H)
+        _req(Xperm, "Xperm", X.dtype, T * k * H)
     _check("moe_dispatch", lib().moe_dispatch(
         ctx.handle, T, k, E, H, xd, capacity, _p(topk_idx), _p(X), _p(counts), _p(offsets),
         _p(row_of_slot), _p(slot_of_row), _p(Xperm), _p(ws), ws.numel() * ws.element_size(),
@@ -252,6 +287,15 @@ def moe_grouped_swiglu(ctx: Context, X, Xperm, offsets, W_gate, W_up, W_down, O,
     T, H = X.shape
     E, I, _ = W_gate.shape
     has_shared = Ws_gate is not None
+    dt = X.dtype
+    _req(Xperm, "Xperm", dt, T * k * H)
+    _req(offsets, "offsets", torch.int32, E + 1)
+    for name, w in (("W_gate", W_gate), ("W_up", W_up), ("W_down", W_down)):
+        _req(w, name, dt, E * I * H)
+    for name, w in (("Ws_gate", Ws_gate), ("Ws_up", Ws_up), ("Ws_down", Ws_down)):
+        _req(w, name, dt, I * H)
+    _req(O, "O", torch.float32, T * k * H)
+    _req(O_shared, "O_shared", torch.float32, T * H)
     d = ExpertDesc(T, H, E, I, k, x_dtype_code(X), int(has_shared))
     _check("moe_grouped_swiglu", lib().moe_grouped_swiglu(
         ctx.handle, C.byref(d), _p(X), _p(Xperm), _p(offsets), _p(W_gate), _p(W_up),
@@ -263,6 +307,8 @@ def moe_quantize_fp8(ctx: Context, W, q, scale, stream=None) -> None:
     """W [..., cols] -> q (uint8, same shape) and scale [...]: one scale per row."""
     cols = W.shape[-1]
     rows = W.numel() // cols
+    _req(q, "q", torch.uint8, W.numel())
+    _req(scale, "scale", torch.float32, rows)
     _check("moe_quantize_fp8", lib().moe_quantize_fp8(
         ctx.handle, rows, cols, x_dtype_code(W), _p(W), _p(q), _p(scale), _stream(stream)))
 
@@ -274,6 +320,16 @@ def moe_grouped_swiglu_fp8(ctx: Context, X, Xperm, offsets, fp8, O, ws, k: int,
     T, H = X.shape
     E, I, _ = fp8["Q_gate"].shape
     has_shared = "Qs_gate" in fp8
+    _req(Xperm, "Xperm", X.dtype, T * k * H)
+    _req(offsets, "offsets", torch.int32, E + 1)
+    sizes = {"gate": (I * H, I), "up": (I * H, I), "down": (H * I, H)}
+    for m, (n_codes, n_scales) in sizes.items():
+        _req(fp8.get("Q_" + m), "Q_" + m, torch.uint8, E * n_codes)
+        _req(fp8.get("S_" + m), "S_" + m, torch.float32, E * n_scales)
+        _req(fp8.get("Qs_" + m), "Qs_" + m, torch.uint8, n_codes)
+        _req(fp8.get("Ss_" + m), "Ss_" + m, torch.float32, n_scales)
+    _req(O, "O", torch.float32, T * k * H)
+    _req(O_shared, "O_shared", torch.float32, T * H)
     d = ExpertDesc(T, H, E, I, k, MOE_DTYPE_BF16, int(has_shared))
     names = ["Q_gate", "S_gate", "Q_up", "S_up", "Q_down", "S_down",
              "Qs_gate", "Ss_gate", "Qs_up", "Ss_up", "Qs_down", "Ss_down"]
@@ -287,6 +343,12 @@ def moe_combine(ctx: Context, O, row_of_slot, topk_gate, Y, O_shared=None, Y_bf1
                 stream=None) -> None:
     T, k = topk_gate.shape
     H = Y.shape[1]
+    _req(topk_gate, "topk_gate", torch.float32, T * k)
+    _req(row_of_slot, "row_of_slot", torch.int32, T * k)
+    _req(O, "O", torch.float32, 0)
+    _req(O_shared, "O_shared", torch.float32, T * H)
+    _req(Y, "Y", torch.float32, T * H)
+    _req(Y_bf16, "Y_bf16", torch.bfloat16, T * H)
     _check("moe_combine", lib().moe_combine(
         ctx.handle, T, k, H, _p(O), _p(O_shared), _p(row_of_slot), _p(topk_gate), _p(Y),
         _p(Y_bf16), _stream(stream)))
@@ -295,6 +357,11 @@ def moe_combine(ctx: Context, O, row_of_slot, topk_gate, Y, O_shared=None, Y_bf1
 def moe_balance_stats(ctx: Context, T: int, k: int, counts, prob_colsum, alpha: float, f, p,
                       out, offsets=None, stream=None) -> None:
     E = counts.shape[0]
+    _req(counts, "counts", torch.int32, E)
+    _req(offsets, "offsets", torch.int32, E + 1)
+    _req(prob_colsum, "prob_colsum", torch.float64, E)
+    for name, t, n in (("f", f, E), ("p", p, E), ("out", out, 4)):
+        _req(t, name, torch.float64, n)
     _check("moe_balance_stats", lib().moe_balance_stats(
         ctx.handle, T, k, E, _p(counts), _p(offsets), _p(prob_colsum), float(alpha), _p(f),
         _p(p), _p(out), _stream(stream)))
@@ -303,6 +370,8 @@ def moe_balance_stats(ctx: Context, T: int, k: int, counts, prob_colsum, alpha: 
 def moe_bias_update(ctx: Context, T: int, k: int, counts, gamma: float, bias,
                     stream=None) -> None:
     E = counts.shape[0]
+    _req(counts, "counts", torch.int32, E)
+    _req(bias, "bias", torch.float32, E)
     _check("moe_bias_update", lib().moe_bias_update(
         ctx.handle, T, k, E, _p(counts), float(gamma), _p(bias), _stream(stream)))
 

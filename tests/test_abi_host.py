@@ -252,3 +252,31 @@ def test_binding_refuses_host_and_strided_tensors(L):
         with pytest.raises(ValueError, match="contiguous"):
             B.moe_combine(_Ctx(), O.cuda(), ros.cuda(), gate.cuda(), strided)
     assert B._p(None) is None
+
+
+def test_binding_checks_dtypes_and_sizes(L):
+    """The library sizes every buffer from the shapes passed beside the pointers, so the
+    binding refuses buffers of the wrong element type or too few elements first."""
+    import torch
+
+    class _Ctx:
+        handle = None
+    T, H, E, I, k = 4, 64, 2, 64, 1
+    X = torch.zeros(T, H)                                   # fp32 activations
+    W = torch.zeros(E, I, H, dtype=torch.bfloat16)          # ... with bf16 weights
+    Wd = torch.zeros(E, H, I, dtype=torch.bfloat16)
+    O = torch.zeros(T * k, H)
+    off = torch.zeros(E + 1, dtype=torch.int32)
+    ws = torch.zeros(256, dtype=torch.uint8)
+    with pytest.raises(TypeError, match="W_gate"):
+        B.moe_grouped_swiglu(_Ctx(), X, X.clone(), off, W, W, Wd, O, ws, k)
+    with pytest.raises(ValueError, match="O: 128 elements"):
+        B.moe_grouped_swiglu(_Ctx(), X, X.clone(), off, W.float(), W.float(), Wd.float(),
+                             O[:2], ws, k)
+    idx = torch.zeros(T, k, dtype=torch.int64)              # int64 routing indices
+    cnt = torch.zeros(E, dtype=torch.int32)
+    with pytest.raises(TypeError, match="topk_idx"):
+        B.moe_dispatch(_Ctx(), idx, E, -1, cnt, off, cnt, cnt, ws, H=H)
+    with pytest.raises(TypeError, match="prob_colsum"):
+        B.moe_balance_stats(_Ctx(), T, k, cnt, torch.zeros(E), 0.01, torch.zeros(E),
+                            torch.zeros(E), torch.zeros(4))

@@ -91,7 +91,10 @@ class MoELayer:
         output goes to Y (default: the layer's own buffer), an optional bf16 copy to
         Y_bf16."""
         c, w = self.cfg, self.w
-        assert X.shape == (self.T, c.H)
+        if tuple(X.shape) != (self.T, c.H):
+            raise ValueError(f"X has shape {tuple(X.shape)}, the layer takes {(self.T, c.H)}")
+        if X.dtype != self.Xperm.dtype:
+            raise TypeError(f"X is {X.dtype}, the layer computes in {self.Xperm.dtype}")
         Y = self.Y if Y is None else Y
         stream = torch.cuda.current_stream(self.dev) if stream is None else stream
         if c.expert_choice:

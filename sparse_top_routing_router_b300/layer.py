@@ -19,7 +19,7 @@ from .configs import MoEConfig
 class MoELayer:
     def __init__(self, cfg: MoEConfig, weights: Dict[str, torch.Tensor],
                  ctx: Optional[B.Context] = None, device: int = 0,
-                 capacity_factor: Optional[float] = None, gather: bool = True,
+                 capacity_factor: Optional[float] = None,
                  bias_gamma: Optional[float] = None):
         self.cfg = cfg
         # not None: every forward ends with the bias update step (update_bias)

@@ -106,7 +106,7 @@ def selection_keys(l: np.ndarray, score: str,
 # ---------------------------------------------------------------------------
 
 def select_topk(key: np.ndarray, k: int) -> Tuple[np.ndarray, np.ndarray]:
-    """The k largest keys of each row.
+    """The k largest keys of each row  [LI §14.2.1 step 3; KM step three; SN Case 1].
 
     Returns idx[T, k] (the chosen experts, ascending expert index) and gap[T] =
     key_(k) - key_(k+1), the margin between the k-th and (k+1)-th largest key
@@ -198,9 +198,9 @@ def gates_for(l: np.ndarray, idx: np.ndarray, score: str, renorm: bool) -> np.nd
 
 
 def row_probabilities(l: np.ndarray, score: str) -> np.ndarray:
-    """p[t, e] used by the balance statistics: the softmax row, or for sigmoid scoring
-    the affinities normalised over the row (an extension: the pages define p_i only as
-    "the router's mean probability for expert i")."""
+    """p[t, e] used by the balance statistics  [LI §14.2.3]: the softmax row, or for
+    sigmoid scoring the affinities normalised over the row (an extension: the pages
+    define p_i only as the router's mean probability for expert i)."""
     if score == "softmax":
         return softmax_rows(l)
     s = sigmoid(l)
@@ -306,7 +306,8 @@ def quantize_fp8_rows(W: np.ndarray) -> Tuple[np.ndarray, np.ndarray]:
 
 
 def dequantize_fp8_rows(q: np.ndarray, scale: np.ndarray) -> np.ndarray:
-    """scale[r] * value(q[r, :]) in float64 (exact: a 4-bit significand times an fp32)."""
+    """scale[r] * value(q[r, :]) in float64 (exact: a 4-bit significand times an fp32);
+    the weights an FP8 expert computes with  [LI §14.2.5]."""
     return np.asarray(scale, dtype=f64)[..., None] * e4m3_decode(q)
 
 
@@ -388,8 +389,9 @@ def bias_update(bias: np.ndarray, counts: np.ndarray, T: int, k: int,
 def route(X, Wg, k: int, score: str, renorm: bool, bias=None, logit_bias=None,
           C: Optional[int] = None, n_groups: int = 0,
           topk_groups: int = 0) -> Dict[str, np.ndarray]:
-    """Steps 2-4 on every token (capacity is a property of the whole batch).  With
-    n_groups > 1 the selection is group-limited (group_limited_topk)."""
+    """Steps 2-4 on every token  [LI §14.2.1 steps 2-4; KM capacity] (capacity is a
+    property of the whole batch).  With n_groups > 1 the selection is group-limited
+    (group_limited_topk)."""
     l = router_logits(X, Wg, logit_bias)
     key = selection_keys(l, score, bias)
     if n_groups > 1:
@@ -443,10 +445,11 @@ def expert_choice(S: np.ndarray, C: int) -> Dict[str, np.ndarray]:
 
 
 def route_expert_choice(X, Wg, k: int, score: str, logit_bias=None) -> Dict[str, np.ndarray]:
-    """Scoring and expert-choice selection on every token.  Each expert takes the
-    balanced load C = T*k/E (the average number of experts per token is k), which must
-    be an integer; S is the unbiased affinity (routing_affinity), since a per-expert
-    selection bias would shift a whole column and change no expert's choice."""
+    """Scoring and expert-choice selection on every token  [LI §14.2, the two selection
+    paradigms: expert-choice].  Each expert takes the balanced load C = T*k/E (the
+    average number of experts per token is k), which must be an integer; S is the
+    unbiased affinity (routing_affinity), since a per-expert selection bias would shift
+    a whole column and change no expert's choice."""
     l = router_logits(X, Wg, logit_bias)
     T, E = l.shape
     if (T * k) % E:
@@ -494,7 +497,7 @@ def combine_subset(X, routing: Dict[str, np.ndarray], expert: ExpertFn, tokens,
 def moe_layer(X, Wg, W_gate, W_up, W_down, k: int, score: str, renorm: bool,
               bias=None, logit_bias=None, C: Optional[int] = None,
               shared=None, tokens=None) -> Tuple[np.ndarray, Dict[str, np.ndarray]]:
-    """The full forward on in-memory weights (small workloads)."""
+    """The full forward on in-memory weights (small workloads)  [LI §14.2.1 steps 1-6]."""
     routing = route(X, Wg, k, score, renorm, bias, logit_bias, C)
     if tokens is None:
         tokens = np.arange(np.asarray(X).shape[0])
@@ -508,13 +511,15 @@ def moe_layer(X, Wg, W_gate, W_up, W_down, k: int, score: str, renorm: bool,
 # ---------------------------------------------------------------------------
 
 def expert_params(H: int, I: int) -> int:
-    """One SwiGLU expert is three [H, I] matrices: 3*H*I parameters."""
+    """One SwiGLU expert is three [H, I] matrices: 3*H*I parameters  [LI §14.2.2]."""
     return 3 * H * I
 
 
 def layer_params(H: int, I: int, routed: int, shared: int) -> int:
+    """Parameters of one MoE layer: every routed and shared expert  [LI §14.2.2]."""
     return (routed + shared) * expert_params(H, I)
 
 
 def active_params(H: int, I: int, k: int, shared: int) -> int:
+    """Expert parameters one token uses in a layer: k routed + the shared  [LI §14.2.2]."""
     return (k + shared) * expert_params(H, I)

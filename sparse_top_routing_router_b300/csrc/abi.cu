@@ -11,6 +11,8 @@
 #include <string>
 #include <vector>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "moe_internal.h"
 
 using namespace moe;
@@ -66,6 +68,15 @@ int ok() {
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// An NVTX range named after the entry point around each compute call, so a profiler can
+// group the kernels of one call (host-side only; a no-op unless a tool is attached).
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
 
 cudaEvent_t take_event(moe_ctx* c) {
   if (!c->pool.empty()) {
@@ -302,6 +313,7 @@ int moe_router_topk(moe_ctx* ctx, const moe_router_desc* d, const void* X, const
                     const float* bias, const float* logit_bias, int32_t* topk_idx,
                     float* topk_gate, float* key_gap, double* prob_colsum, void* ws,
                     size_t ws_bytes, moe_stream_t stream) {
+  const NvtxRange nvtx_range(__func__);
   if (!d) return fail(MOE_ERR_INVALID_ARG, "desc is null");
   int r = check_shape(d->T, d->E, d->k);
   if (r) return r;
@@ -362,6 +374,7 @@ int moe_expert_choice(moe_ctx* ctx, const moe_router_desc* d, const void* X, con
                       const float* logit_bias, int32_t* offsets, int32_t* row_of_slot,
                       int32_t* slot_of_row, float* slot_gate, float* col_gap, void* ws,
                       size_t ws_bytes, moe_stream_t stream) {
+  const NvtxRange nvtx_range(__func__);
   if (!d) return fail(MOE_ERR_INVALID_ARG, "desc is null");
   int r = check_shape(d->T, d->E, d->k);
   if (r) return r;
@@ -433,6 +446,7 @@ int moe_expert_choice(moe_ctx* ctx, const moe_router_desc* d, const void* X, con
 
 int moe_gather_rows(moe_ctx* ctx, int R, int k, int H, int x_dtype, const int32_t* slot_of_row,
                     const void* X, int T, void* Xperm, void* ws, moe_stream_t stream) {
+  const NvtxRange nvtx_range(__func__);
   if (R < 0 || k < 1 || k > kMaxE || T < 0)
     return fail(MOE_ERR_INVALID_ARG, "R = %d, k = %d, T = %d", R, k, T);
   if (x_dtype != MOE_DTYPE_BF16 && x_dtype != MOE_DTYPE_F32)
@@ -458,6 +472,7 @@ int moe_dispatch(moe_ctx* ctx, int T, int k, int E, int H, int x_dtype, int capa
                  const int32_t* topk_idx, const void* X, int32_t* counts, int32_t* offsets,
                  int32_t* row_of_slot, int32_t* slot_of_row, void* Xperm, void* ws,
                  size_t ws_bytes, moe_stream_t stream) {
+  const NvtxRange nvtx_range(__func__);
   int r = check_shape(T, E, k);
   if (r) return r;
   if (!counts || !offsets || !ws) return fail(MOE_ERR_INVALID_ARG, "counts/offsets/ws null");
@@ -521,6 +536,7 @@ int moe_grouped_swiglu(moe_ctx* ctx, const moe_expert_desc* d, const void* X,
                        const void* W_up, const void* W_down, const void* Ws_gate,
                        const void* Ws_up, const void* Ws_down, float* O, float* O_shared,
                        void* ws, size_t ws_bytes, moe_stream_t stream) {
+  const NvtxRange nvtx_range(__func__);
   if (!d) return fail(MOE_ERR_INVALID_ARG, "desc is null");
   int r = check_shape(d->T, d->E, d->k);
   if (r) return r;
@@ -596,6 +612,7 @@ int moe_grouped_swiglu(moe_ctx* ctx, const moe_expert_desc* d, const void* X,
 
 int moe_quantize_fp8(moe_ctx* ctx, int rows, int cols, int w_dtype, const void* W,
                      uint8_t* q, float* scale, moe_stream_t stream) {
+  const NvtxRange nvtx_range(__func__);
   if (rows < 0 || cols < 2 || cols % 2)
     return fail(MOE_ERR_INVALID_ARG, "rows = %d, cols = %d (cols even and >= 2)", rows, cols);
   if (w_dtype != MOE_DTYPE_BF16 && w_dtype != MOE_DTYPE_F32)
@@ -616,6 +633,7 @@ int moe_grouped_swiglu_fp8(moe_ctx* ctx, const moe_expert_desc* d, const void* X
                            const float* Ss_gate, const uint8_t* Qs_up, const float* Ss_up,
                            const uint8_t* Qs_down, const float* Ss_down, float* O,
                            float* O_shared, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  const NvtxRange nvtx_range(__func__);
   if (!d) return fail(MOE_ERR_INVALID_ARG, "desc is null");
   int r = check_shape(d->T, d->E, d->k);
   if (r) return r;
@@ -674,6 +692,7 @@ int moe_grouped_swiglu_fp8(moe_ctx* ctx, const moe_expert_desc* d, const void* X
 int moe_combine(moe_ctx* ctx, int T, int k, int H, const float* O, const float* O_shared,
                 const int32_t* row_of_slot, const float* topk_gate, float* Y, void* Y_bf16,
                 moe_stream_t stream) {
+  const NvtxRange nvtx_range(__func__);
   if (T < 0 || k < 1 || k > kMaxE) return fail(MOE_ERR_INVALID_ARG, "T = %d, k = %d", T, k);
   if (H < 4 || H % 4) return fail(MOE_ERR_UNSUPPORTED, "combine needs H %% 4 == 0");
   if (T > 0 && (!O || !row_of_slot || !topk_gate || !Y))
@@ -692,6 +711,7 @@ int moe_combine(moe_ctx* ctx, int T, int k, int H, const float* O, const float* 
 int moe_balance_stats(moe_ctx* ctx, int T, int k, int E, const int32_t* counts,
                       const int32_t* offsets, const double* prob_colsum, double alpha,
                       double* f, double* p, double* out, moe_stream_t stream) {
+  const NvtxRange nvtx_range(__func__);
   int r = check_shape(T, E, k);
   if (r) return r;
   if (!counts || !prob_colsum || !f || !p || !out)
@@ -705,6 +725,7 @@ int moe_balance_stats(moe_ctx* ctx, int T, int k, int E, const int32_t* counts,
 
 int moe_bias_update(moe_ctx* ctx, int T, int k, int E, const int32_t* counts, float gamma,
                     float* bias, moe_stream_t stream) {
+  const NvtxRange nvtx_range(__func__);
   int r = check_shape(T, E, k);
   if (r) return r;
   if (!counts || !bias) return fail(MOE_ERR_INVALID_ARG, "counts and bias are required");

@@ -481,8 +481,16 @@ def run_gpu(args, cfg, cf):
         "clocks": clk,
     }
     if world == 1 and not args.no_cpu_baseline:
-        tr, tf, n, threads = cpu_baseline_sample(cfg, d, cf, args.cpu_tokens,
-                                                 args.cpu_seconds)
+        try:
+            tr, tf, n, threads = cpu_baseline_sample(cfg, d, cf, args.cpu_tokens,
+                                                     args.cpu_seconds)
+        except Exception as exc:          # the GPU figures above still get printed
+            line["cpu_baseline"] = {"value": None, "unit": "tokens/s", "kind": "oracle",
+                                    "error": f"{type(exc).__name__}: {exc}"}
+            print(json.dumps(line), flush=True)
+            if dist is not None:
+                dist.destroy_process_group()
+            return
         v = cfg.T / (tr + tf * cfg.T / n)
         line["cpu_baseline"] = {
             "value": v, "unit": "tokens/s", "cores": threads, "kind": "oracle",

@@ -33,7 +33,7 @@ from sparse_top_routing_router_b300 import configs as K  # noqa: E402
 from sparse_top_routing_router_b300.inputs import make_inputs, token_subset  # noqa: E402
 
 METRIC = "MoE-layer fwd tokens/s on 1 B300; % of bf16 tensor peak / % of HBM roofline"
-DEFAULT_CONFIG = K.MIXTRAL.name
+DEFAULT_CONFIG = K.DSV3_PREFILL.name
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "expert_gate_up_traffic.txt")
 L2_BYTES = 126e6          # B300 L2
 KERNEL_SRC = os.path.join(ROOT, "sparse_top_routing_router_b300", "csrc", "expert_tc.cu")
@@ -73,6 +73,36 @@ def workload_config(cfg: K.MoEConfig, cf) -> dict:
     if cfg.expert_choice:
         d["routing"] = f"expert choice: each expert takes its C = T*k/E = {cfg.T * cfg.k // cfg.E} best tokens"
     return d
+
+
+def l2_note(cfg: K.MoEConfig) -> str:
+    elt = 1 if cfg.fp8_experts else (2 if cfg.dtype == "bf16" else 4)
+    w_all = 3 * (cfg.E + (1 if cfg.shared else 0)) * cfg.H * cfg.I * elt
+    if w_all > L2_BYTES:
+        return (f"inputs larger than L2: the expert weights ({w_all / 1e9:.2f} GB) stream "
+                "from HBM every step (no flush needed)")
+    return (f"inputs fit in L2 ({w_all / 1e6:.1f} MB of weights), no flush: a latency "
+            "figure, not a bandwidth one")
+
+
+def run_config(cfg: K.MoEConfig, cf, world: int) -> dict:
+    """The `config` object of both arms' JSON lines: the workload, the L2 statement and
+    the parallelism."""
+    return dict(workload_config(cfg, cf), l2=l2_note(cfg), parallelism=f"replicas x{world}")
+
+
+def step_quantiles(xs) -> dict:
+    """Median, 10th and 90th percentile (linear interpolation) and mean of per-step times."""
+    v = sorted(xs)
+
+    def q(f):
+        if len(v) == 1:
+            return v[0]
+        pos = f * (len(v) - 1)
+        lo = int(pos)
+        hi = min(lo + 1, len(v) - 1)
+        return v[lo] + (v[hi] - v[lo]) * (pos - lo)
+    return {"median": q(0.5), "p10": q(0.1), "p90": q(0.9), "mean": sum(v) / len(v)}
 
 
 def peaks() -> dict:
@@ -152,18 +182,20 @@ class ClockSampler:
                 "reasons": sorted(reasons)}
 
 
-def traffic_from_profile():
-    """dram bytes per launch of expert_gate_up from the committed ncu summary, if the
-    kernel source has not changed since it was captured."""
+def traffic_from_profile(workload: str):
+    """DRAM bytes per launch of expert_gate_up on `workload` from the committed ncu
+    summary (a JSON list, one entry per workload), if the kernel source has not changed
+    since the counters were taken; else None."""
     if not os.path.exists(PROFILE_TRAFFIC):
         return None
     with open(PROFILE_TRAFFIC) as fh:
         j = json.load(fh)
     with open(KERNEL_SRC, "rb") as fh:
         h = hashlib.sha256(fh.read()).hexdigest()[:16]
-    if j.get("kernel_sha") != h:
-        return None
-    return j
+    for entry in (j if isinstance(j, list) else [j]):
+        if entry.get("workload_name") == workload and entry.get("kernel_sha") == h:
+            return dict(entry, source=f"ncu capture, {os.path.relpath(PROFILE_TRAFFIC, ROOT)}")
+    return None
 
 
 # --------------------------------------------------------------------------- CPU oracle
@@ -188,28 +220,38 @@ _HOST_CACHE_BYTES = [0]
 _HOST_CACHE_LIMIT = 16 << 30
 
 
+def host_cores() -> int:
+    """Host cores this process may run on (nproc)."""
+    return len(os.sched_getaffinity(0))
+
+
+def _host(t):
+    """t as a float64 host array (exact for bf16 and fp32 values), kept for later calls
+    while the cache holds less than 16 GB."""
+    key = (t.data_ptr(), tuple(t.shape), str(t.device))
+    a = _HOST_CACHE.get(key)
+    if a is None:
+        a = t.detach().to("cpu").double().numpy()
+        if _HOST_CACHE_BYTES[0] + a.nbytes <= _HOST_CACHE_LIMIT:
+            _HOST_CACHE[key] = a
+            _HOST_CACHE_BYTES[0] += a.nbytes
+    return a
+
+
 def oracle_sample(cfg, d, cf, n_tokens: int, seed: int):
     """Time the fp64 oracle: routing of all T tokens (capacity is a batch property), then
-    experts + combine for a seeded sample of n_tokens.  Inputs and the sample's expert
-    weights are staged in host memory as float64 (exact for bf16 and fp32 values) before
-    the clock starts, and kept for later samples up to 16 GB, so repeated samples neither
-    repeat the copies nor time the widening."""
+    experts + combine for a seeded sample of n_tokens.  The inputs are staged in host
+    memory as float64 (exact for bf16 and fp32 values) before the clock starts; the expert
+    weights are widened one expert at a time as the oracle asks for them, and the time
+    spent widening is taken off the clock, so the figure is the oracle's arithmetic, not
+    its staging.  Widened weights are kept for later samples up to 16 GB.
+    Returns (t_route, t_ffn, tokens, staging seconds)."""
     from oracle import moe_oracle as O
 
-    def host(t):
-        key = (t.data_ptr(), tuple(t.shape), str(t.device))
-        a = _HOST_CACHE.get(key)
-        if a is None:
-            a = t.detach().to("cpu").double().numpy()
-            if _HOST_CACHE_BYTES[0] + a.nbytes <= _HOST_CACHE_LIMIT:
-                _HOST_CACHE[key] = a
-                _HOST_CACHE_BYTES[0] += a.nbytes
-        return a
-
-    X = host(d["X"])
-    Wg = host(d["Wg"])
-    bias = host(d["bias"]) if "bias" in d else None
-    lb = host(d["logit_bias"]) if "logit_bias" in d else None
+    X = _host(d["X"])
+    Wg = _host(d["Wg"])
+    bias = _host(d["bias"]) if "bias" in d else None
+    lb = _host(d["logit_bias"]) if "logit_bias" in d else None
     C = None if cf is None else O.capacity(cf, cfg.T, cfg.k, cfg.E)
     t0 = time.perf_counter()
     if cfg.expert_choice:
@@ -219,57 +261,46 @@ def oracle_sample(cfg, d, cf, n_tokens: int, seed: int):
                     topk_groups=cfg.topk_groups)
     t_route = time.perf_counter() - t0
     tokens = token_subset(cfg.T, n_tokens, seed).numpy()
-    ks = r["idx"].shape[1]
-    taken = r["row_of_slot"].reshape(cfg.T, ks)[tokens] >= 0
-    need = sorted({int(e) for e in r["idx"][tokens][taken]})
-    W = {e: (host(d["W_gate"][e]), host(d["W_up"][e]), host(d["W_down"][e])) for e in need}
-    shared = (host(d["Ws_gate"]), host(d["Ws_up"]), host(d["Ws_down"])) if cfg.shared else None
+    staging = [0.0]
+
+    def fetch(e):
+        t1 = time.perf_counter()
+        w = (_host(d["W_gate"][e]), _host(d["W_up"][e]), _host(d["W_down"][e]))
+        staging[0] += time.perf_counter() - t1
+        return w
+
+    shared = (_host(d["Ws_gate"]), _host(d["Ws_up"]), _host(d["Ws_down"])) if cfg.shared \
+        else None
     t0 = time.perf_counter()
-    O.combine_subset(X, r, lambda e: W[e], tokens, shared)
-    t_ffn = time.perf_counter() - t0
-    return t_route, t_ffn, int(tokens.size), blas_threads()
+    O.combine_subset(X, r, fetch, tokens, shared)
+    t_ffn = time.perf_counter() - t0 - staging[0]
+    return t_route, t_ffn, int(tokens.size), staging[0]
 
 
-def cpu_baseline_sample(cfg, d, cf, first_tokens: int, min_seconds: float,
-                        mem_bytes: int = _HOST_CACHE_LIMIT):
+def cpu_baseline_sample(cfg, d, cf, first_tokens: int, min_seconds: float):
     """The oracle's bounded sample for the cpu_baseline figure: routing of all T tokens,
-    then experts + combine of a seeded token sample that doubles (from first_tokens)
-    until the expert stage alone takes min_seconds, the sample is the whole batch, or the
-    next sample's float64 expert weights could exceed mem_bytes.  A few tokens would
-    time the oracle reading its weights rather than computing: per token it touches k
-    whole experts."""
-    per_expert = 3 * cfg.H * cfg.I * 8
-    slots = cfg.E if cfg.expert_choice else cfg.k
+    then experts + combine of a seeded token sample that starts at first_tokens and
+    doubles until the expert stage alone takes min_seconds or the sample is the whole
+    batch.  A few tokens would time the oracle reading each touched expert's weights
+    rather than computing with them: per token it touches k whole experts."""
     n = max(1, min(first_tokens, cfg.T))
     res = oracle_sample(cfg, d, cf, n, seed=1)
     while res[1] < min_seconds and res[2] < cfg.T:
         n = min(2 * n, cfg.T)
-        touched = min(cfg.E, n * slots) + (1 if cfg.shared else 0)
-        if touched * per_expert > mem_bytes:
-            break
-        try:
-            res = oracle_sample(cfg, d, cf, n, seed=1)
-        except MemoryError:
-            break            # keep the last sample that fitted
+        res = oracle_sample(cfg, d, cf, n, seed=1)
     return res
 
 
-def reference_sample_tokens(cfg, d, cf, step_budget_s: float,
-                            mem_bytes: int = _HOST_CACHE_LIMIT) -> int:
-    """Tokens per step of the reference arm: the sample doubles from 2 while one step,
-    by the wall clock and with its weight staging, stays within step_budget_s and its
-    float64 expert weights within mem_bytes.  Each size runs twice on seeds of its own
-    and the second run is timed: the first stages the experts a small layer then keeps
-    cached (as the timed steps find them), while a large layer stages fresh experts on
-    both, as its timed steps do."""
-    per_expert = 3 * cfg.H * cfg.I * 8
-    slots = cfg.E if cfg.expert_choice else cfg.k
+def reference_sample_tokens(cfg, d, cf, step_budget_s: float) -> int:
+    """Tokens per step of the reference arm: the sample doubles from 2 while one step, by
+    the wall clock and with its weight staging, stays within step_budget_s.  Each size
+    runs twice on seeds of its own and the second run is timed: the first stages the
+    experts a small layer then keeps cached (as the timed steps find them), while a large
+    layer stages fresh experts on both, as its timed steps do."""
     n, seed = min(2, cfg.T), 10_000
     oracle_sample(cfg, d, cf, n, seed)      # stages the inputs
     while n < cfg.T:
         n2 = min(2 * n, cfg.T)
-        if (min(cfg.E, n2 * slots) + (1 if cfg.shared else 0)) * per_expert > mem_bytes:
-            break
         oracle_sample(cfg, d, cf, n2, seed + 1)
         t0 = time.perf_counter()
         oracle_sample(cfg, d, cf, n2, seed + 2)
@@ -288,26 +319,28 @@ def run_reference(args, cfg, cf):
     step_budget = args.ref_budget / (args.warmup + args.steps)
     n_tok = args.ref_tokens or reference_sample_tokens(cfg, d, cf, step_budget)
     times = []
-    threads = 1
     for i in range(args.warmup + args.steps):
-        tr, tf, n, threads = oracle_sample(cfg, d, cf, n_tok, seed=1 + i)
+        tr, tf, n, _ = oracle_sample(cfg, d, cf, n_tok, seed=1 + i)
         if i >= args.warmup:
-            times.append(cfg.T / (tr + tf * cfg.T / n))
+            times.append(tr + tf * cfg.T / n)      # seconds per step, extrapolated to T
         log(f"reference step {i}: route {tr:.2f}s ffn({n} tok) {tf:.2f}s")
-    v = statistics.mean(times)
+    q = step_quantiles(times)
+    v = cfg.T / q["median"]
     sample = (f"routing of all {cfg.T} tokens + experts/combine of {n_tok} seeded tokens "
-              f"per step, throughput extrapolated to {cfg.T} tokens"
+              f"per step (expert weights widened to float64 outside the clock), throughput "
+              f"extrapolated to {cfg.T} tokens; median of {args.steps} steps"
               + ("" if args.ref_tokens else
                  f"; {n_tok} = the largest doubling of 2 tokens whose step fits "
                  f"{step_budget:.2f} s, so the {args.warmup + args.steps} steps take about "
                  f"{args.ref_budget:g} s"))
     line = {"metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * cfg.T / v,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * q["median"],
+            "step_ms": {k: 1e3 * x for k, x in q.items()},
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f64", "data": "synthetic", "impl": "reference",
-            "config": workload_config(cfg, cf),
-            "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": threads,
-                             "kind": "oracle", "sample": sample},
+            "config": run_config(cfg, cf, world),
+            "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": blas_threads(),
+                             "nproc": host_cores(), "kind": "oracle", "sample": sample},
             "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -350,22 +383,25 @@ def run_gpu(args, cfg, cf):
     time.sleep(0.5)
     barrier()
     torch.cuda.synchronize()
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # one event between consecutive forwards: per-step times, median reported
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
     clocks.mark(True)
-    ev0.record(stream)
-    for _ in range(args.steps):
+    evs[0].record(stream)
+    for i in range(args.steps):
         layer.forward(X)
-    ev1.record(stream)
+        evs[i + 1].record(stream)
     torch.cuda.synchronize()
     clocks.mark(False)
     barrier()
     clk = clocks.stop()
-    ms = ev0.elapsed_time(ev1)
+    ms = evs[0].elapsed_time(evs[-1])
+    q = step_quantiles([evs[i].elapsed_time(evs[i + 1]) for i in range(args.steps)])
     kern = layer.ctx.trace_read()
     layer.ctx.set_tracing(False)
     ms = reduce_max_ms(ms, dist, dev)
-    ms_step = ms / args.steps
-    value = world * cfg.T * args.steps / (ms / 1e3)
+    q = {key: reduce_max_ms(v, dist, dev) for key, v in q.items()}
+    ms_step = q["median"]
+    value = world * cfg.T / (ms_step / 1e3)
 
     # ---- end to end: pinned host X -> device, forward, bf16 Y -> pinned host, the copies
     # of neighbouring steps overlapped with compute (MoELayer.host_pipeline)
@@ -410,33 +446,36 @@ def run_gpu(args, cfg, cf):
     # algorithmic bytes of the gate/up launch: its touched weights once, A rows in, h out
     gu_bytes = (n_touched * (2 * cfg.H * cfg.I * welt + (8 * cfg.I if cfg.fp8_experts else 0))
                 + rows * cfg.H * elt + rows * cfg.I * 2)
-    prof = traffic_from_profile() if cfg.name == K.MIXTRAL.name else None
-    # A kernel timed inside a long back-to-back run (>= 0.5 s) is compared with the
-    # sustained bf16 peak, a short burst with the burst peak.
-    sustained = ms >= 500.0 and pk.get("bf16_tflops_sustained")
-    tpeak = pk["bf16_tflops_sustained"] if sustained else pk["bf16_tflops"]
-    src = "%s (MEASURED_PEAKS.json, %s)" % (pk["source"], "sustained" if sustained else "burst")
+    prof = traffic_from_profile(cfg.name)
+    # The headline fraction is against the burst bf16 peak (a cuBLAS GEMM timed alone);
+    # the fraction of the power-capped sustained peak is given beside it.
+    tpeak = pk["bf16_tflops"]
+    spk = pk.get("bf16_tflops_sustained")
+    src = "%s (MEASURED_PEAKS.json, burst)" % pk["source"]
     tensor_bound = R >= 128 * cfg.E     # rows per expert fill the 128/256-row tiles
     if tensor_bound:
         achieved = gu_flops / (gu_ms / 1e3) / 1e12
         roofline = {"kernel": "expert_gate_up", "bound": "tensor", "achieved": achieved,
                     "peak": tpeak, "unit": "TFLOP/s", "frac": achieved / tpeak,
-                    "frac_of_burst_peak": achieved / pk["bf16_tflops"], "peak_source": src,
-                    "timed_region_ms": ms,
+                    "frac_of_sustained_peak": achieved / spk if spk else None,
+                    "peak_source": src, "timed_region_ms": ms,
                     "traffic": prof["dram_bytes_per_launch"] if prof else None,
-                    "algorithmic_flops_per_launch": gu_flops, "avg_launch_ms": gu_ms}
+                    "traffic_source": prof["source"] if prof else None,
+                    "algorithmic_flops_per_launch": gu_flops,
+                    "algorithmic_bytes_per_launch": gu_bytes, "avg_launch_ms": gu_ms}
     else:
         achieved = gu_bytes / (gu_ms / 1e3) / 1e9
         roofline = {"kernel": "expert_gate_up", "bound": "hbm", "achieved": achieved,
                     "peak": pk["hbm_gbs"], "unit": "GB/s",
                     "frac": achieved / pk["hbm_gbs"],
                     "peak_source": "%s (MEASURED_PEAKS.json, copy)" % pk["source"],
-                    "traffic": None, "algorithmic_bytes_per_launch": gu_bytes,
-                    "avg_launch_ms": gu_ms}
+                    "traffic": prof["dram_bytes_per_launch"] if prof else None,
+                    "traffic_source": prof["source"] if prof else None,
+                    "algorithmic_bytes_per_launch": gu_bytes, "avg_launch_ms": gu_ms}
     gemm_tflops = (gu_flops + dn_flops) / ((gu_ms + dn_ms) / 1e3) / 1e12
     extra = {
-        "expert_gemms": {"tflops": gemm_tflops, "frac_of_bf16_peak": gemm_tflops / tpeak,
-                         "frac_of_burst_peak": gemm_tflops / pk["bf16_tflops"],
+        "expert_gemms": {"tflops": gemm_tflops, "frac_of_burst_peak": gemm_tflops / tpeak,
+                         "frac_of_sustained_peak": gemm_tflops / spk if spk else None,
                          "ms": gu_ms + dn_ms},
         "touched_experts": n_touched,
         "hbm_on_touched_weights": {
@@ -448,27 +487,21 @@ def run_gpu(args, cfg, cf):
     }
     launches = sum(n for n, _ in kern.values())
     layer_flops = cfg.flops(R)
-    w_all = 3 * (cfg.E + (1 if cfg.shared else 0)) * cfg.H * cfg.I * elt
-    if w_all > L2_BYTES:
-        l2_note = (f"inputs larger than L2: the expert weights ({w_all / 1e9:.2f} GB) "
-                   "stream from HBM every step (no flush needed)")
-    else:
-        l2_note = (f"inputs fit in L2 ({w_all / 1e6:.1f} MB of weights), no flush: a "
-                   "latency figure, not a bandwidth one")
     kernels = {k: {"launches": n, "ms_per_step": t / args.steps,
                    "share": t / max(sum(x for _, x in kern.values()), 1e-9)}
                for k, (n, t) in kern.items() if n}
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "step_ms": dict(q, timed_region=ms),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16"
         if cfg.dtype == "bf16" else "f32",
         "data": "synthetic (seeded N(0,1) tokens, N(0,0.02) random-init weights)",
-        "config": dict(workload_config(cfg, cf), l2=l2_note, kept_rows=R,
-                       parallelism=f"replicas x{world}",
+        "config": dict(run_config(cfg, cf, world),
                        **({"bias_update_gamma": args.bias_update}
                           if args.bias_update is not None else {})),
-        "tflops": world * layer_flops * args.steps / (ms / 1e3) / 1e12,
+        "kept_rows": R,
+        "tflops": world * layer_flops / (ms_step / 1e3) / 1e12,
         "roofline": roofline,
         "e2e": {"value": world * cfg.T * args.steps / (ms_e2e / 1e3), "unit": "tokens/s",
                 "h2d_bytes_per_step": X.numel() * X.element_size(),
@@ -482,7 +515,7 @@ def run_gpu(args, cfg, cf):
     }
     if world == 1 and not args.no_cpu_baseline:
         try:
-            tr, tf, n, threads = cpu_baseline_sample(cfg, d, cf, args.cpu_tokens,
+            tr, tf, n, stage_s = cpu_baseline_sample(cfg, d, cf, args.cpu_tokens,
                                                      args.cpu_seconds)
         except Exception as exc:          # the GPU figures above still get printed
             line["cpu_baseline"] = {"value": None, "unit": "tokens/s", "kind": "oracle",
@@ -493,13 +526,16 @@ def run_gpu(args, cfg, cf):
             return
         v = cfg.T / (tr + tf * cfg.T / n)
         line["cpu_baseline"] = {
-            "value": v, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "value": v, "unit": "tokens/s", "cores": blas_threads(), "nproc": host_cores(),
+            "kind": "oracle",
             "sample": f"fp64 oracle: routing of all {cfg.T} tokens ({tr:.2f} s) + experts and "
                       + (f"combine of all {cfg.T} tokens ({tf:.2f} s)" if n >= cfg.T else
                          f"combine of {n} seeded tokens ({tf:.2f} s), extrapolated to "
                          f"{cfg.T} tokens")
-                      + f"; the token sample doubles from {args.cpu_tokens} until the expert "
-                        f"stage takes {args.cpu_seconds:g} s or covers the batch"}
+                      + f"; expert weights widened to float64 one expert at a time outside "
+                        f"the clock ({stage_s:.1f} s); the token sample starts at "
+                        f"{min(args.cpu_tokens, cfg.T)} and doubles until the expert stage "
+                        f"takes {args.cpu_seconds:g} s or covers the batch"}
     print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
@@ -513,7 +549,7 @@ def main():
     ap.add_argument("--config", default=DEFAULT_CONFIG, choices=sorted(K.BY_NAME))
     ap.add_argument("--capacity-factor", type=float, default=None)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
-    ap.add_argument("--cpu-tokens", type=int, default=8,
+    ap.add_argument("--cpu-tokens", type=int, default=512,
                     help="first token sample of the cpu_baseline oracle (it doubles)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="grow the cpu_baseline sample until its expert stage takes this long")
@@ -531,9 +567,20 @@ def main():
                     help="expert-choice routing: every expert takes its C = T*k/E best tokens")
     ap.add_argument("--router-groups", default=None, metavar="G:M",
                     help="group-limited routing: G expert groups, M of them per token")
+    ap.add_argument("--shape", default=None, metavar="T=..,E=..",
+                    help="the workload's recipe at other sizes (T, H, E, I, k), for small "
+                         "profiling cases; such a line is not a bench figure of the workload")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)     # fewer warm-up steps give no valid number
     cfg = K.BY_NAME[args.config]
+    if args.shape:
+        kw = {}
+        for item in args.shape.split(","):
+            key, _, val = item.partition("=")
+            if key not in ("T", "H", "E", "I", "k") or not val.isdigit():
+                ap.error(f"--shape takes T, H, E, I, k as KEY=integer, not {item!r}")
+            kw[key] = int(val)
+        cfg = K.scaled(cfg, name=f"{cfg.name}@{args.shape}", **kw)
     if args.bias_update is not None and cfg.selection_bias_std <= 0:
         ap.error("--bias-update needs a workload with a selection bias (sigmoid scoring)")
     if args.router_groups:

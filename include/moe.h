@@ -190,28 +190,39 @@ int moe_gather_rows(moe_ctx* ctx, int R, int k, int H, int x_dtype,
  *   H          hidden size, >= 1 even without a gather (it sizes the workspace layout)
  *   X, Xperm   nullable pair: when both are given, Xperm[row] = X[slot / k] for every
  *              kept row (x_dtype element type, Xperm has T*k rows)
- * Rows are ordered by (expert ascending, token ascending). */
+ * Rows are ordered by (expert ascending, token ascending).  The k experts of a token must
+ * be distinct (moe_router_topk's always are): an index outside [0, E) or repeated within a
+ * row is recorded in the workspace status word (MOE_ERR_DEVICE_INDEX), and the rows of
+ * that expert are then unspecified (never out of bounds). */
 int moe_dispatch(moe_ctx* ctx, int T, int k, int E, int H, int x_dtype, int capacity,
                  const int32_t* topk_idx, const void* X, int32_t* counts,
                  int32_t* offsets, int32_t* row_of_slot, int32_t* slot_of_row,
                  void* Xperm, void* ws, size_t ws_bytes, moe_stream_t stream);
 
-/* Allocation-free dispatch.  The paper has no counterpart to this call: it exists for
- * callers that cannot call cudaMalloc - code running while a CUDA graph is being captured,
- * or under a runtime that owns all device memory and will not hand out scratch.  It does
- * what moe_dispatch does, with the same arguments minus the context and the workspace:
- * its scratch (the per-chunk count and base tables) is a file-scope static device array
- * of 1 MiB that every GPU which loads the library keeps until the process exits.
+/* Allocation-free dispatch.  The paper has no counterpart to this call.  It is for callers
+ * that may not allocate device memory at the moment they dispatch: an inference engine or
+ * host runtime that owns all device memory and hands out only the buffers it planned, or
+ * a process whose allocator must never grow (cudaMalloc can also synchronise the device,
+ * which a latency-bound decode loop cannot afford).  It does what moe_dispatch does, with
+ * the same arguments minus the context and the workspace: its scratch (the per-chunk count
+ * and base tables) is a file-scope static device array of 1 MiB that every GPU which loads
+ * the library keeps until the process exits.
  *  - T may be at most 65536; larger T returns MOE_ERR_UNSUPPORTED and enqueues nothing.
  *  - It calls no cudaMalloc, cudaFree or other allocating routine.
  *  - The first call on a device looks up the array's device address (once per device,
- *    with that device current); make that first call before any stream capture begins.
+ *    with that device current) and caches it for the life of the process; make that first
+ *    call before any stream capture begins.  The cache is keyed on the CURRENT device:
+ *    `stream` must belong to it.  After a cudaDeviceReset (or anything else that destroys
+ *    the device's primary context) the cached address is stale: do not call this entry
+ *    point on that device again in the same process.
  *  - Every call shares the one array: calls whose work overlaps on the GPU (different
  *    streams, or different host threads on one device) race and corrupt each other; the
  *    array keeps the last call's contents, and each call rewrites every entry it reads.
- *  - Out-of-range expert indices are skipped (their slots get -1) but not reported: there
- *    is no workspace status word.
- * Returns MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED or MOE_ERR_CUDA. */
+ *  - Out-of-range or repeated expert indices are not reported (there is no workspace
+ *    status word): out-of-range slots get -1, and a repeated expert's rows are
+ *    unspecified (never out of bounds).
+ * Returns MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED or MOE_ERR_CUDA, with the reason
+ * in moe_last_error_detail(). */
 int moe_dispatch_static(int T, int k, int E, int H, int x_dtype, int capacity,
                         const int32_t* topk_idx, const void* X, int32_t* counts,
                         int32_t* offsets, int32_t* row_of_slot, int32_t* slot_of_row,

@@ -30,6 +30,33 @@ constexpr float kRouterEpsCuda = 1.9073486328125e-06f;     // 2^-19
 constexpr float kRouterEpsTensor = 1.52587890625e-05f;     // 2^-16
 }
 
+namespace {
+thread_local std::string g_detail;
+}
+
+namespace moe {
+
+int fail(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_detail = buf;
+  return code;
+}
+
+int ok() {
+  g_detail.clear();
+  return MOE_OK;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+  return fail(MOE_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+}  // namespace moe
+
 struct moe_ctx {
   int device = 0;
   int num_sms = 0;
@@ -49,34 +76,7 @@ struct moe_ctx {
 
 namespace {
 
-thread_local std::string g_detail;
-
-int fail(int code, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
-int fail(int code, const char* fmt, ...) {
-  char buf[512];
-  va_list ap;
-  va_start(ap, fmt);
-  vsnprintf(buf, sizeof buf, fmt, ap);
-  va_end(ap);
-  g_detail = buf;
-  return code;
-}
-
-int ok() {
-  g_detail.clear();
-  return MOE_OK;
-}
-
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-
-// An NVTX range named after the entry point around each compute call, so a profiler can
-// group the kernels of one call (host-side only; a no-op unless a tool is attached).
-struct NvtxRange {
-  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
-  ~NvtxRange() { nvtxRangePop(); }
-  NvtxRange(const NvtxRange&) = delete;
-  NvtxRange& operator=(const NvtxRange&) = delete;
-};
 
 cudaEvent_t take_event(moe_ctx* c) {
   if (!c->pool.empty()) {
@@ -111,10 +111,6 @@ int check_ctx(moe_ctx* c) {
     return fail(MOE_ERR_INVALID_ARG, "current device %d is not the context's device %d", dev,
                 c->device);
   return MOE_OK;
-}
-
-int cuda_fail(cudaError_t e, const char* what) {
-  return fail(MOE_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
 }
 
 int check_shape(int T, int E, int k) {

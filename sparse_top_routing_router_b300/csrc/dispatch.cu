@@ -97,7 +97,10 @@ __global__ void __launch_bounds__(kChunk) dispatch_scatter_kernel(DispatchArgs a
   if (t < a.T) {
     for (int j = 0; j < a.k; ++j) {
       const int e = a.idx[(size_t)t * a.k + j];
-      if (e >= 0 && e < a.E) atomicOr(&bits[e][wd], me);
+      // this thread alone sets bit `me`: finding it already set means the token named
+      // expert e twice, which would give two slots one row (reported, not repaired)
+      if (e >= 0 && e < a.E && (atomicOr(&bits[e][wd], me) & me))
+        set_status(a.status, MOE_ERR_DEVICE_INDEX);
     }
   }
   __syncthreads();
@@ -218,12 +221,13 @@ cudaError_t launch_dispatch_gather(const DispatchArgs& a, cudaStream_t s) {
 
 // ---------------------------------------------------------------- allocation-free entry
 //
-// moe_dispatch_static: the same dispatch for callers that cannot call cudaMalloc - code
-// that runs where the device allocator is off limits (inside a region that a CUDA graph is
-// being captured from, under a host runtime or inference engine that owns all device
-// memory and hands out only fixed buffers, or in a process whose allocator must never
-// grow).  Its scratch (the per-chunk count and base tables) lives in the array below,
-// which the module holds on every GPU that loads the library until the process exits.
+// moe_dispatch_static: the same dispatch for callers that may not allocate device memory
+// at the moment they dispatch - an inference engine or host runtime that owns all device
+// memory and hands out only the buffers it planned, or a process whose allocator must
+// never grow (cudaMalloc can also synchronise the device, which a latency-bound decode loop
+// cannot afford).  Its scratch (the per-chunk count and base tables) lives in the array
+// below, which the module holds on every GPU that loads the library until the process
+// exits.
 
 namespace {
 constexpr int kStaticMaxT = 65536;                                   // tokens per call
@@ -265,25 +269,37 @@ extern "C" int moe_dispatch_static(int T, int k, int E, int H, int x_dtype, int 
                                    int32_t* offsets, int32_t* row_of_slot,
                                    int32_t* slot_of_row, void* Xperm, moe_stream_t stream) {
   using namespace moe;
-  if (T < 0 || E < 1 || E > kMaxE || k < 1 || k > E || k > kMaxK) return MOE_ERR_INVALID_ARG;
-  if (T > kStaticMaxT) return MOE_ERR_UNSUPPORTED;   // beyond the static scratch
-  if (!counts || !offsets) return MOE_ERR_INVALID_ARG;
-  if (T > 0 && (!topk_idx || !row_of_slot || !slot_of_row)) return MOE_ERR_INVALID_ARG;
-  if ((X == nullptr) != (Xperm == nullptr)) return MOE_ERR_INVALID_ARG;
+  const NvtxRange nvtx_range(__func__);
+  if (T < 0) return fail(MOE_ERR_INVALID_ARG, "T = %d < 0", T);
+  if (E < 1 || E > kMaxE || k < 1 || k > E || k > kMaxK)
+    return fail(MOE_ERR_INVALID_ARG, "E = %d, k = %d: need 1 <= k <= min(E, %d), E <= %d", E,
+                k, kMaxK, kMaxE);
+  if (T > kStaticMaxT)
+    return fail(MOE_ERR_UNSUPPORTED, "T = %d exceeds the %d tokens the static scratch holds",
+                T, kStaticMaxT);
+  if (!counts || !offsets) return fail(MOE_ERR_INVALID_ARG, "counts/offsets null");
+  if (T > 0 && (!topk_idx || !row_of_slot || !slot_of_row))
+    return fail(MOE_ERR_INVALID_ARG, "topk_idx/row_of_slot/slot_of_row null");
+  if ((X == nullptr) != (Xperm == nullptr))
+    return fail(MOE_ERR_INVALID_ARG, "X and Xperm must be given together");
   if (Xperm) {
-    if (x_dtype != MOE_DTYPE_BF16 && x_dtype != MOE_DTYPE_F32) return MOE_ERR_INVALID_ARG;
-    if (H < 1 || (H * (x_dtype == MOE_DTYPE_BF16 ? 2 : 4)) % 16 != 0) return MOE_ERR_UNSUPPORTED;
+    if (x_dtype != MOE_DTYPE_BF16 && x_dtype != MOE_DTYPE_F32)
+      return fail(MOE_ERR_INVALID_ARG, "x_dtype = %d", x_dtype);
+    if (H < 1 || (H * (x_dtype == MOE_DTYPE_BF16 ? 2 : 4)) % 16 != 0)
+      return fail(MOE_ERR_UNSUPPORTED, "row of H = %d elements is not a multiple of 16 B", H);
     if ((reinterpret_cast<uintptr_t>(X) | reinterpret_cast<uintptr_t>(Xperm)) & 15u)
-      return MOE_ERR_INVALID_ARG;
+      return fail(MOE_ERR_INVALID_ARG, "X and Xperm must be 16-byte aligned");
   }
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   int32_t* scratch = nullptr;
-  if (static_scratch(&scratch) != cudaSuccess) return MOE_ERR_CUDA;
+  cudaError_t e;
+  if ((e = static_scratch(&scratch)) != cudaSuccess)
+    return cuda_fail(e, "static scratch address lookup");
   if (T == 0) {
-    if (cudaMemsetAsync(counts, 0, sizeof(int32_t) * E, s) != cudaSuccess ||
-        cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (E + 1), s) != cudaSuccess)
-      return MOE_ERR_CUDA;
-    return MOE_OK;
+    if ((e = cudaMemsetAsync(counts, 0, sizeof(int32_t) * E, s)) != cudaSuccess ||
+        (e = cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (E + 1), s)) != cudaSuccess)
+      return cuda_fail(e, "cudaMemsetAsync");
+    return ok();
   }
   const int nchunks = (T + kDispatchChunk - 1) / kDispatchChunk;
   DispatchArgs a;
@@ -305,10 +321,12 @@ extern "C" int moe_dispatch_static(int T, int k, int E, int H, int x_dtype, int 
   a.chunk_counts = scratch;
   a.chunk_base = scratch + (size_t)nchunks * E;
   a.status = nullptr;
-  if (launch_dispatch_count(a, s) != cudaSuccess || launch_dispatch_scan(a, s) != cudaSuccess ||
-      launch_dispatch_scatter(a, s) != cudaSuccess ||
-      (Xperm && launch_dispatch_gather(a, s) != cudaSuccess))
-    return MOE_ERR_CUDA;
-  return MOE_OK;
+  if ((e = launch_dispatch_count(a, s)) != cudaSuccess) return cuda_fail(e, "dispatch_count launch");
+  if ((e = launch_dispatch_scan(a, s)) != cudaSuccess) return cuda_fail(e, "dispatch_scan launch");
+  if ((e = launch_dispatch_scatter(a, s)) != cudaSuccess)
+    return cuda_fail(e, "dispatch_scatter launch");
+  if (Xperm && (e = launch_dispatch_gather(a, s)) != cudaSuccess)
+    return cuda_fail(e, "dispatch_gather launch");
+  return ok();
 }
 

@@ -44,6 +44,10 @@ constexpr int kMaxGroups = kMaxE + 1;
 constexpr int kMaxRing = 12;   // router tiles of a narrow N cut the same bytes into more stages
 
 enum Mode { GATE_UP = 0, DOWN = 1, ROUTER = 2 };
+enum GroupOrder { kOrderIndex = 0, kOrderInterleave = 1 };
+#ifndef MOE_GROUP_ORDER
+#define MOE_GROUP_ORDER kOrderIndex
+#endif
 
 template <bool PAIR>
 struct Cfg {
@@ -81,6 +85,7 @@ struct TcParams {
   uint32_t router_tx;   // bytes per stage: A box + the W_g-piece box(es)
   int ring;             // stages of the ring (ROUTER; the others use Cfg::kStages)
   uint32_t stage_bytes; // bytes between stages (ROUTER; a multiple of 1024)
+  int order;            // kOrderIndex or kOrderInterleave: group order of the tile list
 };
 
 template <bool PAIR>
@@ -95,7 +100,8 @@ struct __align__(1024) Smem {
   int abort_flag;
   int ngroups;
   int total_tiles;
-  int tile_start[kMaxGroups + 1];
+  int tile_start[kMaxGroups + 1];   // first tile of the group at each list position
+  int grp_at[kMaxGroups];           // group at each position of the tile list
   int grp_rows[kMaxGroups];
   int grp_row0[kMaxGroups];   // first A row of the group
   int grp_out0[kMaxGroups];   // first output row (h, O or O_shared) of the group
@@ -123,10 +129,11 @@ __device__ __forceinline__ TileInfo decode_tile(const Smem<PAIR>& S, int tile, i
   }
   constexpr int TM = Cfg<PAIR>::kTileM;
   TileInfo ti;
-  ti.g = lo;
-  ti.rows = S.grp_rows[lo];
-  ti.row0 = S.grp_row0[lo];
-  ti.out0 = S.grp_out0[lo];
+  const int g = S.grp_at[lo];
+  ti.g = g;
+  ti.rows = S.grp_rows[g];
+  ti.row0 = S.grp_row0[g];
+  ti.out0 = S.grp_out0[g];
   const int mt = (ti.rows + TM - 1) / TM;
   const int local = tile - S.tile_start[lo];
   ti.m0 = (local % mt) * TM;
@@ -280,8 +287,28 @@ __global__ void __launch_bounds__(kThreads, 1)
     S.grp_out0[g] = out0;
   }
   __syncthreads();
-  for (int g = tid; g < ngroups; g += kThreads)
-    S.tile_start[g] = ((S.grp_rows[g] + TM - 1) / TM) * n_tiles_n *
+  // Order of the groups in the tile list.  kOrderIndex: expert index order (the shared
+  // expert last).  kOrderInterleave: by row count, largest and smallest alternating
+  // (largest, smallest, 2nd largest, 2nd smallest, ...; ties to the lower index), so that
+  // the CTAs working at any moment mix tiles of large groups, whose weight tile many m-tiles
+  // share through L2 (bound by the tensor pipe), with tiles of small groups, which stream
+  // their weights from HBM for a few rows.
+  for (int g = tid; g < ngroups; g += kThreads) {
+    int pos = g;
+    if (MODE != ROUTER && p.order == kOrderInterleave) {
+      const int mg = S.grp_rows[g];
+      int r = 0;
+      for (int h = 0; h < ngroups; ++h) {
+        const int mh = S.grp_rows[h];
+        r += (mh > mg) || (mh == mg && h < g);
+      }
+      pos = r < (ngroups + 1) / 2 ? 2 * r : 2 * (ngroups - 1 - r) + 1;
+    }
+    S.grp_at[pos] = g;
+  }
+  __syncthreads();
+  for (int q = tid; q < ngroups; q += kThreads)
+    S.tile_start[q] = ((S.grp_rows[S.grp_at[q]] + TM - 1) / TM) * n_tiles_n *
                       (MODE == ROUTER ? p.splits : 1);     // count, scanned below
   __syncthreads();
   if (warp == 0) {
@@ -841,6 +868,7 @@ cudaError_t launch_tc(const ExpertArgs& a, EncodeTiledFn enc, bool* encode_faile
   p.router_tx = 0;
   p.ring = Cfg<PAIR>::kStages;
   p.stage_bytes = Cfg<PAIR>::kStageBytes;
+  p.order = MOE_GROUP_ORDER;
 
   constexpr int TM = Cfg<PAIR>::kTileM;
   const int n_tiles_n = (N + n_tile - 1) / n_tile;

@@ -7,10 +7,27 @@
 #include <stdint.h>
 
 #include <cuda_bf16.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include "../../include/moe.h"
 
 namespace moe {
+
+// Error reporting shared by every entry point (defined in abi.cu): fail() records the
+// text that moe_last_error_detail() returns to this thread and passes `code` through;
+// ok() clears it and returns MOE_OK.
+int fail(int code, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
+int ok();
+int cuda_fail(cudaError_t e, const char* what);
+
+// An NVTX range named after the entry point around each compute call, so a profiler can
+// group the kernels of one call (host-side only; a no-op unless a tool is attached).
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
 
 constexpr int kMaxE = 512;
 constexpr int kMaxK = 32;

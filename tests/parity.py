@@ -16,13 +16,12 @@ from sparse_top_routing_router_b300.inputs import make_inputs, token_subset
 from sparse_top_routing_router_b300.layer import MoELayer
 
 GAP_EXCLUDE = 1e-6          # rows whose k-th/(k+1)-th key margin is below this are excluded
-# Gates are computed from the fp32 logits.  A softmax (renormalised or not) or a
-# renormalised sigmoid gate moves by at most 2 max|dl| when the logits move by dl, so the
-# gate tolerance is twice the router's logit error bound (the bound its exactness guard
-# uses: eps_rel * max(1, max|l|) * sqrt(max(1, H/1024)), eps_rel = 2^-17 for the
-# tensor-core logits, the larger of the two paths) plus fp32 rounding of exp and divide.
-LOGIT_EPS_REL = 2.0 ** -17
-GATE_FP32_SLACK = 2e-6
+# One fixed bound on |gate - gate_oracle| for every workload and both router paths, set
+# from what the output needs, not from any kernel's error: a gate enters Y only as the
+# weight of an expert output, so k gates each off by 1e-5 move Y by at most
+# k * 1e-5 * max|o|, under 0.1 % of the 2e-2 * RMS(Y) output budget for k <= 8; it is also
+# 200x finer than the bf16 resolution of a gate near 0.5.
+GATE_ATOL = 1e-5
 Y_TOL = {"bf16": 2e-2, "f32": 1e-4}   # max-abs error / RMS(Y_oracle)
 
 
@@ -76,13 +75,10 @@ def check_routing(run: Run, ref: Dict[str, np.ndarray]) -> Dict[str, object]:
         assert np.all(chosen[~ok_rows] >= kth[~ok_rows] - GAP_EXCLUDE)
     # ascending expert order, distinct experts
     assert np.all(np.diff(idx, axis=1) > 0)
-    # gates of the agreed rows, against the bound derived from the logit error bound
-    H = run.cfg.H
-    l_scale = np.maximum(1.0, np.abs(ref["logits"]).max(axis=1)) * np.sqrt(max(1.0, H / 1024))
-    g_tol = 2 * LOGIT_EPS_REL * l_scale + GATE_FP32_SLACK
+    # gates of the agreed rows, against the fixed bound
     g_dev = np.abs(gate - ref["gate"]).max(axis=1)
     g_err = float(g_dev[ok_rows].max()) if ok_rows.any() else 0.0
-    assert np.all(g_dev[ok_rows] <= g_tol[ok_rows]), f"gate error {g_err}"
+    assert g_err <= GATE_ATOL, f"gate error {g_err:.3e} > {GATE_ATOL:g}"
     if run.cfg.renorm:
         np.testing.assert_allclose(gate.sum(1), 1.0, atol=1e-5)
     # the reported gap agrees with the oracle's where it is informative

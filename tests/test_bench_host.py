@@ -67,21 +67,28 @@ def test_traffic_figure_only_for_the_profiled_source(tmp_path, monkeypatch):
     src.write_bytes(b"// kernel source\n")
     sha = hashlib.sha256(src.read_bytes()).hexdigest()[:16]
     prof = tmp_path / "traffic.txt"
-    prof.write_text(json.dumps({"kernel_sha": sha, "dram_bytes_per_launch": 123}))
+    prof.write_text(json.dumps([
+        {"workload_name": "a", "kernel_sha": sha, "dram_bytes_per_launch": 123},
+        {"workload_name": "b", "kernel_sha": "0" * 16, "dram_bytes_per_launch": 456}]))
     monkeypatch.setattr(bench, "KERNEL_SRC", str(src))
     monkeypatch.setattr(bench, "PROFILE_TRAFFIC", str(prof))
-    assert bench.traffic_from_profile()["dram_bytes_per_launch"] == 123
+    assert bench.traffic_from_profile("a")["dram_bytes_per_launch"] == 123
+    assert bench.traffic_from_profile("b") is None          # profiled on another source
+    assert bench.traffic_from_profile("c") is None          # never profiled
     src.write_bytes(b"// kernel source, changed\n")
-    assert bench.traffic_from_profile() is None
+    assert bench.traffic_from_profile("a") is None
     monkeypatch.setattr(bench, "PROFILE_TRAFFIC", str(tmp_path / "missing.txt"))
-    assert bench.traffic_from_profile() is None
+    assert bench.traffic_from_profile("a") is None
 
 
 def test_committed_traffic_profile_is_well_formed():
     with open(bench.PROFILE_TRAFFIC) as fh:
-        j = json.load(fh)
-    assert j["dram_bytes_per_launch"] == j["dram_bytes_read"] + j["dram_bytes_write"]
-    assert len(j["kernel_sha"]) == 16 and "--clock-control none" in j["command"]
+        entries = json.load(fh)
+    assert isinstance(entries, list) and entries
+    for j in entries:
+        assert j["workload_name"] in K.BY_NAME
+        assert j["dram_bytes_per_launch"] == j["dram_bytes_read"] + j["dram_bytes_write"]
+        assert len(j["kernel_sha"]) == 16 and "--clock-control none" in j["command"]
 
 
 def test_workload_config_names_the_workload():
@@ -102,7 +109,7 @@ def test_peaks_are_read_from_the_measured_file():
                      "bf16_tflops_sustained": 1400.0, "source": "fallback"}
 
 
-def test_cpu_baseline_sample_grows_to_the_batch_or_the_memory_cap(monkeypatch):
+def test_cpu_baseline_sample_grows_to_the_batch(monkeypatch):
     from sparse_top_routing_router_b300.inputs import make_inputs
     cfg = K.TINY_F32                       # T=64, E=8, k=2
     d = make_inputs(cfg, device="cpu")
@@ -114,17 +121,31 @@ def test_cpu_baseline_sample_grows_to_the_batch_or_the_memory_cap(monkeypatch):
         return real(cfg_, d_, cf_, n, seed)
     monkeypatch.setattr(bench, "oracle_sample", spy)
     # a time floor it never reaches: doubles from 5 up to the whole batch
-    tr, tf, n, threads = bench.cpu_baseline_sample(cfg, d, None, 5, min_seconds=1e9)
-    assert sizes == [5, 10, 20, 40, 64] and n == 64 and threads >= 1
+    tr, tf, n, staging = bench.cpu_baseline_sample(cfg, d, None, 5, min_seconds=1e9)
+    assert sizes == [5, 10, 20, 40, 64] and n == 64 and staging >= 0.0
     # a floor the first sample meets: one sample
     sizes.clear()
     bench.cpu_baseline_sample(cfg, d, None, 5, min_seconds=0.0)
     assert sizes == [5]
-    # memory: 3 experts' float64 weights allowed, so 2 tokens (4 slots) are not
-    sizes.clear()
-    per_expert = 3 * cfg.H * cfg.I * 8
-    bench.cpu_baseline_sample(cfg, d, None, 1, min_seconds=1e9, mem_bytes=3 * per_expert)
-    assert sizes == [1]
+
+
+def test_oracle_sample_takes_weight_staging_off_the_clock(monkeypatch):
+    from sparse_top_routing_router_b300.inputs import make_inputs
+    cfg = K.TINY_F32
+    d = make_inputs(cfg, device="cpu")
+    bench._HOST_CACHE.clear()
+    bench._HOST_CACHE_BYTES[0] = 0
+    real = bench._host
+
+    def slow(t):                           # staging that takes 20 ms per tensor
+        bench.time.sleep(0.02)
+        return real(t)
+    monkeypatch.setattr(bench, "_host", slow)
+    tr, tf, n, staging = bench.oracle_sample(cfg, d, None, 64, seed=1)
+    # every touched expert's three matrices were staged inside combine_subset ...
+    assert staging >= 0.02 * 3 * 2
+    # ... and that time is not in the expert-stage figure
+    assert tf < staging
 
 
 def test_reference_sample_fits_the_step_budget():
@@ -133,6 +154,22 @@ def test_reference_sample_fits_the_step_budget():
     d = make_inputs(cfg, device="cpu")
     assert bench.reference_sample_tokens(cfg, d, None, step_budget_s=1e9) == 64
     assert bench.reference_sample_tokens(cfg, d, None, step_budget_s=0.0) == 2
-    per_expert = 3 * cfg.H * cfg.I * 8
-    # 4 tokens (8 slots) would need all 8 experts: capped at 2 tokens by memory
-    assert bench.reference_sample_tokens(cfg, d, None, 1e9, mem_bytes=7 * per_expert) == 2
+
+
+def test_step_quantiles():
+    q = bench.step_quantiles([5.0, 1.0, 3.0, 2.0, 4.0])
+    assert q["median"] == 3.0 and q["mean"] == 3.0
+    assert abs(q["p10"] - 1.4) < 1e-12 and abs(q["p90"] - 4.6) < 1e-12
+    assert bench.step_quantiles([7.0]) == {"median": 7.0, "p10": 7.0, "p90": 7.0, "mean": 7.0}
+
+
+def test_both_arms_describe_the_same_config():
+    c = bench.run_config(K.DSV3_PREFILL, None, 1)
+    assert c["workload"] == "dsv3_prefill_bf16" and c["parallelism"] == "replicas x1"
+    assert "larger than L2" in c["l2"]
+    assert "smaller" not in bench.run_config(K.TINY_F32, None, 1)["l2"]
+    assert "fit in L2" in bench.run_config(K.TINY_F32, None, 1)["l2"]
+
+
+def test_default_workload_is_the_largest_single_gpu_config():
+    assert bench.DEFAULT_CONFIG == K.DSV3_PREFILL.name

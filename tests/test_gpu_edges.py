@@ -130,6 +130,26 @@ def test_bad_routing_index_is_reported(ctx):
     assert B.moe_get_device_status(ctx, ws) == 0      # reset by the previous read
 
 
+def test_repeated_expert_in_a_row_is_reported(ctx):
+    # the k experts of a token must be distinct; a repeat is reported in the status word
+    # (its rows are then unspecified, never out of bounds)
+    T, k, E = 300, 3, 8
+    idx = torch.tensor([[0, 2, 5]] * T, dtype=torch.int32, device="cuda")
+    idx[260, 2] = 2
+    ws = torch.zeros(B.moe_workspace_bytes(T, 64, E, 64, k, 0, 0), dtype=torch.uint8,
+                     device="cuda")
+    counts = torch.empty(E, dtype=torch.int32, device="cuda")
+    offsets = torch.empty(E + 1, dtype=torch.int32, device="cuda")
+    ros = torch.empty(T * k, dtype=torch.int32, device="cuda")
+    sor = torch.empty(T * k, dtype=torch.int32, device="cuda")
+    B.moe_dispatch(ctx, idx, E, -1, counts, offsets, ros, sor, ws, H=64)
+    assert B.moe_get_device_status(ctx, ws) == B.MOE_ERR_DEVICE_INDEX
+    assert int(ros.max()) < T * k and int(ros.min()) >= 0
+    idx[260, 2] = 5
+    B.moe_dispatch(ctx, idx, E, -1, counts, offsets, ros, sor, ws, H=64)
+    assert B.moe_get_device_status(ctx, ws) == 0
+
+
 def test_bad_offsets_are_reported(ctx):
     cfg = _small(T=32)
     d = make_inputs(cfg, device="cuda")

@@ -1,8 +1,8 @@
 """GPU parity of expert-choice routing ("LLM Internals §14.2", the two selection
 paradigms; "MoE 03: efficiency frontiers", Expert Choice Routing) against the fp64 oracle,
 through the C ABI: every expert's C = T*k/E tokens bit-exact (columns whose oracle margin
-is below 1e-6 excluded and counted, and checked for validity), gates within the bound
-derived from the logit error, and Y within the layer tolerance."""
+is below 1e-6 excluded and counted, and checked for validity), gates within the fixed
+bound of the token-choice tests (1e-5), and Y within the layer tolerance."""
 
 import numpy as np
 import pytest
@@ -46,11 +46,10 @@ def check_expert_choice(run, ref, all_columns=False, n_tokens=None):
             assert np.all(S[chosen[e], e] >= kth - P.GAP_EXCLUDE)
     gate = P.to_np(L.gate)
     taken = ros.reshape(T, E) >= 0
-    l_scale = np.maximum(1.0, np.abs(ref["logits"]).max(axis=1)) * \
-        np.sqrt(max(1.0, c.H / 1024))
-    g_tol = 2 * P.LOGIT_EPS_REL * l_scale[:, None] + P.GATE_FP32_SLACK
     both = taken & (ref["row_of_slot"].reshape(T, E) >= 0)
-    assert np.all(np.abs(gate - ref["gate"])[both] <= np.broadcast_to(g_tol, gate.shape)[both])
+    g_err = float(np.abs(gate - ref["gate"])[both].max()) if both.any() else 0.0
+    print(f"{c.name}: max gate error {g_err:.3e}")
+    assert g_err <= P.GATE_ATOL
     assert np.all(gate[~taken] == 0)
     # outputs of tokens whose expert set agrees with the oracle's
     tokens = token_subset(T, n_tokens if n_tokens else T, 1).numpy()

@@ -14,6 +14,7 @@ from sparse_top_routing_router_b300 import binding as B
 from sparse_top_routing_router_b300 import configs as K
 
 from . import parity as P
+from .fp8_oracle_pool import ordered_fetch
 
 pytestmark = pytest.mark.gpu
 
@@ -47,7 +48,7 @@ def _fp8_expert_fetch(d):
     return get
 
 
-def _check_fp8_layer(cfg, n_tokens=None):
+def _check_fp8_layer(cfg, n_tokens=None, pool=False):
     run = P.run_gpu(cfg)
     assert run.status == 0
     ref = P.oracle_route(run)
@@ -66,7 +67,18 @@ def _check_fp8_layer(cfg, n_tokens=None):
     if c.shared:
         shared = tuple(O.dequantize_fp8_rows(*O.quantize_fp8_rows(
             P.to_np(d[n]).astype(np.float32))) for n in ("Ws_gate", "Ws_up", "Ws_down"))
-    Yref = O.combine_subset(P.to_np(d["X"]), ref, _fp8_expert_fetch(d), tokens, shared)
+    if pool:
+        idx, ros = ref["idx"], ref["row_of_slot"].reshape(c.T, c.k)
+        need = sorted({int(idx[t, j]) for t in tokens for j in range(c.k) if ros[t, j] >= 0})
+        fetch, close = ordered_fetch(
+            need, lambda e: tuple(P.to_np(d[n][e]).astype(np.float32)
+                                  for n in ("W_gate", "W_up", "W_down")))
+        try:
+            Yref = O.combine_subset(P.to_np(d["X"]), ref, fetch, tokens, shared)
+        finally:
+            close()
+    else:
+        Yref = O.combine_subset(P.to_np(d["X"]), ref, _fp8_expert_fetch(d), tokens, shared)
     Y = P.to_np(L.Y[torch.as_tensor(tokens, device=L.Y.device)])
     rms = float(np.sqrt(np.mean(Yref ** 2)))
     err = float(np.abs(Y - Yref).max())
@@ -90,4 +102,5 @@ def test_fp8_layer_small(cfg):
 
 def test_fp8_layer_full_size_decode():
     cfg = dataclasses.replace(K.DSV3_DECODE, name="dsv3_decode_bf16_fp8", fp8_experts=True)
-    print(cfg.name, _check_fp8_layer(cfg, n_tokens=4))
+    # every one of the 64 tokens, their experts quantized by the oracle in a process pool
+    print(cfg.name, _check_fp8_layer(cfg, pool=True))

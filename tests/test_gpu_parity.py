@@ -62,8 +62,10 @@ def test_small_full_parity(cfg):
     _cleanup()
 
 
-FULL = [(K.MIXTRAL, None, 48), (K.DSV3_DECODE, None, 64), (K.DSV3_PREFILL, None, 24),
-        (K.SWITCH, 1.0, 96), (K.SWITCH, 1.25, 96)]
+# (workload, capacity factor, tokens whose output is compared with the oracle); routing,
+# dispatch and gates are compared on every token
+FULL = [(K.MIXTRAL, None, 256), (K.DSV3_DECODE, None, 64), (K.DSV3_PREFILL, None, 256),
+        (K.SWITCH, 1.0, 256), (K.SWITCH, 1.25, 256)]
 
 
 @pytest.mark.parametrize("cfg,cf,n_tok", FULL,

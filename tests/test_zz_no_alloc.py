@@ -1,21 +1,24 @@
 """The allocation-free dispatch entry point, moe_dispatch_static.
 
-Some callers cannot allocate device memory at the moment they need the dispatch: a
-program in the middle of capturing a CUDA graph (an allocation there breaks or
-invalidates the capture), or an engine that plans every device buffer up front and
-forbids the allocator from growing afterwards.  moe_dispatch_static serves them: it takes
-only inputs and outputs and keeps its scratch in a static device array inside the
-library.  This test calls it through the C ABI and checks it against moe_dispatch (the
-workspace-based entry point) on two calls in a row, so the second call runs on the
-scratch contents the first one left behind.  Dispatch is integer work, so the comparison
-is exact.  This file is named to be collected last.
+Some callers may not allocate device memory at the moment they need the dispatch: an
+engine or host runtime that plans every device buffer up front and forbids the allocator
+from growing afterwards, or a latency-bound loop that cannot afford the device-wide
+synchronisation a cudaMalloc may cause.  moe_dispatch_static serves them: it takes only
+inputs and outputs and keeps its scratch in a static device array inside the library.
+This test calls it through the C ABI and checks it against moe_dispatch (the
+workspace-based entry point) and against the oracle's dispatch of the same routing, on two
+calls in a row, so the second call runs on the scratch contents the first one left
+behind.  Dispatch is integer work, so the comparison is exact.  This file is named to be
+collected last.
 """
 
 import ctypes as C
 
+import numpy as np
 import pytest
 import torch
 
+from oracle import moe_oracle as O
 from sparse_top_routing_router_b300 import binding as B
 
 pytestmark = pytest.mark.gpu
@@ -67,6 +70,14 @@ def test_static_dispatch_matches_workspace_dispatch():
         assert torch.equal(out[3][:R], ref[3][:R])    # slot_of_row
         assert torch.equal(out[4][:R], ref[4][:R])    # gathered rows
         assert B.moe_get_device_status(ctx, ws) == 0
+        # and directly against the oracle's dispatch of the same routing
+        o = O.dispatch(idx.cpu().numpy().astype(np.int64), E, None if cap < 0 else cap)
+        assert np.array_equal(out[0].cpu().numpy(), o["counts"])
+        assert np.array_equal(out[1].cpu().numpy(), o["offsets"])
+        assert np.array_equal(out[2].cpu().numpy(), o["row_of_slot"])
+        assert np.array_equal(out[3][:R].cpu().numpy(), o["slot_of_row"])
+        toks = torch.as_tensor(o["slot_of_row"] // k, device="cuda")
+        assert torch.equal(out[4][:R], X[toks])
 
 
 def test_static_dispatch_rejects_too_many_tokens():
@@ -75,3 +86,4 @@ def test_static_dispatch_rejects_too_many_tokens():
                               C.c_void_p(16), C.c_void_p(16), C.c_void_p(16), C.c_void_p(16),
                               None, None)
     assert r == B.MOE_ERR_UNSUPPORTED
+    assert b"65537" in L.moe_last_error_detail()

@@ -8,8 +8,9 @@
 //            rows, so the SwiGLU is applied in the epilogue straight from TMEM.
 //   DOWN:    o = h W_down^T, fp32 out, 256-column tiles.
 // and two shapes of work unit:
-//   single CTA (PAIR = false): 128-row tiles, tcgen05.mma.cta_group::1 M=128 N=256; a
-//            stage holds A [128 x 64] and both weight boxes [2 x 128 x 64] (48 KB), 4 stages.
+//   single CTA (PAIR = false): 128-row tiles, tcgen05.mma.cta_group::1 M=128 N=256 (M=64
+//            for a group's last tile of at most 64 rows); a stage holds A [128 x 64] and
+//            both weight boxes [2 x 128 x 64] (48 KB), 4 stages.
 //   CTA pair   (PAIR = true):  a cluster of 2 CTAs owns a 256-row tile; each CTA loads its
 //            own 128 rows of A and one 128-row weight box (32 KB per stage, 6 stages),
 //            the leader CTA issues tcgen05.mma.cta_group::2 M=256 N=256 over both CTAs'
@@ -44,10 +45,11 @@ constexpr int kMaxGroups = kMaxE + 1;
 constexpr int kMaxRing = 12;   // router tiles of a narrow N cut the same bytes into more stages
 
 enum Mode { GATE_UP = 0, DOWN = 1, ROUTER = 2 };
-enum GroupOrder { kOrderIndex = 0, kOrderInterleave = 1 };
-#ifndef MOE_GROUP_ORDER
-#define MOE_GROUP_ORDER kOrderIndex
-#endif
+// A group taller than kMBlockRows rows runs its m-tiles in blocks of kMBlockRows rows,
+// every n-tile of a block before the next block, so that the block's A rows (29 MB at
+// H = 7168) stay in L2 across its n-tiles.  Without the blocks a tall group - above all the
+// shared expert, whose A is all of X - streams its A once per n-tile pass.
+constexpr int kMBlockRows = 2048;
 
 template <bool PAIR>
 struct Cfg {
@@ -85,7 +87,6 @@ struct TcParams {
   uint32_t router_tx;   // bytes per stage: A box + the W_g-piece box(es)
   int ring;             // stages of the ring (ROUTER; the others use Cfg::kStages)
   uint32_t stage_bytes; // bytes between stages (ROUTER; a multiple of 1024)
-  int order;            // kOrderIndex or kOrderInterleave: group order of the tile list
 };
 
 template <bool PAIR>
@@ -100,13 +101,16 @@ struct __align__(1024) Smem {
   int abort_flag;
   int ngroups;
   int total_tiles;
-  int tile_start[kMaxGroups + 1];   // first tile of the group at each list position
-  int grp_at[kMaxGroups];           // group at each position of the tile list
+  int tile_start[kMaxGroups + 1];
   int grp_rows[kMaxGroups];
   int grp_row0[kMaxGroups];   // first A row of the group
   int grp_out0[kMaxGroups];   // first output row (h, O or O_shared) of the group
   float stage[4][32][33];     // epilogue: one 32 x 32 fp32 chunk per warp, padded rows
 };
+
+// dynamic shared memory of one CTA (+ 1 KB to align the tiles) within the 227 KB limit
+static_assert(sizeof(Smem<false>) + 1024 <= 227 * 1024, "single-CTA shared memory");
+static_assert(sizeof(Smem<true>) + 1024 <= 227 * 1024, "CTA-pair shared memory");
 
 // The gate and up weights as 64-row boxes: a CTA pair's half tile takes them in the
 // order [gate 0-63 | up 0-63 | gate 64-127 | up 64-127] (see half_tile).
@@ -120,7 +124,7 @@ struct TileInfo {
 
 template <bool PAIR>
 __device__ __forceinline__ TileInfo decode_tile(const Smem<PAIR>& S, int tile, int n_tile,
-                                                int n_tiles_n) {
+                                                int n_tiles_n, int mblock) {
   int lo = 0, hi = S.ngroups - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
@@ -129,13 +133,24 @@ __device__ __forceinline__ TileInfo decode_tile(const Smem<PAIR>& S, int tile, i
   }
   constexpr int TM = Cfg<PAIR>::kTileM;
   TileInfo ti;
-  const int g = S.grp_at[lo];
-  ti.g = g;
-  ti.rows = S.grp_rows[g];
-  ti.row0 = S.grp_row0[g];
-  ti.out0 = S.grp_out0[g];
+  ti.g = lo;
+  ti.rows = S.grp_rows[lo];
+  ti.row0 = S.grp_row0[lo];
+  ti.out0 = S.grp_out0[lo];
   const int mt = (ti.rows + TM - 1) / TM;
   const int local = tile - S.tile_start[lo];
+  if (mblock > 0 && mt > mblock) {
+    // a group taller than mblock m-tiles: blocks of mblock m-tiles, every n-tile of a block
+    // before the next block, so that the block's A rows stay in L2 across the n-tiles
+    const int per_block = mblock * n_tiles_n;
+    const int b = local / per_block;
+    const int in = local - b * per_block;
+    const int bm = min(mblock, mt - b * mblock);
+    ti.m0 = (b * mblock + in % bm) * TM;
+    ti.n0 = (in / bm) * n_tile;
+    ti.z = 0;
+    return ti;
+  }
   ti.m0 = (local % mt) * TM;
   const int rest = local / mt;                 // n-tile, then split-K slice (router)
   ti.n0 = (rest % n_tiles_n) * n_tile;
@@ -166,6 +181,14 @@ __device__ __forceinline__ bool is_swapped_tail(const TileInfo& ti, int swap_row
 
 __device__ __forceinline__ int swap_cols(const TileInfo& ti) {
   return (ti.rows - ti.m0 + 15) & ~15;   // 16..kSwapRows rounded up to 16
+}
+
+// Single-CTA tail tiles of at most 64 live rows run as M = 64 MMAs (half the multiply-adds
+// of an M = 128 tile).  Their accumulator rows sit 16 to a TMEM lane quadrant: row r in
+// lane 32 (r / 16) + r % 16, so epilogue warp q holds rows 16 q .. 16 q + 15 in its
+// lanes 0-15.
+__device__ __forceinline__ bool is_m64_tail(const TileInfo& ti) {
+  return ti.rows - ti.m0 <= 64;
 }
 
 // CTA pairs: a group's last tile of at most 128 rows runs as M = 128 (64 rows from each
@@ -287,28 +310,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     S.grp_out0[g] = out0;
   }
   __syncthreads();
-  // Order of the groups in the tile list.  kOrderIndex: expert index order (the shared
-  // expert last).  kOrderInterleave: by row count, largest and smallest alternating
-  // (largest, smallest, 2nd largest, 2nd smallest, ...; ties to the lower index), so that
-  // the CTAs working at any moment mix tiles of large groups, whose weight tile many m-tiles
-  // share through L2 (bound by the tensor pipe), with tiles of small groups, which stream
-  // their weights from HBM for a few rows.
-  for (int g = tid; g < ngroups; g += kThreads) {
-    int pos = g;
-    if (MODE != ROUTER && p.order == kOrderInterleave) {
-      const int mg = S.grp_rows[g];
-      int r = 0;
-      for (int h = 0; h < ngroups; ++h) {
-        const int mh = S.grp_rows[h];
-        r += (mh > mg) || (mh == mg && h < g);
-      }
-      pos = r < (ngroups + 1) / 2 ? 2 * r : 2 * (ngroups - 1 - r) + 1;
-    }
-    S.grp_at[pos] = g;
-  }
-  __syncthreads();
-  for (int q = tid; q < ngroups; q += kThreads)
-    S.tile_start[q] = ((S.grp_rows[S.grp_at[q]] + TM - 1) / TM) * n_tiles_n *
+  for (int g = tid; g < ngroups; g += kThreads)
+    S.tile_start[g] = ((S.grp_rows[g] + TM - 1) / TM) * n_tiles_n *
                       (MODE == ROUTER ? p.splits : 1);     // count, scanned below
   __syncthreads();
   if (warp == 0) {
@@ -338,6 +341,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int total = S.total_tiles;
   const volatile int* abort_flag = &S.abort_flag;
   const unsigned long long lim = p.wait_limit_ns;
+  constexpr bool M64 = !PAIR && MODE != ROUTER;   // M = 64 tail tiles (single CTA)
+  const int mblock = MODE == ROUTER ? 0 : kMBlockRows / Cfg<PAIR>::kTileM;
 
   if (warp == 0 && lane == 0) {
     // ---------------------------------------------------------------- TMA producer
@@ -354,7 +359,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t issued_mask = 0, issued_parity = 0;
     bool ok = true;
     for (int tile = unit; tile < total && ok; tile += n_units) {
-      const TileInfo ti = decode_tile<PAIR>(S, tile, p.n_tile, n_tiles_n);
+      const TileInfo ti = decode_tile<PAIR>(S, tile, p.n_tile, n_tiles_n, mblock);
       const bool sh = (MODE == ROUTER) || ti.g >= p.E;
       const CUtensorMap* a_map = sh ? &mA_sh : &mA;
       // a pair's half tile (M = 128) takes 64 rows from each CTA
@@ -458,17 +463,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       int kb_lo = 0, kb_hi = nkb;
       bool swap = false;
       uint32_t sw_idesc = 0;
+      uint32_t mma_idesc = idesc;
       if (MODE == ROUTER) {
-        const TileInfo ti = decode_tile<PAIR>(S, tile, p.n_tile, n_tiles_n);
+        const TileInfo ti = decode_tile<PAIR>(S, tile, p.n_tile, n_tiles_n, mblock);
         kb_lo = (int)((long long)nkb * ti.z / p.splits);
         kb_hi = (int)((long long)nkb * (ti.z + 1) / p.splits);
-      } else if (SWAP) {
-        const TileInfo ti = decode_tile<PAIR>(S, tile, p.n_tile, n_tiles_n);
-        swap = is_swapped_tail(ti, p.swap_rows);
+      } else if (SWAP || M64) {
+        const TileInfo ti = decode_tile<PAIR>(S, tile, p.n_tile, n_tiles_n, mblock);
+        swap = SWAP && is_swapped_tail(ti, p.swap_rows);
         if (swap) sw_idesc = idesc_bf16_f32(128, swap_cols(ti));
+        else if (M64 && is_m64_tail(ti)) mma_idesc = idesc_bf16_f32(64, 256);
       }
       uint32_t pair_idesc = C::kIdesc;
-      if (PAIR && half_tile<PAIR>(decode_tile<PAIR>(S, tile, p.n_tile, n_tiles_n)))
+      if (PAIR && half_tile<PAIR>(decode_tile<PAIR>(S, tile, p.n_tile, n_tiles_n, mblock)))
         pair_idesc = idesc_bf16_f32(128, 256);
       const bool got = PAIR ? mbar_wait_cluster(&S.tempty[acc], acc_phase ^ 1u, abort_flag, lim)
                             : mbar_wait(&S.tempty[acc], acc_phase ^ 1u, abort_flag, lim);
@@ -511,7 +518,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int kk = 0; kk < BK / 16; ++kk) {
             const uint32_t accum = (kb != kb_lo || kk != 0) ? 1u : 0u;
             if (PAIR) umma_bf16_pair(d, adesc + 2 * kk, bdesc + 2 * kk, pair_idesc, accum);
-            else umma_bf16(d, adesc + 2 * kk, bdesc + 2 * kk, idesc, accum);
+            else umma_bf16(d, adesc + 2 * kk, bdesc + 2 * kk, mma_idesc, accum);
           }
         }
         if (PAIR) umma_commit_pair_mc(&S.empty[stage], 0x3);
@@ -547,7 +554,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int tile = unit; tile < total; tile += n_units) {
-      const TileInfo ti = decode_tile<PAIR>(S, tile, p.n_tile, n_tiles_n);
+      const TileInfo ti = decode_tile<PAIR>(S, tile, p.n_tile, n_tiles_n, mblock);
       const bool got = mbar_wait(&S.tfull[acc], acc_phase, abort_flag, lim);
       if (!__all_sync(0xffffffffu, got)) {
         S.abort_flag = 1;
@@ -556,8 +563,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_after();
       const uint32_t tb = tmem_base + acc * kAccCols + (static_cast<uint32_t>(q * 32) << 16);
-      const int m = ti.m0 + r_in_tile;
-      const bool valid = m < ti.rows;
+      const bool m64 = M64 && is_m64_tail(ti) && !(SWAP && is_swapped_tail(ti, p.swap_rows));
+      const int m = ti.m0 + (m64 ? q * 16 + (lane & 15) : r_in_tile);
+      const bool valid = m < ti.rows && (!m64 || lane < 16);
       const bool sh = ti.g >= p.E;
       if (PAIR && MODE != ROUTER) {
         // A full tile (M = 256): this lane is row 128 r + q*32 + lane with all 256
@@ -721,8 +729,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       } else {
         // this warp's 32 rows start at m - lane
-        const int wrow = m - lane;
-        const int nrows = min(32, max(0, ti.rows - wrow));
+        const int wrow = m64 ? ti.m0 + q * 16 : m - lane;
+        const int nrows = min(m64 ? 16 : 32, max(0, ti.rows - wrow));
         float* dst = (sh ? p.O_shared : p.O) + ((size_t)ti.out0 + wrow) * p.N + ti.n0;
 #pragma unroll 1
         for (int c = 0; c < 256; c += 32) {
@@ -868,7 +876,6 @@ cudaError_t launch_tc(const ExpertArgs& a, EncodeTiledFn enc, bool* encode_faile
   p.router_tx = 0;
   p.ring = Cfg<PAIR>::kStages;
   p.stage_bytes = Cfg<PAIR>::kStageBytes;
-  p.order = MOE_GROUP_ORDER;
 
   constexpr int TM = Cfg<PAIR>::kTileM;
   const int n_tiles_n = (N + n_tile - 1) / n_tile;

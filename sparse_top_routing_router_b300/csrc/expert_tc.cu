@@ -116,6 +116,9 @@ static_assert(sizeof(Smem<true>) + 1024 <= 227 * 1024, "CTA-pair shared memory")
 // order [gate 0-63 | up 0-63 | gate 64-127 | up 64-127] (see half_tile).
 struct HalfMaps {
   CUtensorMap gate, up, gate_sh, up_sh;
+  // A (and the shared expert's A) with 64-row boxes: a tile of at most 64 live rows per
+  // CTA (single-CTA tails of <= 64 rows, a pair's half tiles) loads only those rows
+  CUtensorMap a64, a64_sh;
 };
 
 struct TileInfo {
@@ -391,8 +394,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_2d(st + kBoxBytes + q * p.piece_bytes, &mB0_sh, &S.full[stage],
                         kx + q * p.a_kmod, ti.n0);
         } else if (!PAIR) {
-          mbar_arrive_expect_tx(&S.full[stage], MODE == ROUTER ? p.router_tx : C::kTxBytes);
-          tma_load_2d(st, a_map, &S.full[stage], MODE == ROUTER ? kx % p.a_kmod : kx, ay);
+          // a tail of at most 64 rows (M = 64 or operand-swapped MMAs) reads A rows 0-63
+          const bool a64 = MODE != ROUTER && is_m64_tail(ti);
+          mbar_arrive_expect_tx(&S.full[stage],
+                                MODE == ROUTER ? p.router_tx
+                                               : (a64 ? C::kTxBytes - kBoxBytes / 2 : C::kTxBytes));
+          tma_load_2d(st, a64 ? (sh ? &hm.a64_sh : &hm.a64) : a_map, &S.full[stage],
+                      MODE == ROUTER ? kx % p.a_kmod : kx, ay);
           const CUtensorMap* b0 = sh ? &mB0_sh : &mB0;
           const CUtensorMap* b1 = (MODE == GATE_UP) ? (sh ? &mB1_sh : &mB1) : b0;
           const int n1 = (MODE == GATE_UP) ? ti.n0 : ti.n0 + 128;
@@ -406,10 +414,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_3d(st + 2 * kBoxBytes, b1, &S.full[stage], kx, n1, ti.g);
           }
         } else {
-          // both CTAs' copies count on the leader's barrier; the leader expects all bytes
-          if (rank == 0) mbar_arrive_expect_tx(&S.full[stage], C::kTxBytes);
+          // both CTAs' copies count on the leader's barrier; the leader expects all bytes.
+          // A half tile (M = 128) takes 64 rows of A from each CTA.
+          const bool hf = half_tile<PAIR>(ti);
+          if (rank == 0)
+            mbar_arrive_expect_tx(&S.full[stage], hf ? C::kTxBytes - kBoxBytes : C::kTxBytes);
           const uint32_t bar = mapa_shared(smem_u32(&S.full[stage]), 0);
-          tma_load_2d_pair(st, a_map, bar, kx, ay);
+          tma_load_2d_pair(st, hf ? (sh ? &hm.a64_sh : &hm.a64) : a_map, bar, kx, ay);
           // weight half of this CTA.  GATE_UP full tile: rank 0 the gate rows, rank 1 the
           // up rows n0 .. + 127; half tile: gate rows n0 + 64 r .. + 63, then the up rows
           // of the same outputs (64-row boxes), so that every TMEM lane holds the gate and
@@ -838,9 +849,14 @@ cudaError_t launch_tc(const ExpertArgs& a, EncodeTiledFn enc, bool* encode_faile
       ok &= encode_2d(enc, &hm.gate_sh, a.has_shared ? a.Ws_gate : a.W_gate, K, N, 64);
       ok &= encode_2d(enc, &hm.up_sh, a.has_shared ? a.Ws_up : a.W_up, K, N, 64);
     }
+    ok &= encode_2d(enc, &hm.a64, a.Xperm, K, Tk, 64);
+    ok &= encode_2d(enc, &hm.a64_sh, a.has_shared ? a.X : a.Xperm, K, a.has_shared ? a.T : Tk,
+                    64);
   } else {
     ok &= encode_2d(enc, &mA, a.h, K, h_rows);
     mA_sh = mA;
+    ok &= encode_2d(enc, &hm.a64, a.h, K, h_rows, 64);
+    hm.a64_sh = hm.a64;
     ok &= encode_3d(enc, &mB0, a.W_down, K, N, a.E);
     mB1 = mB0;
     ok &= encode_2d(enc, &mB0_sh, a.has_shared ? a.Ws_down : a.W_down, K, N);

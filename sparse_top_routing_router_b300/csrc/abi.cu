@@ -678,10 +678,17 @@ int moe_grouped_swiglu_fp8(moe_ctx* ctx, const moe_expert_desc* d, const void* X
   a.O_shared = O_shared;
   a.status = static_cast<int*>(ws);
   cudaError_t e;
-  if ((e = traced(ctx, MOE_K_EXPERT_GATE_UP, s, [&] { return launch_expert_gate_up_fp8(a, s); })))
-    return cuda_fail(e, "expert_gate_up (fp8) launch");
-  if ((e = traced(ctx, MOE_K_EXPERT_DOWN, s, [&] { return launch_expert_down_fp8(a, s); })))
-    return cuda_fail(e, "expert_down (fp8) launch");
+  bool bad = false;
+  e = traced(ctx, MOE_K_EXPERT_GATE_UP, s, [&] {
+    return launch_expert_gate_up_fp8(a, ctx->encode, &bad, ctx->wait_limit_ns, s);
+  });
+  if (bad) return fail(MOE_ERR_INVALID_ARG, "tensor map encoding failed (fp8 gate/up)");
+  if (e) return cuda_fail(e, "expert_gate_up (fp8) launch");
+  e = traced(ctx, MOE_K_EXPERT_DOWN, s, [&] {
+    return launch_expert_down_fp8(a, ctx->encode, &bad, ctx->wait_limit_ns, s);
+  });
+  if (bad) return fail(MOE_ERR_INVALID_ARG, "tensor map encoding failed (fp8 down)");
+  if (e) return cuda_fail(e, "expert_down (fp8) launch");
   return ok();
 }
 

@@ -8,11 +8,21 @@
 // with saturation; both divisions are correctly rounded fp32.
 //
 // The expert GEMMs of a decode step do 2 b FLOP per weight byte for b rows per expert (a
-// few): the step streams weights, and the arithmetic only has to keep pace with HBM.
-// Each warp takes 16 weight rows against 8 rows of the expert (m16n8k16 bf16 mma.sync,
-// fp32 accumulation), decoding the codes exactly to bf16 in registers on the way; a
-// tcgen05 tile would spend its 128-row operand on 8 live rows and would need the codes
-// converted in shared memory first.  The channel's scale multiplies the finished sum.
+// few): the step streams weights, and the arithmetic only has to keep pace with HBM.  Both
+// GEMVs multiply 16 weight rows by up to 8 rows of the expert with m16n8k16 bf16 mma.sync
+// (fp32 accumulation), decoding the codes exactly to bf16 in registers on the way; the
+// channel's scale multiplies the finished sum.  (A tcgen05 tile would spend its 128-row
+// operand on 8 live rows and would need the codes converted in shared memory first.)
+//  gate/up  a work item is (expert, up to 8 of its rows, 64 output channels).  One CTA per
+//           SM: a producer warp streams the item's gate and up code rows and its input rows
+//           through a 5-stage shared-memory ring with TMA (128-byte swizzle, 256 k per
+//           stage), about 140 KB of weight reads in flight per SM; 16 consumer warps, four
+//           k groups of four, each take one 64-wide k slice of every stage for 16 channels,
+//           and the groups' partial sums are added in group order at the end of the item.
+//  down     the rows of W_down are only I codes long: every warp loads its 16 rows itself
+//           with one 64-wide chunk in flight, three CTAs of 8 warps per SM.
+#include <string.h>
+
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
 
@@ -220,47 +230,6 @@ __device__ __forceinline__ int find_group8(const Fp8Table& S, int item) {
 constexpr int kChanPerWarp = 16;
 constexpr int kChanPerCta = kChanPerWarp * (kFp8Threads / 32);   // 128
 
-// Gate/up: a warp takes 16 channels, their gate and up rows; h = SiLU(s_g a) * (s_u u),
-// rounded to bf16 as in the tensor-core path.
-__global__ void __launch_bounds__(kFp8Threads) fp8_gate_up_kernel(Fp8Args a) {
-  __shared__ Fp8Table S;
-  const int n_blk = (a.I + kChanPerCta - 1) / kChanPerCta;
-  build_fp8_table(S, a, 0, n_blk);
-  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  const int g = lane >> 2, t = lane & 3;
-  const __nv_bfloat16* Xp = static_cast<const __nv_bfloat16*>(a.Xperm);
-  const __nv_bfloat16* X = static_cast<const __nv_bfloat16*>(a.X);
-  __nv_bfloat16* h = static_cast<__nv_bfloat16*>(a.h);
-  for (int item = blockIdx.x; item < S.total; item += gridDim.x) {
-    const int grp = find_group8(S, item);
-    const int local = item - S.start[grp];
-    const int pass = local / n_blk, blk = local % n_blk;
-    const int r0 = pass * kFp8Rows;
-    const int mr = min(kFp8Rows, S.rows[grp] - r0);
-    const int i0 = blk * kChanPerCta + w * kChanPerWarp;
-    if (i0 >= a.I) continue;   // I % 64 == 0, so a started warp has all 16 channels
-    const bool sh = grp >= a.E;
-    const uint8_t* Wg = (sh ? a.Qs_gate : a.Q_gate + (size_t)grp * a.I * a.H) + (size_t)i0 * a.H;
-    const uint8_t* Wu = (sh ? a.Qs_up : a.Q_up + (size_t)grp * a.I * a.H) + (size_t)i0 * a.H;
-    const float* sg = (sh ? a.Ss_gate : a.S_gate + (size_t)grp * a.I) + i0;
-    const float* su = (sh ? a.Ss_up : a.S_up + (size_t)grp * a.I) + i0;
-    const uint8_t* const rows[2] = {Wg, Wu};
-    const __nv_bfloat16* xr = (sh ? X : Xp) + (size_t)(S.row0[grp] + r0) * a.H;
-    float acc[2][4];
-    gemv_mma<2>(rows, a.H, xr, a.H, mr, a.H, lane, acc);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int ch = g + (i >= 2 ? 8 : 0);
-      const int n = 2 * t + (i & 1);
-      if (n < mr) {
-        const float gv = sg[ch] * acc[0][i], uv = su[ch] * acc[1][i];
-        h[(size_t)(S.out0[grp] + r0 + n) * a.I + i0 + ch] =
-            __float2bfloat16_rn(gv / (1.f + __expf(-gv)) * uv);
-      }
-    }
-  }
-}
-
 // Down: a warp takes 16 output channels of W_down; O = s_d * (h . code).
 __global__ void __launch_bounds__(kFp8Threads) fp8_down_kernel(Fp8Args a) {
   __shared__ Fp8Table S;
@@ -294,6 +263,298 @@ __global__ void __launch_bounds__(kFp8Threads) fp8_down_kernel(Fp8Args a) {
   }
 }
 
+constexpr int kF8Chunk = 256;            // k per ring stage
+constexpr int kF8Ch = 64;                // output channels per work item
+constexpr int kF8KGroups = 4;            // consumer warp groups, one 64-wide k slice each
+constexpr int kF8Consumers = 4 * kF8KGroups;   // 16 channels per warp of a group
+constexpr int kF8Threads = (kF8Consumers + 1) * 32;
+constexpr int kF8Stages = 5;
+constexpr int kCodeBox = 64 * 128;       // TMA box: 64 channel rows x 128 codes
+constexpr int kXBox = kFp8Rows * 128;    // TMA box: 8 input rows x 64 bf16
+
+// NMAT code matrices per item (2: gate and up; the ring kernel is instantiated for the
+// gate/up GEMV).  A stage holds, per matrix, two code boxes (k 0-127, 128-255 of the
+// stage), then four input-row boxes (64 k each).
+template <int NMAT>
+struct F8Smem {
+  static constexpr int kStageBytes = NMAT * 2 * kCodeBox + 4 * kXBox;   // 36 or 20 KB
+  uint8_t ring[kF8Stages][kStageBytes];
+  uint64_t full[kF8Stages];
+  uint64_t empty[kF8Stages];
+  uint64_t part_written, part_read;   // per item: partial sums stored / consumed
+  int abort_flag;
+  float part[kF8KGroups - 1][4][NMAT * 4][32];   // partial sums of k groups 1.. per item
+  Fp8Table T;
+};
+
+// 16 bytes at logical 16-byte chunk `c` of row `r` of a box written by TMA with the
+// 128-byte swizzle (rows of 128 B; the chunk index is XORed with the row index mod 8).
+__device__ __forceinline__ uint4 ld_sw128(const uint8_t* box, int r, int c) {
+  return *reinterpret_cast<const uint4*>(box + r * 128 + ((c ^ (r & 7)) << 4));
+}
+
+// One 64-wide k slice of a stage.  Consumer warp w of a group holds rows w*16 + g and
+// w*16 + g + 8 of each code box (g = lane / 4) and input row g; inside each 64-wide k slice
+// lane t = lane % 4 supplies k = 16 t + 4 s + 0..3 at mma step s to both operands (a dot
+// product does not depend on the order of its terms), i.e. 16 contiguous codes of each of
+// its code rows and 16 contiguous bf16 of its input row.  acc[m] is the mma's D fragment
+// for matrix m: (channel g, rows 2t, 2t+1), (channel g + 8, rows 2t, 2t+1).
+template <int NMAT>
+__device__ __forceinline__ void f8_slice_mma(const uint8_t* st, int j, int w, int lane,
+                                             float (&acc)[NMAT][4]) {
+  const int g = lane >> 2, t = lane & 3;
+  const int r_lo = w * 16 + g, r_hi = r_lo + 8;
+  {                                         // 64-wide k slice j of the stage
+    const uint8_t* xb = st + NMAT * 2 * kCodeBox + j * kXBox;
+    const uint4 x0 = ld_sw128(xb, g, 2 * t), x1 = ld_sw128(xb, g, 2 * t + 1);
+    const uint32_t xw[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+    const int cb = (j & 1) * 4 + t;         // 16-byte chunk of the 128-code box row
+#pragma unroll
+    for (int m = 0; m < NMAT; ++m) {
+      const uint8_t* box = st + (m * 2 + (j >> 1)) * kCodeBox;
+      const uint4 c0 = ld_sw128(box, r_lo, cb), c8 = ld_sw128(box, r_hi, cb);
+      const uint32_t a0w[4] = {c0.x, c0.y, c0.z, c0.w};
+      const uint32_t a8w[4] = {c8.x, c8.y, c8.z, c8.w};
+#pragma unroll
+      for (int sstep = 0; sstep < 4; ++sstep) {
+        uint32_t l0, h0, l8, h8;
+        e4m3x4_to_bf16(a0w[sstep], l0, h0);
+        e4m3x4_to_bf16(a8w[sstep], l8, h8);
+        mma_16816(acc[m], l0, l8, h0, h8, xw[2 * sstep], xw[2 * sstep + 1]);
+      }
+    }
+  }
+}
+
+struct F8Maps {
+  CUtensorMap q0, q1, q0s, q1s;   // codes as [rows, K] uint8 (routed: E * N rows; shared: N)
+  CUtensorMap x, xs;              // input rows [rows, K] bf16 (routed, shared expert)
+};
+
+// NMAT = 2: gate/up, h = SiLU(s_g a) * (s_u u) rounded to bf16 as in the tensor-core path.
+// NMAT = 1: down, O = s_d * (h . code).
+template <int NMAT>
+__global__ void __launch_bounds__(kF8Threads, 1)
+    fp8_gemv_kernel(const __grid_constant__ F8Maps mp, const Fp8Args a,
+                    unsigned long long lim) {
+  extern __shared__ uint8_t f8_raw[];
+  F8Smem<NMAT>& S = *reinterpret_cast<F8Smem<NMAT>*>(
+      (reinterpret_cast<uintptr_t>(f8_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  constexpr int kMode = NMAT == 2 ? 0 : 1;
+  constexpr uint32_t kTx = (uint32_t)F8Smem<NMAT>::kStageBytes;
+  const int N = NMAT == 2 ? a.I : a.H;      // output channels of one expert
+  const int K = NMAT == 2 ? a.H : a.I;      // reduction length
+  const int n_blk = N / kF8Ch;
+  const int nchunks = (K + kF8Chunk - 1) / kF8Chunk;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (tid == 0) {
+    S.abort_flag = 0;
+    for (int q = 0; q < kF8Stages; ++q) {
+      mbar_init(&S.full[q], 1);
+      mbar_init(&S.empty[q], kF8Consumers);   // every consumer warp releases each stage
+    }
+    mbar_init(&S.part_written, kF8Consumers);
+    mbar_init(&S.part_read, kF8Consumers);
+    fence_mbar_init();
+  }
+  build_fp8_table(S.T, a, kMode, n_blk);   // ends with __syncthreads
+  const volatile int* abort_flag = &S.abort_flag;
+
+  if (warp == kF8Consumers) {
+    // ---------------------------------------------------------------- TMA producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0, issued_mask = 0, issued_parity = 0;
+      bool ok = true;
+      for (int item = blockIdx.x; item < S.T.total && ok; item += gridDim.x) {
+        const int grp = find_group8(S.T, item);
+        const int local = item - S.T.start[grp];
+        const int r0 = (local / n_blk) * kFp8Rows, ch0 = (local % n_blk) * kF8Ch;
+        const bool sh = grp >= a.E;
+        const int qrow = sh ? ch0 : grp * N + ch0;
+        const int xrow = S.T.row0[grp] + r0;
+        for (int c = 0; c < nchunks; ++c) {
+          if (!mbar_wait(&S.empty[stage], phase ^ 1u, abort_flag, lim)) {
+            ok = false;
+            break;
+          }
+          uint8_t* st = S.ring[stage];
+          const int k0 = c * kF8Chunk;
+          mbar_arrive_expect_tx(&S.full[stage], kTx);
+#pragma unroll
+          for (int m = 0; m < NMAT; ++m) {
+            const CUtensorMap* q = m == 0 ? (sh ? &mp.q0s : &mp.q0) : (sh ? &mp.q1s : &mp.q1);
+            tma_load_2d(st + (m * 2) * kCodeBox, q, &S.full[stage], k0, qrow);
+            tma_load_2d(st + (m * 2 + 1) * kCodeBox, q, &S.full[stage], k0 + 128, qrow);
+          }
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            tma_load_2d(st + NMAT * 2 * kCodeBox + j * kXBox, sh ? &mp.xs : &mp.x,
+                        &S.full[stage], k0 + 64 * j, xrow);
+          issued_mask |= 1u << stage;
+          issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+          if (++stage == kF8Stages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        S.abort_flag = 1;
+        set_status(a.status, MOE_ERR_TIMEOUT);
+        const int zero = 0;   // let every copy already issued land before leaving
+        for (int q = 0; q < kF8Stages; ++q)
+          if (issued_mask >> q & 1u) mbar_wait(&S.full[q], issued_parity >> q & 1u, &zero, lim);
+      }
+    }
+  } else {
+    // ---------------------------------------------------------------- consumers
+    // warp = kg * 4 + w: k group kg takes slice kg of every stage, w its 16 channels
+    const int kg = warp >> 2, w = warp & 3;
+    const int g = lane >> 2, t = lane & 3;
+    int stage = 0;
+    uint32_t phase = 0, item_phase = 0;
+    bool ok = true;
+    // a bounded wait of the whole warp; false (with the abort flag raised) if it gave up
+    auto warp_wait = [&](uint64_t* bar, uint32_t parity) {
+      const bool got = mbar_wait(bar, parity, abort_flag, lim);
+      if (__all_sync(0xffffffffu, got)) return true;
+      S.abort_flag = 1;
+      set_status(a.status, MOE_ERR_TIMEOUT);
+      return false;
+    };
+    for (int item = blockIdx.x; item < S.T.total && ok; item += gridDim.x) {
+      const int grp = find_group8(S.T, item);
+      const int local = item - S.T.start[grp];
+      const int r0 = (local / n_blk) * kFp8Rows, ch0 = (local % n_blk) * kF8Ch + w * 16;
+      const int mr = min(kFp8Rows, S.T.rows[grp] - r0);
+      const bool sh = grp >= a.E;
+      float acc[NMAT][4];
+#pragma unroll
+      for (int m = 0; m < NMAT; ++m)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc[m][i] = 0.f;
+      for (int c = 0; c < nchunks; ++c) {
+        if (!warp_wait(&S.full[stage], phase)) {
+          ok = false;
+          break;
+        }
+        f8_slice_mma<NMAT>(S.ring[stage], kg, w, lane, acc);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&S.empty[stage]);
+        if (++stage == kF8Stages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (!ok) break;
+      // the k groups' partial sums, added in group order by group 0; the next item's
+      // partials are stored only once group 0 has read these
+      if (kg > 0) {
+#pragma unroll
+        for (int m = 0; m < NMAT; ++m)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) S.part[kg - 1][w][m * 4 + i][lane] = acc[m][i];
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&S.part_written);
+      if (!warp_wait(&S.part_written, item_phase)) break;
+      if (kg == 0) {
+#pragma unroll
+        for (int q = 0; q < kF8KGroups - 1; ++q)
+#pragma unroll
+          for (int m = 0; m < NMAT; ++m)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) acc[m][i] += S.part[q][w][m * 4 + i][lane];
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&S.part_read);
+      if (!warp_wait(&S.part_read, item_phase)) break;
+      item_phase ^= 1u;
+      if (kg > 0) continue;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int ch = g + (i >= 2 ? 8 : 0);
+        const int n = 2 * t + (i & 1);
+        if (n >= mr) continue;
+        const size_t orow = (size_t)(S.T.out0[grp] + r0 + n);
+        if (NMAT == 2) {
+          const float* sg = (sh ? a.Ss_gate : a.S_gate + (size_t)grp * a.I) + ch0;
+          const float* su = (sh ? a.Ss_up : a.S_up + (size_t)grp * a.I) + ch0;
+          const float gv = sg[ch] * acc[0][i], uv = su[ch] * acc[NMAT - 1][i];
+          static_cast<__nv_bfloat16*>(a.h)[orow * a.I + ch0 + ch] =
+              __float2bfloat16_rn(gv / (1.f + __expf(-gv)) * uv);
+        } else {
+          const float* sd = (sh ? a.Ss_down : a.S_down + (size_t)grp * a.H) + ch0;
+          (sh ? a.O_shared : a.O)[orow * a.H + ch0 + ch] = sd[ch] * acc[0][i];
+        }
+      }
+    }
+  }
+}
+
+bool encode_f8(EncodeTiledFn enc, CUtensorMap* m, bool codes, const void* base, uint64_t K,
+               uint64_t rows) {
+  const cuuint64_t dims[2] = {K, rows};
+  const cuuint64_t strides[1] = {K * (codes ? 1 : 2)};
+  const cuuint32_t box[2] = {codes ? 128u : 64u, codes ? 64u : (cuuint32_t)kFp8Rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(m, codes ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+             const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int NMAT>
+cudaError_t launch_f8(const Fp8Args& a, EncodeTiledFn enc, bool* encode_failed,
+                      unsigned long long lim, cudaStream_t s) {
+  *encode_failed = false;
+  const int Tk = a.T * a.k;
+  F8Maps mp;
+  memset(&mp, 0, sizeof(mp));
+  bool ok = true;
+  if (NMAT == 2) {
+    ok &= encode_f8(enc, &mp.q0, true, a.Q_gate, a.H, (uint64_t)a.E * a.I);
+    ok &= encode_f8(enc, &mp.q1, true, a.Q_up, a.H, (uint64_t)a.E * a.I);
+    ok &= encode_f8(enc, &mp.q0s, true, a.has_shared ? a.Qs_gate : a.Q_gate, a.H, a.I);
+    ok &= encode_f8(enc, &mp.q1s, true, a.has_shared ? a.Qs_up : a.Q_up, a.H, a.I);
+    ok &= encode_f8(enc, &mp.x, false, a.Xperm, a.H, Tk);
+    ok &= encode_f8(enc, &mp.xs, false, a.has_shared ? a.X : a.Xperm, a.H,
+                    a.has_shared ? a.T : Tk);
+  } else {
+    ok &= encode_f8(enc, &mp.q0, true, a.Q_down, a.I, (uint64_t)a.E * a.H);
+    ok &= encode_f8(enc, &mp.q0s, true, a.has_shared ? a.Qs_down : a.Q_down, a.I, a.H);
+    mp.q1 = mp.q0;
+    mp.q1s = mp.q0s;
+    ok &= encode_f8(enc, &mp.x, false, a.h, a.I, (uint64_t)Tk + (a.has_shared ? a.T : 0));
+    mp.xs = mp.x;
+  }
+  if (!ok) {
+    *encode_failed = true;
+    return cudaErrorInvalidValue;
+  }
+  const size_t smem = sizeof(F8Smem<NMAT>) + 1024;
+  auto* fn = fp8_gemv_kernel<NMAT>;
+  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  static int grid = 0;      // one resident wave of CTAs, computed once per process
+  if (!grid) {
+    int per_sm = 0, dev = 0, sms = kGridSms;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kF8Threads, smem) !=
+            cudaSuccess || per_sm < 1) {
+      cudaGetLastError();
+      per_sm = 1;
+    }
+    if (cudaGetDevice(&dev) == cudaSuccess)
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    grid = per_sm * (sms > 0 ? sms : kGridSms);
+  }
+  fn<<<grid, kF8Threads, smem, s>>>(mp, a, lim);
+  return cudaGetLastError();
+}
+
+static_assert(sizeof(F8Smem<2>) + 1024 <= 227 * 1024, "FP8 gate/up shared memory");
+
 }  // namespace
 
 cudaError_t launch_quantize_fp8_rows(int rows, int cols, int w_dtype, const void* W,
@@ -308,29 +569,35 @@ cudaError_t launch_quantize_fp8_rows(int rows, int cols, int w_dtype, const void
   return cudaGetLastError();
 }
 
-// A persistent grid: as many CTAs as fit on the GPU at once.
-static int resident_grid(const void* fn) {
-  int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kFp8Threads, 0) !=
-          cudaSuccess ||
-      per_sm < 1) {
-    cudaGetLastError();
-    per_sm = 1;
+cudaError_t launch_expert_gate_up_fp8(const Fp8Args& a, EncodeTiledFn enc,
+                                      bool* encode_failed, unsigned long long wait_limit_ns,
+                                      cudaStream_t s) {
+  return launch_f8<2>(a, enc, encode_failed, wait_limit_ns, s);
+}
+
+// The down GEMV streams W_down rows of only I codes (2 KB at I = 2048) per channel: there
+// the register-direct kernel (every warp loading its 16 rows itself, three CTAs of 8 warps
+// per SM) kept HBM busier than the TMA ring, whose per-item synchronisation of the k
+// groups weighs more on 8-stage items (DSV3-shaped decode, same-call A/B: 0.335 against
+// 0.463 ms).
+cudaError_t launch_expert_down_fp8(const Fp8Args& a, EncodeTiledFn enc, bool* encode_failed,
+                                   unsigned long long wait_limit_ns, cudaStream_t s) {
+  (void)enc;
+  (void)wait_limit_ns;
+  *encode_failed = false;
+  static int grid = 0;
+  if (!grid) {
+    int per_sm = 0, dev = 0, sms = kGridSms;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+            &per_sm, reinterpret_cast<const void*>(fp8_down_kernel), kFp8Threads, 0) !=
+            cudaSuccess || per_sm < 1) {
+      cudaGetLastError();
+      per_sm = 1;
+    }
+    if (cudaGetDevice(&dev) == cudaSuccess)
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    grid = per_sm * (sms > 0 ? sms : kGridSms);
   }
-  int dev = 0, sms = kGridSms;
-  if (cudaGetDevice(&dev) == cudaSuccess)
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  return per_sm * (sms > 0 ? sms : kGridSms);
-}
-
-cudaError_t launch_expert_gate_up_fp8(const Fp8Args& a, cudaStream_t s) {
-  static const int grid = resident_grid(reinterpret_cast<const void*>(fp8_gate_up_kernel));
-  fp8_gate_up_kernel<<<grid, kFp8Threads, 0, s>>>(a);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_expert_down_fp8(const Fp8Args& a, cudaStream_t s) {
-  static const int grid = resident_grid(reinterpret_cast<const void*>(fp8_down_kernel));
   fp8_down_kernel<<<grid, kFp8Threads, 0, s>>>(a);
   return cudaGetLastError();
 }

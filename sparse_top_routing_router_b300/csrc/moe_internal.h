@@ -241,8 +241,14 @@ struct Fp8Args {
 };
 cudaError_t launch_quantize_fp8_rows(int rows, int cols, int w_dtype, const void* W,
                                      uint8_t* q, float* scale, cudaStream_t s);
-cudaError_t launch_expert_gate_up_fp8(const Fp8Args& a, cudaStream_t s);
-cudaError_t launch_expert_down_fp8(const Fp8Args& a, cudaStream_t s);
+// TMA-fed: `encode` is the driver's cuTensorMapEncodeTiled (cudaErrorInvalidValue with
+// *encode_failed set when a tensor map cannot be encoded); waits give up after
+// wait_limit_ns.
+cudaError_t launch_expert_gate_up_fp8(const Fp8Args& a, EncodeTiledFn encode,
+                                      bool* encode_failed, unsigned long long wait_limit_ns,
+                                      cudaStream_t s);
+cudaError_t launch_expert_down_fp8(const Fp8Args& a, EncodeTiledFn encode, bool* encode_failed,
+                                   unsigned long long wait_limit_ns, cudaStream_t s);
 // fp32 CUDA-core path.
 cudaError_t launch_expert_gate_up_f32(const ExpertArgs& a, cudaStream_t s);
 cudaError_t launch_expert_down_f32(const ExpertArgs& a, cudaStream_t s);

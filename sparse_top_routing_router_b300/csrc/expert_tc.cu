@@ -399,16 +399,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive_expect_tx(&S.full[stage],
                                 MODE == ROUTER ? p.router_tx
                                                : (a64 ? C::kTxBytes - kBoxBytes / 2 : C::kTxBytes));
-          tma_load_2d(st, a64 ? (sh ? &hm.a64_sh : &hm.a64) : a_map, &S.full[stage],
-                      MODE == ROUTER ? kx % p.a_kmod : kx, ay);
+          // ROUTER over [X, X, X] . [hi; mid; lo]: the k-blocks run h-block by h-block,
+          // the three pieces of a 64-wide block of h one after another, so a split-K slice
+          // covers a range of h with all three pieces and each X box comes from DRAM once
+          // (the next two loads of it hit L2)
+          const int ka = MODE == ROUTER ? (kb / 3) * BK : kx;
+          const int kw = MODE == ROUTER ? (kb % 3) * p.a_kmod + (kb / 3) * BK : kx;
+          tma_load_2d(st, a64 ? (sh ? &hm.a64_sh : &hm.a64) : a_map, &S.full[stage], ka, ay);
           const CUtensorMap* b0 = sh ? &mB0_sh : &mB0;
           const CUtensorMap* b1 = (MODE == GATE_UP) ? (sh ? &mB1_sh : &mB1) : b0;
           const int n1 = (MODE == GATE_UP) ? ti.n0 : ti.n0 + 128;
           if (sh) {
-            tma_load_2d(st + kBoxBytes, b0, &S.full[stage], kx, ti.n0);
+            tma_load_2d(st + kBoxBytes, b0, &S.full[stage], kw, ti.n0);
             // a router tile of at most 128 experts takes one box of n_tile rows
             if (MODE != ROUTER || p.n_tile > 128)
-              tma_load_2d(st + 2 * kBoxBytes, b1, &S.full[stage], kx, n1);
+              tma_load_2d(st + 2 * kBoxBytes, b1, &S.full[stage], kw, n1);
           } else {
             tma_load_3d(st + kBoxBytes, b0, &S.full[stage], kx, ti.n0, ti.g);
             tma_load_3d(st + 2 * kBoxBytes, b1, &S.full[stage], kx, n1, ti.g);

@@ -13,14 +13,16 @@
 // (fp32 accumulation), decoding the codes exactly to bf16 in registers on the way; the
 // channel's scale multiplies the finished sum.  (A tcgen05 tile would spend its 128-row
 // operand on 8 live rows and would need the codes converted in shared memory first.)
-//  gate/up  a work item is (expert, up to 8 of its rows, 64 output channels).  One CTA per
-//           SM: a producer warp streams the item's gate and up code rows and its input rows
-//           through a 5-stage shared-memory ring with TMA (128-byte swizzle, 256 k per
-//           stage), about 140 KB of weight reads in flight per SM; 16 consumer warps, four
-//           k groups of four, each take one 64-wide k slice of every stage for 16 channels,
-//           and the groups' partial sums are added in group order at the end of the item.
-//  down     the rows of W_down are only I codes long: every warp loads its 16 rows itself
-//           with one 64-wide chunk in flight, three CTAs of 8 warps per SM.
+// A work item is (expert, up to 8 of its rows, a block of output channels).  One CTA per
+// SM: a producer warp streams the item's code rows and input rows through a shared-memory
+// ring with TMA (128-byte swizzle, 256 k per stage, about 140-200 KB in flight per SM), and
+// 16 consumer warps run the mma on what lands:
+//  gate/up  64 channels per item, gate and up rows (36 KB a stage, 5 stages); the warps
+//           form four k groups of four, each taking one 64-wide k slice of every stage for
+//           16 channels, and the groups' partial sums are added in group order at the end
+//           of the item.
+//  down     256 channels per item (68 KB a stage, 3 stages); every warp takes 16 channels
+//           over the whole k range, so an item ends with no hand-over between warps.
 #include <string.h>
 
 #include <cuda_fp16.h>
@@ -32,7 +34,6 @@
 namespace moe {
 namespace {
 
-constexpr int kFp8Threads = 256;      // 8 warps
 constexpr int kFp8Rows = 8;           // expert rows per pass: the mma's N
 constexpr int kMaxGroups8 = kMaxE + 1;
 
@@ -99,75 +100,6 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// One warp: NT tiles of 16 weight rows (rows[q] + g and + 8 for lane g = lane / 4) times
-// the 8 input rows xr + n * ldx (n < mr; zeros beyond), over K in 64-wide chunks.  The
-// mma's k order inside a chunk is permuted - lane t = lane % 4 supplies k = 16 t + 4 s
-// + 0..3 at step s for both operands - so each lane reads 16 contiguous codes of its two
-// weight rows and 16 contiguous bf16 of its input row; a dot product does not depend on
-// the order of its terms.  The next chunk's loads are issued before the current chunk's
-// conversions and MMAs.  acc[q] is the mma's D fragment: (row g, cols 2t, 2t+1), (row g+8,
-// cols 2t, 2t+1).
-template <int NT>
-__device__ __forceinline__ void gemv_mma(const uint8_t* const (&rows)[NT], size_t ldw,
-                                         const __nv_bfloat16* xr, size_t ldx, int mr, int K,
-                                         int lane, float (&acc)[NT][4]) {
-  const int g = lane >> 2, t = lane & 3;
-#pragma unroll
-  for (int q = 0; q < NT; ++q)
-#pragma unroll
-    for (int i = 0; i < 4; ++i) acc[q][i] = 0.f;
-  const uint8_t* w0[NT];
-  const uint8_t* w8[NT];
-#pragma unroll
-  for (int q = 0; q < NT; ++q) {
-    w0[q] = rows[q] + (size_t)g * ldw + 16 * t;
-    w8[q] = rows[q] + (size_t)(g + 8) * ldw + 16 * t;
-  }
-  const bool xin = g < mr;
-  const __nv_bfloat16* xp = xr + (size_t)(xin ? g : 0) * ldx + 16 * t;
-  uint4 c0[NT], c8[NT], cx0, cx1;
-#pragma unroll
-  for (int q = 0; q < NT; ++q) {
-    c0[q] = *reinterpret_cast<const uint4*>(w0[q]);
-    c8[q] = *reinterpret_cast<const uint4*>(w8[q]);
-  }
-  cx0 = xin ? reinterpret_cast<const uint4*>(xp)[0] : make_uint4(0, 0, 0, 0);
-  cx1 = xin ? reinterpret_cast<const uint4*>(xp)[1] : make_uint4(0, 0, 0, 0);
-  for (int kb = 0; kb < K; kb += 64) {
-    const int kn = kb + 64;
-    uint4 n0[NT], n8[NT], nx0 = make_uint4(0, 0, 0, 0), nx1 = make_uint4(0, 0, 0, 0);
-#pragma unroll
-    for (int q = 0; q < NT; ++q) {
-      n0[q] = kn < K ? *reinterpret_cast<const uint4*>(w0[q] + kn) : make_uint4(0, 0, 0, 0);
-      n8[q] = kn < K ? *reinterpret_cast<const uint4*>(w8[q] + kn) : make_uint4(0, 0, 0, 0);
-    }
-    if (xin && kn < K) {
-      nx0 = reinterpret_cast<const uint4*>(xp + kn)[0];
-      nx1 = reinterpret_cast<const uint4*>(xp + kn)[1];
-    }
-    const uint32_t xw[8] = {cx0.x, cx0.y, cx0.z, cx0.w, cx1.x, cx1.y, cx1.z, cx1.w};
-#pragma unroll
-    for (int q = 0; q < NT; ++q) {
-      const uint32_t a0w[4] = {c0[q].x, c0[q].y, c0[q].z, c0[q].w};
-      const uint32_t a8w[4] = {c8[q].x, c8[q].y, c8[q].z, c8[q].w};
-#pragma unroll
-      for (int st = 0; st < 4; ++st) {
-        uint32_t l0, h0, l8, h8;
-        e4m3x4_to_bf16(a0w[st], l0, h0);
-        e4m3x4_to_bf16(a8w[st], l8, h8);
-        mma_16816(acc[q], l0, l8, h0, h8, xw[2 * st], xw[2 * st + 1]);
-      }
-    }
-#pragma unroll
-    for (int q = 0; q < NT; ++q) {
-      c0[q] = n0[q];
-      c8[q] = n8[q];
-    }
-    cx0 = nx0;
-    cx1 = nx1;
-  }
-}
-
 struct Fp8Table {
   int ngroups, total;
   int start[kMaxGroups8 + 1];   // first work item of each group
@@ -227,63 +159,36 @@ __device__ __forceinline__ int find_group8(const Fp8Table& S, int item) {
   return lo;
 }
 
-constexpr int kChanPerWarp = 16;
-constexpr int kChanPerCta = kChanPerWarp * (kFp8Threads / 32);   // 128
-
-// Down: a warp takes 16 output channels of W_down; O = s_d * (h . code).
-__global__ void __launch_bounds__(kFp8Threads) fp8_down_kernel(Fp8Args a) {
-  __shared__ Fp8Table S;
-  const int n_blk = (a.H + kChanPerCta - 1) / kChanPerCta;
-  build_fp8_table(S, a, 1, n_blk);
-  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  const int g = lane >> 2, t = lane & 3;
-  const __nv_bfloat16* h = static_cast<const __nv_bfloat16*>(a.h);
-  for (int item = blockIdx.x; item < S.total; item += gridDim.x) {
-    const int grp = find_group8(S, item);
-    const int local = item - S.start[grp];
-    const int pass = local / n_blk, blk = local % n_blk;
-    const int r0 = pass * kFp8Rows;
-    const int mr = min(kFp8Rows, S.rows[grp] - r0);
-    const int j0 = blk * kChanPerCta + w * kChanPerWarp;
-    if (j0 >= a.H) continue;   // H % 64 == 0
-    const bool sh = grp >= a.E;
-    const uint8_t* Wd = (sh ? a.Qs_down : a.Q_down + (size_t)grp * a.H * a.I) + (size_t)j0 * a.I;
-    const float* sd = (sh ? a.Ss_down : a.S_down + (size_t)grp * a.H) + j0;
-    const uint8_t* const rows[1] = {Wd};
-    const __nv_bfloat16* xr = h + (size_t)(S.row0[grp] + r0) * a.I;
-    float acc[1][4];
-    gemv_mma<1>(rows, a.I, xr, a.I, mr, a.I, lane, acc);
-    float* out = sh ? a.O_shared : a.O;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int ch = g + (i >= 2 ? 8 : 0);
-      const int n = 2 * t + (i & 1);
-      if (n < mr) out[(size_t)(S.out0[grp] + r0 + n) * a.H + j0 + ch] = sd[ch] * acc[0][i];
-    }
-  }
-}
-
 constexpr int kF8Chunk = 256;            // k per ring stage
-constexpr int kF8Ch = 64;                // output channels per work item
-constexpr int kF8KGroups = 4;            // consumer warp groups, one 64-wide k slice each
-constexpr int kF8Consumers = 4 * kF8KGroups;   // 16 channels per warp of a group
+constexpr int kF8Consumers = 16;         // consumer warps, 16 channels each
 constexpr int kF8Threads = (kF8Consumers + 1) * 32;
-constexpr int kF8Stages = 5;
 constexpr int kCodeBox = 64 * 128;       // TMA box: 64 channel rows x 128 codes
 constexpr int kXBox = kFp8Rows * 128;    // TMA box: 8 input rows x 64 bf16
 
-// NMAT code matrices per item (2: gate and up; the ring kernel is instantiated for the
-// gate/up GEMV).  A stage holds, per matrix, two code boxes (k 0-127, 128-255 of the
-// stage), then four input-row boxes (64 k each).
-template <int NMAT>
+// Shape of the ring kernel.  NMAT code matrices per item (2: gate and up; 1: W_down); KG
+// k groups: the consumer warps split into KG groups of 16 / KG warps, group kg takes the
+// 64-wide k slices kg, kg + KG, ... of every stage, and the groups' partial sums are added
+// in group order at the end of an item.  An item covers 16 * 16 / KG channels; a stage
+// holds, per matrix, the item's code rows as 64-row boxes of k 0-127 and 128-255, then four
+// input-row boxes (64 k each).
+template <int NMAT, int KG>
+struct F8Shape {
+  static constexpr int kChanWarps = kF8Consumers / KG;
+  static constexpr int kCh = 16 * kChanWarps;             // channels per item
+  static constexpr int kRowGroups = kCh / 64;             // 64-row code boxes per k half
+  static constexpr int kStageBytes = NMAT * kRowGroups * 2 * kCodeBox + 4 * kXBox;
+  static constexpr int kStages = 210 * 1024 / kStageBytes < 5 ? 210 * 1024 / kStageBytes : 5;
+};
+
+template <int NMAT, int KG>
 struct F8Smem {
-  static constexpr int kStageBytes = NMAT * 2 * kCodeBox + 4 * kXBox;   // 36 or 20 KB
-  uint8_t ring[kF8Stages][kStageBytes];
-  uint64_t full[kF8Stages];
-  uint64_t empty[kF8Stages];
-  uint64_t part_written, part_read;   // per item: partial sums stored / consumed
+  using Sh = F8Shape<NMAT, KG>;
+  uint8_t ring[Sh::kStages][Sh::kStageBytes];
+  uint64_t full[Sh::kStages];
+  uint64_t empty[Sh::kStages];
+  uint64_t part_written, part_read;   // per item: partial sums stored / consumed (KG > 1)
   int abort_flag;
-  float part[kF8KGroups - 1][4][NMAT * 4][32];   // partial sums of k groups 1.. per item
+  float part[KG > 1 ? KG - 1 : 1][Sh::kChanWarps][NMAT * 4][32];   // groups 1.. per item
   Fp8Table T;
 };
 
@@ -299,19 +204,20 @@ __device__ __forceinline__ uint4 ld_sw128(const uint8_t* box, int r, int c) {
 // product does not depend on the order of its terms), i.e. 16 contiguous codes of each of
 // its code rows and 16 contiguous bf16 of its input row.  acc[m] is the mma's D fragment
 // for matrix m: (channel g, rows 2t, 2t+1), (channel g + 8, rows 2t, 2t+1).
-template <int NMAT>
+template <int NMAT, int RG>
 __device__ __forceinline__ void f8_slice_mma(const uint8_t* st, int j, int w, int lane,
                                              float (&acc)[NMAT][4]) {
   const int g = lane >> 2, t = lane & 3;
-  const int r_lo = w * 16 + g, r_hi = r_lo + 8;
+  const int rg = RG == 1 ? 0 : (w * 16) / 64;   // the 64-row code box of this warp's rows
+  const int r_lo = (RG == 1 ? w * 16 : (w * 16) % 64) + g, r_hi = r_lo + 8;
   {                                         // 64-wide k slice j of the stage
-    const uint8_t* xb = st + NMAT * 2 * kCodeBox + j * kXBox;
+    const uint8_t* xb = st + NMAT * RG * 2 * kCodeBox + j * kXBox;
     const uint4 x0 = ld_sw128(xb, g, 2 * t), x1 = ld_sw128(xb, g, 2 * t + 1);
     const uint32_t xw[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
     const int cb = (j & 1) * 4 + t;         // 16-byte chunk of the 128-code box row
 #pragma unroll
     for (int m = 0; m < NMAT; ++m) {
-      const uint8_t* box = st + (m * 2 + (j >> 1)) * kCodeBox;
+      const uint8_t* box = st + ((m * RG + rg) * 2 + (j >> 1)) * kCodeBox;
       const uint4 c0 = ld_sw128(box, r_lo, cb), c8 = ld_sw128(box, r_hi, cb);
       const uint32_t a0w[4] = {c0.x, c0.y, c0.z, c0.w};
       const uint32_t a8w[4] = {c8.x, c8.y, c8.z, c8.w};
@@ -333,18 +239,20 @@ struct F8Maps {
 
 // NMAT = 2: gate/up, h = SiLU(s_g a) * (s_u u) rounded to bf16 as in the tensor-core path.
 // NMAT = 1: down, O = s_d * (h . code).
-template <int NMAT>
+template <int NMAT, int KG>
 __global__ void __launch_bounds__(kF8Threads, 1)
     fp8_gemv_kernel(const __grid_constant__ F8Maps mp, const Fp8Args a,
                     unsigned long long lim) {
+  using Sh = F8Shape<NMAT, KG>;
+  constexpr int kF8Stages = Sh::kStages, kF8Ch = Sh::kCh, kRG = Sh::kRowGroups;
   extern __shared__ uint8_t f8_raw[];
-  F8Smem<NMAT>& S = *reinterpret_cast<F8Smem<NMAT>*>(
+  F8Smem<NMAT, KG>& S = *reinterpret_cast<F8Smem<NMAT, KG>*>(
       (reinterpret_cast<uintptr_t>(f8_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   constexpr int kMode = NMAT == 2 ? 0 : 1;
-  constexpr uint32_t kTx = (uint32_t)F8Smem<NMAT>::kStageBytes;
+  constexpr uint32_t kTx = (uint32_t)Sh::kStageBytes;
   const int N = NMAT == 2 ? a.I : a.H;      // output channels of one expert
   const int K = NMAT == 2 ? a.H : a.I;      // reduction length
-  const int n_blk = N / kF8Ch;
+  const int n_blk = (N + kF8Ch - 1) / kF8Ch;
   const int nchunks = (K + kF8Chunk - 1) / kF8Chunk;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid == 0) {
@@ -384,12 +292,16 @@ __global__ void __launch_bounds__(kF8Threads, 1)
 #pragma unroll
           for (int m = 0; m < NMAT; ++m) {
             const CUtensorMap* q = m == 0 ? (sh ? &mp.q0s : &mp.q0) : (sh ? &mp.q1s : &mp.q1);
-            tma_load_2d(st + (m * 2) * kCodeBox, q, &S.full[stage], k0, qrow);
-            tma_load_2d(st + (m * 2 + 1) * kCodeBox, q, &S.full[stage], k0 + 128, qrow);
+#pragma unroll
+            for (int rg = 0; rg < kRG; ++rg) {
+              uint8_t* box = st + (m * kRG + rg) * 2 * kCodeBox;
+              tma_load_2d(box, q, &S.full[stage], k0, qrow + 64 * rg);
+              tma_load_2d(box + kCodeBox, q, &S.full[stage], k0 + 128, qrow + 64 * rg);
+            }
           }
 #pragma unroll
           for (int j = 0; j < 4; ++j)
-            tma_load_2d(st + NMAT * 2 * kCodeBox + j * kXBox, sh ? &mp.xs : &mp.x,
+            tma_load_2d(st + NMAT * kRG * 2 * kCodeBox + j * kXBox, sh ? &mp.xs : &mp.x,
                         &S.full[stage], k0 + 64 * j, xrow);
           issued_mask |= 1u << stage;
           issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
@@ -409,8 +321,9 @@ __global__ void __launch_bounds__(kF8Threads, 1)
     }
   } else {
     // ---------------------------------------------------------------- consumers
-    // warp = kg * 4 + w: k group kg takes slice kg of every stage, w its 16 channels
-    const int kg = warp >> 2, w = warp & 3;
+    // warp = kg * (16 / KG) + w: k group kg takes slices kg, kg + KG, ... of every stage,
+    // w its 16 channels
+    const int kg = warp / Sh::kChanWarps, w = warp % Sh::kChanWarps;
     const int g = lane >> 2, t = lane & 3;
     int stage = 0;
     uint32_t phase = 0, item_phase = 0;
@@ -427,6 +340,10 @@ __global__ void __launch_bounds__(kF8Threads, 1)
       const int grp = find_group8(S.T, item);
       const int local = item - S.T.start[grp];
       const int r0 = (local / n_blk) * kFp8Rows, ch0 = (local % n_blk) * kF8Ch + w * 16;
+      // N % 64 == 0, so a warp's 16 channels are all in range or all past the end (never
+      // past it for 64-channel items); a warp past the end still takes part in every
+      // stage's hand-over
+      const bool live = kF8Ch == 64 || ch0 < N;
       const int mr = min(kFp8Rows, S.T.rows[grp] - r0);
       const bool sh = grp >= a.E;
       float acc[NMAT][4];
@@ -439,7 +356,11 @@ __global__ void __launch_bounds__(kF8Threads, 1)
           ok = false;
           break;
         }
-        f8_slice_mma<NMAT>(S.ring[stage], kg, w, lane, acc);
+        if (live) {
+#pragma unroll
+          for (int jj = 0; jj < 4 / KG; ++jj)
+            f8_slice_mma<NMAT, kRG>(S.ring[stage], kg + jj * KG, w, lane, acc);
+        }
         __syncwarp();
         if (lane == 0) mbar_arrive(&S.empty[stage]);
         if (++stage == kF8Stages) {
@@ -450,6 +371,7 @@ __global__ void __launch_bounds__(kF8Threads, 1)
       if (!ok) break;
       // the k groups' partial sums, added in group order by group 0; the next item's
       // partials are stored only once group 0 has read these
+      if (KG > 1) {
       if (kg > 0) {
 #pragma unroll
         for (int m = 0; m < NMAT; ++m)
@@ -461,7 +383,7 @@ __global__ void __launch_bounds__(kF8Threads, 1)
       if (!warp_wait(&S.part_written, item_phase)) break;
       if (kg == 0) {
 #pragma unroll
-        for (int q = 0; q < kF8KGroups - 1; ++q)
+        for (int q = 0; q < KG - 1; ++q)
 #pragma unroll
           for (int m = 0; m < NMAT; ++m)
 #pragma unroll
@@ -472,6 +394,8 @@ __global__ void __launch_bounds__(kF8Threads, 1)
       if (!warp_wait(&S.part_read, item_phase)) break;
       item_phase ^= 1u;
       if (kg > 0) continue;
+      }
+      if (!live) continue;
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const int ch = g + (i >= 2 ? 8 : 0);
@@ -505,7 +429,7 @@ bool encode_f8(EncodeTiledFn enc, CUtensorMap* m, bool codes, const void* base, 
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int NMAT>
+template <int NMAT, int KG>
 cudaError_t launch_f8(const Fp8Args& a, EncodeTiledFn enc, bool* encode_failed,
                       unsigned long long lim, cudaStream_t s) {
   *encode_failed = false;
@@ -533,8 +457,8 @@ cudaError_t launch_f8(const Fp8Args& a, EncodeTiledFn enc, bool* encode_failed,
     *encode_failed = true;
     return cudaErrorInvalidValue;
   }
-  const size_t smem = sizeof(F8Smem<NMAT>) + 1024;
-  auto* fn = fp8_gemv_kernel<NMAT>;
+  const size_t smem = sizeof(F8Smem<NMAT, KG>) + 1024;
+  auto* fn = fp8_gemv_kernel<NMAT, KG>;
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   static int grid = 0;      // one resident wave of CTAs, computed once per process
@@ -553,7 +477,8 @@ cudaError_t launch_f8(const Fp8Args& a, EncodeTiledFn enc, bool* encode_failed,
   return cudaGetLastError();
 }
 
-static_assert(sizeof(F8Smem<2>) + 1024 <= 227 * 1024, "FP8 gate/up shared memory");
+static_assert(sizeof(F8Smem<2, 4>) + 1024 <= 227 * 1024, "FP8 gate/up shared memory");
+static_assert(sizeof(F8Smem<1, 1>) + 1024 <= 227 * 1024, "FP8 down shared memory");
 
 }  // namespace
 
@@ -572,34 +497,12 @@ cudaError_t launch_quantize_fp8_rows(int rows, int cols, int w_dtype, const void
 cudaError_t launch_expert_gate_up_fp8(const Fp8Args& a, EncodeTiledFn enc,
                                       bool* encode_failed, unsigned long long wait_limit_ns,
                                       cudaStream_t s) {
-  return launch_f8<2>(a, enc, encode_failed, wait_limit_ns, s);
+  return launch_f8<2, 4>(a, enc, encode_failed, wait_limit_ns, s);
 }
 
-// The down GEMV streams W_down rows of only I codes (2 KB at I = 2048) per channel: there
-// the register-direct kernel (every warp loading its 16 rows itself, three CTAs of 8 warps
-// per SM) kept HBM busier than the TMA ring, whose per-item synchronisation of the k
-// groups weighs more on 8-stage items (DSV3-shaped decode, same-call A/B: 0.335 against
-// 0.463 ms).
 cudaError_t launch_expert_down_fp8(const Fp8Args& a, EncodeTiledFn enc, bool* encode_failed,
                                    unsigned long long wait_limit_ns, cudaStream_t s) {
-  (void)enc;
-  (void)wait_limit_ns;
-  *encode_failed = false;
-  static int grid = 0;
-  if (!grid) {
-    int per_sm = 0, dev = 0, sms = kGridSms;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-            &per_sm, reinterpret_cast<const void*>(fp8_down_kernel), kFp8Threads, 0) !=
-            cudaSuccess || per_sm < 1) {
-      cudaGetLastError();
-      per_sm = 1;
-    }
-    if (cudaGetDevice(&dev) == cudaSuccess)
-      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    grid = per_sm * (sms > 0 ? sms : kGridSms);
-  }
-  fp8_down_kernel<<<grid, kFp8Threads, 0, s>>>(a);
-  return cudaGetLastError();
+  return launch_f8<1, 1>(a, enc, encode_failed, wait_limit_ns, s);
 }
 
 }  // namespace moe

@@ -14,15 +14,14 @@
 // channel's scale multiplies the finished sum.  (A tcgen05 tile would spend its 128-row
 // operand on 8 live rows and would need the codes converted in shared memory first.)
 // A work item is (expert, up to 8 of its rows, a block of output channels).  One CTA per
-// SM: a producer warp streams the item's code rows and input rows through a shared-memory
-// ring with TMA (128-byte swizzle, 256 k per stage, about 140-200 KB in flight per SM), and
-// 16 consumer warps run the mma on what lands:
-//  gate/up  64 channels per item, gate and up rows (36 KB a stage, 5 stages); the warps
-//           form four k groups of four, each taking one 64-wide k slice of every stage for
-//           16 channels, and the groups' partial sums are added in group order at the end
-//           of the item.
-//  down     256 channels per item (68 KB a stage, 3 stages); every warp takes 16 channels
-//           over the whole k range, so an item ends with no hand-over between warps.
+// SM: a producer warp streams the item's code rows (128-row TMA boxes) and input rows
+// through a shared-memory ring (128-byte swizzle, 256 k per stage, 3 stages of about
+// 68 KB), and 16 consumer warps run the mma on what lands:
+//  gate/up  128 channels per item, gate and up rows; the warps form two k groups of eight,
+//           each taking two of the four 64-wide k slices of every stage for 16 channels,
+//           and the groups' partial sums are added in group order at the end of the item.
+//  down     256 channels per item; every warp takes 16 channels over the whole k range,
+//           so an item ends with no hand-over between warps.
 #include <string.h>
 
 #include <cuda_fp16.h>
@@ -162,21 +161,22 @@ __device__ __forceinline__ int find_group8(const Fp8Table& S, int item) {
 constexpr int kF8Chunk = 256;            // k per ring stage
 constexpr int kF8Consumers = 16;         // consumer warps, 16 channels each
 constexpr int kF8Threads = (kF8Consumers + 1) * 32;
-constexpr int kCodeBox = 64 * 128;       // TMA box: 64 channel rows x 128 codes
 constexpr int kXBox = kFp8Rows * 128;    // TMA box: 8 input rows x 64 bf16
 
 // Shape of the ring kernel.  NMAT code matrices per item (2: gate and up; 1: W_down); KG
 // k groups: the consumer warps split into KG groups of 16 / KG warps, group kg takes the
 // 64-wide k slices kg, kg + KG, ... of every stage, and the groups' partial sums are added
 // in group order at the end of an item.  An item covers 16 * 16 / KG channels; a stage
-// holds, per matrix, the item's code rows as 64-row boxes of k 0-127 and 128-255, then four
+// holds, per matrix, the item's kCh code rows of k 0-127, then of k 128-255 (each loaded as
+// TMA boxes of kBoxRows rows x 128 codes, 128 when the item has that many), then four
 // input-row boxes (64 k each).
 template <int NMAT, int KG>
 struct F8Shape {
   static constexpr int kChanWarps = kF8Consumers / KG;
   static constexpr int kCh = 16 * kChanWarps;             // channels per item
-  static constexpr int kRowGroups = kCh / 64;             // 64-row code boxes per k half
-  static constexpr int kStageBytes = NMAT * kRowGroups * 2 * kCodeBox + 4 * kXBox;
+  static constexpr int kBoxRows = kCh >= 128 ? 128 : 64;  // code rows per TMA box
+  static constexpr int kHalfBytes = kCh * 128;            // one matrix, one 128-code k half
+  static constexpr int kStageBytes = NMAT * 2 * kHalfBytes + 4 * kXBox;
   static constexpr int kStages = 210 * 1024 / kStageBytes < 5 ? 210 * 1024 / kStageBytes : 5;
 };
 
@@ -204,20 +204,19 @@ __device__ __forceinline__ uint4 ld_sw128(const uint8_t* box, int r, int c) {
 // product does not depend on the order of its terms), i.e. 16 contiguous codes of each of
 // its code rows and 16 contiguous bf16 of its input row.  acc[m] is the mma's D fragment
 // for matrix m: (channel g, rows 2t, 2t+1), (channel g + 8, rows 2t, 2t+1).
-template <int NMAT, int RG>
+template <int NMAT, int HALF>
 __device__ __forceinline__ void f8_slice_mma(const uint8_t* st, int j, int w, int lane,
                                              float (&acc)[NMAT][4]) {
   const int g = lane >> 2, t = lane & 3;
-  const int rg = RG == 1 ? 0 : (w * 16) / 64;   // the 64-row code box of this warp's rows
-  const int r_lo = (RG == 1 ? w * 16 : (w * 16) % 64) + g, r_hi = r_lo + 8;
+  const int r_lo = w * 16 + g, r_hi = r_lo + 8;
   {                                         // 64-wide k slice j of the stage
-    const uint8_t* xb = st + NMAT * RG * 2 * kCodeBox + j * kXBox;
+    const uint8_t* xb = st + NMAT * 2 * HALF + j * kXBox;
     const uint4 x0 = ld_sw128(xb, g, 2 * t), x1 = ld_sw128(xb, g, 2 * t + 1);
     const uint32_t xw[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
     const int cb = (j & 1) * 4 + t;         // 16-byte chunk of the 128-code box row
 #pragma unroll
     for (int m = 0; m < NMAT; ++m) {
-      const uint8_t* box = st + ((m * RG + rg) * 2 + (j >> 1)) * kCodeBox;
+      const uint8_t* box = st + (m * 2 + (j >> 1)) * HALF;
       const uint4 c0 = ld_sw128(box, r_lo, cb), c8 = ld_sw128(box, r_hi, cb);
       const uint32_t a0w[4] = {c0.x, c0.y, c0.z, c0.w};
       const uint32_t a8w[4] = {c8.x, c8.y, c8.z, c8.w};
@@ -244,7 +243,8 @@ __global__ void __launch_bounds__(kF8Threads, 1)
     fp8_gemv_kernel(const __grid_constant__ F8Maps mp, const Fp8Args a,
                     unsigned long long lim) {
   using Sh = F8Shape<NMAT, KG>;
-  constexpr int kF8Stages = Sh::kStages, kF8Ch = Sh::kCh, kRG = Sh::kRowGroups;
+  constexpr int kF8Stages = Sh::kStages, kF8Ch = Sh::kCh, kHalf = Sh::kHalfBytes;
+  constexpr int kBoxR = Sh::kBoxRows;
   extern __shared__ uint8_t f8_raw[];
   F8Smem<NMAT, KG>& S = *reinterpret_cast<F8Smem<NMAT, KG>*>(
       (reinterpret_cast<uintptr_t>(f8_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -293,15 +293,15 @@ __global__ void __launch_bounds__(kF8Threads, 1)
           for (int m = 0; m < NMAT; ++m) {
             const CUtensorMap* q = m == 0 ? (sh ? &mp.q0s : &mp.q0) : (sh ? &mp.q1s : &mp.q1);
 #pragma unroll
-            for (int rg = 0; rg < kRG; ++rg) {
-              uint8_t* box = st + (m * kRG + rg) * 2 * kCodeBox;
-              tma_load_2d(box, q, &S.full[stage], k0, qrow + 64 * rg);
-              tma_load_2d(box + kCodeBox, q, &S.full[stage], k0 + 128, qrow + 64 * rg);
+            for (int b = 0; b < kF8Ch / kBoxR; ++b) {
+              uint8_t* box = st + m * 2 * kHalf + b * kBoxR * 128;
+              tma_load_2d(box, q, &S.full[stage], k0, qrow + kBoxR * b);
+              tma_load_2d(box + kHalf, q, &S.full[stage], k0 + 128, qrow + kBoxR * b);
             }
           }
 #pragma unroll
           for (int j = 0; j < 4; ++j)
-            tma_load_2d(st + NMAT * kRG * 2 * kCodeBox + j * kXBox, sh ? &mp.xs : &mp.x,
+            tma_load_2d(st + NMAT * 2 * kHalf + j * kXBox, sh ? &mp.xs : &mp.x,
                         &S.full[stage], k0 + 64 * j, xrow);
           issued_mask |= 1u << stage;
           issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
@@ -359,7 +359,7 @@ __global__ void __launch_bounds__(kF8Threads, 1)
         if (live) {
 #pragma unroll
           for (int jj = 0; jj < 4 / KG; ++jj)
-            f8_slice_mma<NMAT, kRG>(S.ring[stage], kg + jj * KG, w, lane, acc);
+            f8_slice_mma<NMAT, kHalf>(S.ring[stage], kg + jj * KG, w, lane, acc);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&S.empty[stage]);
@@ -418,10 +418,10 @@ __global__ void __launch_bounds__(kF8Threads, 1)
 }
 
 bool encode_f8(EncodeTiledFn enc, CUtensorMap* m, bool codes, const void* base, uint64_t K,
-               uint64_t rows) {
+               uint64_t rows, uint32_t code_box_rows = 64) {
   const cuuint64_t dims[2] = {K, rows};
   const cuuint64_t strides[1] = {K * (codes ? 1 : 2)};
-  const cuuint32_t box[2] = {codes ? 128u : 64u, codes ? 64u : (cuuint32_t)kFp8Rows};
+  const cuuint32_t box[2] = {codes ? 128u : 64u, codes ? code_box_rows : (cuuint32_t)kFp8Rows};
   const cuuint32_t estr[2] = {1, 1};
   return enc(m, codes ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
              const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -437,17 +437,18 @@ cudaError_t launch_f8(const Fp8Args& a, EncodeTiledFn enc, bool* encode_failed,
   F8Maps mp;
   memset(&mp, 0, sizeof(mp));
   bool ok = true;
+  constexpr uint32_t br = F8Shape<NMAT, KG>::kBoxRows;
   if (NMAT == 2) {
-    ok &= encode_f8(enc, &mp.q0, true, a.Q_gate, a.H, (uint64_t)a.E * a.I);
-    ok &= encode_f8(enc, &mp.q1, true, a.Q_up, a.H, (uint64_t)a.E * a.I);
-    ok &= encode_f8(enc, &mp.q0s, true, a.has_shared ? a.Qs_gate : a.Q_gate, a.H, a.I);
-    ok &= encode_f8(enc, &mp.q1s, true, a.has_shared ? a.Qs_up : a.Q_up, a.H, a.I);
+    ok &= encode_f8(enc, &mp.q0, true, a.Q_gate, a.H, (uint64_t)a.E * a.I, br);
+    ok &= encode_f8(enc, &mp.q1, true, a.Q_up, a.H, (uint64_t)a.E * a.I, br);
+    ok &= encode_f8(enc, &mp.q0s, true, a.has_shared ? a.Qs_gate : a.Q_gate, a.H, a.I, br);
+    ok &= encode_f8(enc, &mp.q1s, true, a.has_shared ? a.Qs_up : a.Q_up, a.H, a.I, br);
     ok &= encode_f8(enc, &mp.x, false, a.Xperm, a.H, Tk);
     ok &= encode_f8(enc, &mp.xs, false, a.has_shared ? a.X : a.Xperm, a.H,
                     a.has_shared ? a.T : Tk);
   } else {
-    ok &= encode_f8(enc, &mp.q0, true, a.Q_down, a.I, (uint64_t)a.E * a.H);
-    ok &= encode_f8(enc, &mp.q0s, true, a.has_shared ? a.Qs_down : a.Q_down, a.I, a.H);
+    ok &= encode_f8(enc, &mp.q0, true, a.Q_down, a.I, (uint64_t)a.E * a.H, br);
+    ok &= encode_f8(enc, &mp.q0s, true, a.has_shared ? a.Qs_down : a.Q_down, a.I, a.H, br);
     mp.q1 = mp.q0;
     mp.q1s = mp.q0s;
     ok &= encode_f8(enc, &mp.x, false, a.h, a.I, (uint64_t)Tk + (a.has_shared ? a.T : 0));
@@ -477,7 +478,7 @@ cudaError_t launch_f8(const Fp8Args& a, EncodeTiledFn enc, bool* encode_failed,
   return cudaGetLastError();
 }
 
-static_assert(sizeof(F8Smem<2, 4>) + 1024 <= 227 * 1024, "FP8 gate/up shared memory");
+static_assert(sizeof(F8Smem<2, 2>) + 1024 <= 227 * 1024, "FP8 gate/up shared memory");
 static_assert(sizeof(F8Smem<1, 1>) + 1024 <= 227 * 1024, "FP8 down shared memory");
 
 }  // namespace
@@ -497,7 +498,7 @@ cudaError_t launch_quantize_fp8_rows(int rows, int cols, int w_dtype, const void
 cudaError_t launch_expert_gate_up_fp8(const Fp8Args& a, EncodeTiledFn enc,
                                       bool* encode_failed, unsigned long long wait_limit_ns,
                                       cudaStream_t s) {
-  return launch_f8<2, 4>(a, enc, encode_failed, wait_limit_ns, s);
+  return launch_f8<2, 2>(a, enc, encode_failed, wait_limit_ns, s);
 }
 
 cudaError_t launch_expert_down_fp8(const Fp8Args& a, EncodeTiledFn enc, bool* encode_failed,

@@ -446,7 +446,12 @@ def run_gpu(args, cfg, cf):
     # algorithmic bytes of the gate/up launch: its touched weights once, A rows in, h out
     gu_bytes = (n_touched * (2 * cfg.H * cfg.I * welt + (8 * cfg.I if cfg.fp8_experts else 0))
                 + rows * cfg.H * elt + rows * cfg.I * 2)
-    prof = traffic_from_profile(cfg.name)
+    # the profiled capture is of the workload's own routing: a run with a routing variant
+    # (group limit, expert choice, bias updates) or a capacity other than the workload's
+    # first one sees other expert sizes, so it carries no traffic figure
+    plain = (cfg == K.BY_NAME.get(cfg.name) and args.bias_update is None
+             and cf == (cfg.capacity_factors[0] if cfg.capacity_factors else None))
+    prof = traffic_from_profile(cfg.name) if plain else None
     # The headline fraction is against the burst bf16 peak (a cuBLAS GEMM timed alone);
     # the fraction of the power-capped sustained peak is given beside it.
     tpeak = pk["bf16_tflops"]

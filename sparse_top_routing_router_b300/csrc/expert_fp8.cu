@@ -186,9 +186,11 @@ struct F8Smem {
   uint8_t ring[Sh::kStages][Sh::kStageBytes];
   uint64_t full[Sh::kStages];
   uint64_t empty[Sh::kStages];
-  uint64_t part_written, part_read;   // per item: partial sums stored / consumed (KG > 1)
+  // KG > 1: the partial sums of k groups 1.. of the item that ended last; written by those
+  // groups, read by group 0
+  uint64_t part_written, part_read;
   int abort_flag;
-  float part[KG > 1 ? KG - 1 : 1][Sh::kChanWarps][NMAT * 4][32];   // groups 1.. per item
+  float part[KG > 1 ? KG - 1 : 1][KG > 1 ? Sh::kChanWarps : 1][NMAT * 4][32];
   Fp8Table T;
 };
 
@@ -261,8 +263,8 @@ __global__ void __launch_bounds__(kF8Threads, 1)
       mbar_init(&S.full[q], 1);
       mbar_init(&S.empty[q], kF8Consumers);   // every consumer warp releases each stage
     }
-    mbar_init(&S.part_written, kF8Consumers);
-    mbar_init(&S.part_read, kF8Consumers);
+    mbar_init(&S.part_written, (KG - 1) * Sh::kChanWarps);   // the warps of groups 1..
+    mbar_init(&S.part_read, Sh::kChanWarps);                 // the warps of group 0
     fence_mbar_init();
   }
   build_fp8_table(S.T, a, kMode, n_blk);   // ends with __syncthreads
@@ -325,8 +327,8 @@ __global__ void __launch_bounds__(kF8Threads, 1)
     // w its 16 channels
     const int kg = warp / Sh::kChanWarps, w = warp % Sh::kChanWarps;
     const int g = lane >> 2, t = lane & 3;
-    int stage = 0;
-    uint32_t phase = 0, item_phase = 0;
+    int stage = 0, n_items = 0;
+    uint32_t phase = 0;
     bool ok = true;
     // a bounded wait of the whole warp; false (with the abort flag raised) if it gave up
     auto warp_wait = [&](uint64_t* bar, uint32_t parity) {
@@ -369,31 +371,31 @@ __global__ void __launch_bounds__(kF8Threads, 1)
         }
       }
       if (!ok) break;
-      // the k groups' partial sums, added in group order by group 0; the next item's
-      // partials are stored only once group 0 has read these
+      // The k groups' partial sums, added in group order by group 0.  Groups 1.. store
+      // theirs and go on to the next item at once; before storing the next item's they wait
+      // until group 0 has read these (it does so as soon as this item ends, so that wait is
+      // normally over before it starts).
       if (KG > 1) {
-      if (kg > 0) {
+        const uint32_t use = (uint32_t)n_items++;   // items this CTA finished before this one
+        if (kg > 0) {
+          if (use > 0 && !warp_wait(&S.part_read, (use - 1) & 1u)) break;
 #pragma unroll
-        for (int m = 0; m < NMAT; ++m)
+          for (int m = 0; m < NMAT; ++m)
 #pragma unroll
-          for (int i = 0; i < 4; ++i) S.part[kg - 1][w][m * 4 + i][lane] = acc[m][i];
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&S.part_written);
-      if (!warp_wait(&S.part_written, item_phase)) break;
-      if (kg == 0) {
+            for (int i = 0; i < 4; ++i) S.part[kg - 1][w][m * 4 + i][lane] = acc[m][i];
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&S.part_written);
+          continue;
+        }
+        if (!warp_wait(&S.part_written, use & 1u)) break;
 #pragma unroll
         for (int q = 0; q < KG - 1; ++q)
 #pragma unroll
           for (int m = 0; m < NMAT; ++m)
 #pragma unroll
             for (int i = 0; i < 4; ++i) acc[m][i] += S.part[q][w][m * 4 + i][lane];
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&S.part_read);
-      if (!warp_wait(&S.part_read, item_phase)) break;
-      item_phase ^= 1u;
-      if (kg > 0) continue;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&S.part_read);
       }
       if (!live) continue;
 #pragma unroll

@@ -198,6 +198,16 @@ def traffic_from_profile(workload: str):
     return None
 
 
+def traffic_for_run(cfg: K.MoEConfig, cf, bias_update):
+    """The committed traffic figure for this run, if it runs what was profiled: the
+    workload's own routing.  A routing variant (group limit, expert choice, bias updates,
+    FP8 weights), other sizes or a capacity other than the workload's first one see other
+    expert sizes, so such a run carries no traffic figure."""
+    plain = (cfg == K.BY_NAME.get(cfg.name) and bias_update is None
+             and cf == (cfg.capacity_factors[0] if cfg.capacity_factors else None))
+    return traffic_from_profile(cfg.name) if plain else None
+
+
 # --------------------------------------------------------------------------- CPU oracle
 
 def blas_threads() -> int:
@@ -446,12 +456,7 @@ def run_gpu(args, cfg, cf):
     # algorithmic bytes of the gate/up launch: its touched weights once, A rows in, h out
     gu_bytes = (n_touched * (2 * cfg.H * cfg.I * welt + (8 * cfg.I if cfg.fp8_experts else 0))
                 + rows * cfg.H * elt + rows * cfg.I * 2)
-    # the profiled capture is of the workload's own routing: a run with a routing variant
-    # (group limit, expert choice, bias updates) or a capacity other than the workload's
-    # first one sees other expert sizes, so it carries no traffic figure
-    plain = (cfg == K.BY_NAME.get(cfg.name) and args.bias_update is None
-             and cf == (cfg.capacity_factors[0] if cfg.capacity_factors else None))
-    prof = traffic_from_profile(cfg.name) if plain else None
+    prof = traffic_for_run(cfg, cf, args.bias_update)
     # The headline fraction is against the burst bf16 peak (a cuBLAS GEMM timed alone);
     # the fraction of the power-capped sustained peak is given beside it.
     tpeak = pk["bf16_tflops"]

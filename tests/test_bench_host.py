@@ -3,6 +3,7 @@ the throttle reasons read from them, the source-hash gate on the committed DRAM-
 figure, and the workload description of the JSON line."""
 
 import datetime
+import dataclasses
 import hashlib
 import json
 import os
@@ -79,6 +80,24 @@ def test_traffic_figure_only_for_the_profiled_source(tmp_path, monkeypatch):
     assert bench.traffic_from_profile("a") is None
     monkeypatch.setattr(bench, "PROFILE_TRAFFIC", str(tmp_path / "missing.txt"))
     assert bench.traffic_from_profile("a") is None
+
+
+def test_traffic_figure_only_for_the_profiled_routing(monkeypatch):
+    monkeypatch.setattr(bench, "traffic_from_profile", lambda name: {"workload_name": name})
+    dsv3, sw = K.DSV3_PREFILL, K.SWITCH
+    assert bench.traffic_for_run(dsv3, None, None) == {"workload_name": dsv3.name}
+    assert bench.traffic_for_run(sw, sw.capacity_factors[0], None) is not None
+    # another capacity, a routing variant, FP8 weights, bias updates or other sizes: none
+    assert bench.traffic_for_run(sw, 1.25, None) is None
+    assert bench.traffic_for_run(dataclasses.replace(dsv3, n_groups=8, topk_groups=4),
+                                 None, None) is None
+    assert bench.traffic_for_run(dataclasses.replace(dsv3, expert_choice=True), None,
+                                 None) is None
+    assert bench.traffic_for_run(dataclasses.replace(dsv3, fp8_experts=True), None,
+                                 None) is None
+    assert bench.traffic_for_run(dsv3, None, 1e-3) is None
+    assert bench.traffic_for_run(K.scaled(dsv3, name=dsv3.name + "@T=64", T=64), None,
+                                 None) is None
 
 
 def test_committed_traffic_profile_is_well_formed():

@@ -16,6 +16,8 @@
 //            the leader CTA issues tcgen05.mma.cta_group::2 M=256 N=256 over both CTAs'
 //            shared memory, and each CTA's TMEM receives its 128 rows.  Per SM the
 //            operand traffic per MMA cycle drops by a third and the ring is 1.5x deeper.
+//   single-CTA clusters (MCA = true, the down GEMM): two CTAs take the two n-tiles of one
+//            128-row block and each multicasts half of its A rows to both.
 // Work items are (group, n-tile, m-tile) with the m-tile fastest, enumerated on the
 // device from the dispatch offsets (the host never learns m_i), assigned round-robin
 // to the resident CTAs (or CTA pairs).  Neighbouring units thus share the weight tile of
@@ -238,7 +240,12 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
 
 // SWAP: single-CTA launches of decode-sized batches, whose tiny tails swap operands; a
 // separate instantiation, so that the other kernels keep their code unchanged.
-template <int MODE, bool PAIR, bool SWAP = false>
+// MCA: single-CTA tiles run by clusters of two CTAs that take the two n-tiles of one
+// (group, n-tile pair, m-tile) unit; each CTA loads half of the unit's A rows and
+// multicasts them to both, so A is read from L2 once for two tiles.  A ring stage is
+// released only when both CTAs' MMAs have read it (each MMA issuer commits to both CTAs'
+// empty barriers).
+template <int MODE, bool PAIR, bool SWAP = false, bool MCA = false>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap mA,
                         const __grid_constant__ CUtensorMap mA_sh,
@@ -254,11 +261,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   Smem<PAIR>& S = *reinterpret_cast<Smem<PAIR>*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int n_tiles_n = (p.N + p.n_tile - 1) / p.n_tile;
   const int nkb = (p.K + BK - 1) / BK;
-  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;   // 0 = leader
-  const int unit = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
-  const int n_units = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
+  static_assert(!MCA || (!PAIR && !SWAP && MODE != ROUTER), "MCA: single-CTA expert GEMMs");
+  constexpr bool CL = PAIR || MCA;                         // launched as clusters of two
+  const uint32_t rank = CL ? cluster_ctarank() : 0u;       // 0 = leader
+  const int unit = CL ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+  const int n_units = CL ? (int)(gridDim.x >> 1) : (int)gridDim.x;
+  const int mblock = MODE == ROUTER ? 0 : kMBlockRows / Cfg<PAIR>::kTileM;
+  // MCA: a unit spans two n-tiles (the host launches MCA only for an even count)
+  const int n_tile_u = MCA ? 2 * p.n_tile : p.n_tile;
+  const int n_units_n = (p.N + n_tile_u - 1) / n_tile_u;
+  auto decode = [&](int t) {
+    TileInfo ti = decode_tile<PAIR>(S, t, n_tile_u, n_units_n, mblock);
+    if (MCA) ti.n0 += (int)rank * p.n_tile;
+    return ti;
+  };
 
   // ---------------------------------------------------------------- set-up
   const int ngroups = (MODE == ROUTER) ? 1 : p.E + (p.has_shared ? 1 : 0);
@@ -267,7 +284,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     S.abort_flag = 0;
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&S.full[s], 1);
-      mbar_init(&S.empty[s], 1);
+      mbar_init(&S.empty[s], MCA ? 2 : 1);   // MCA: both CTAs' MMAs release a stage
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&S.tfull[b], 1);
@@ -314,7 +331,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   __syncthreads();
   for (int g = tid; g < ngroups; g += kThreads)
-    S.tile_start[g] = ((S.grp_rows[g] + TM - 1) / TM) * n_tiles_n *
+    S.tile_start[g] = ((S.grp_rows[g] + TM - 1) / TM) * n_units_n *
                       (MODE == ROUTER ? p.splits : 1);     // count, scanned below
   __syncthreads();
   if (warp == 0) {
@@ -338,14 +355,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if (PAIR) cluster_sync();   // the peer's barriers exist before anyone signals them
+  if (CL) cluster_sync();   // the peer's barriers exist before anyone signals them
   tc_fence_after();
   const uint32_t tmem_base = S.tmem_base;
   const int total = S.total_tiles;
   const volatile int* abort_flag = &S.abort_flag;
   const unsigned long long lim = p.wait_limit_ns;
   constexpr bool M64 = !PAIR && MODE != ROUTER;   // M = 64 tail tiles (single CTA)
-  const int mblock = MODE == ROUTER ? 0 : kMBlockRows / Cfg<PAIR>::kTileM;
 
   if (warp == 0 && lane == 0) {
     // ---------------------------------------------------------------- TMA producer
@@ -362,7 +378,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t issued_mask = 0, issued_parity = 0;
     bool ok = true;
     for (int tile = unit; tile < total && ok; tile += n_units) {
-      const TileInfo ti = decode_tile<PAIR>(S, tile, p.n_tile, n_tiles_n, mblock);
+      const TileInfo ti = decode(tile);
       const bool sh = (MODE == ROUTER) || ti.g >= p.E;
       const CUtensorMap* a_map = sh ? &mA_sh : &mA;
       // a pair's half tile (M = 128) takes 64 rows from each CTA
@@ -405,7 +421,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           // (the next two loads of it hit L2)
           const int ka = MODE == ROUTER ? (kb / 3) * BK : kx;
           const int kw = MODE == ROUTER ? (kb % 3) * p.a_kmod + (kb / 3) * BK : kx;
-          tma_load_2d(st, a64 ? (sh ? &hm.a64_sh : &hm.a64) : a_map, &S.full[stage], ka, ay);
+          if (MCA) {
+            // half of the unit's A rows from each CTA, multicast to both; a tail of at most
+            // 64 rows comes whole from the leader
+            const CUtensorMap* a_half = sh ? &hm.a64_sh : &hm.a64;
+            if (!a64)
+              tma_load_2d_mc(st + (int)rank * (kBoxBytes / 2), a_half, &S.full[stage], ka,
+                             ay + 64 * (int)rank, 0x3);
+            else if (rank == 0)
+              tma_load_2d_mc(st, a_half, &S.full[stage], ka, ay, 0x3);
+          } else {
+            tma_load_2d(st, a64 ? (sh ? &hm.a64_sh : &hm.a64) : a_map, &S.full[stage], ka, ay);
+          }
           const CUtensorMap* b0 = sh ? &mB0_sh : &mB0;
           const CUtensorMap* b1 = (MODE == GATE_UP) ? (sh ? &mB1_sh : &mB1) : b0;
           const int n1 = (MODE == GATE_UP) ? ti.n0 : ti.n0 + 128;
@@ -468,7 +495,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int s = 0; s < kStages; ++s)
           if (issued_mask >> s & 1u) mbar_wait(&S.full[s], issued_parity >> s & 1u, &zero, lim);
     }
-  } else if (warp == 1 && lane == 0 && rank == 0) {
+  } else if (warp == 1 && lane == 0 && (rank == 0 || !PAIR)) {
     // ---------------------------------------------------------------- MMA issuer
     int stage = 0, acc = 0;
     uint32_t phase = 0, acc_phase = 0;
@@ -481,17 +508,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t sw_idesc = 0;
       uint32_t mma_idesc = idesc;
       if (MODE == ROUTER) {
-        const TileInfo ti = decode_tile<PAIR>(S, tile, p.n_tile, n_tiles_n, mblock);
+        const TileInfo ti = decode(tile);
         kb_lo = (int)((long long)nkb * ti.z / p.splits);
         kb_hi = (int)((long long)nkb * (ti.z + 1) / p.splits);
       } else if (SWAP || M64) {
-        const TileInfo ti = decode_tile<PAIR>(S, tile, p.n_tile, n_tiles_n, mblock);
+        const TileInfo ti = decode(tile);
         swap = SWAP && is_swapped_tail(ti, p.swap_rows);
         if (swap) sw_idesc = idesc_bf16_f32(128, swap_cols(ti));
         else if (M64 && is_m64_tail(ti)) mma_idesc = idesc_bf16_f32(64, 256);
       }
       uint32_t pair_idesc = C::kIdesc;
-      if (PAIR && half_tile<PAIR>(decode_tile<PAIR>(S, tile, p.n_tile, n_tiles_n, mblock)))
+      if (PAIR && half_tile<PAIR>(decode(tile)))
         pair_idesc = idesc_bf16_f32(128, 256);
       const bool got = PAIR ? mbar_wait_cluster(&S.tempty[acc], acc_phase ^ 1u, abort_flag, lim)
                             : mbar_wait(&S.tempty[acc], acc_phase ^ 1u, abort_flag, lim);
@@ -538,6 +565,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         if (PAIR) umma_commit_pair_mc(&S.empty[stage], 0x3);
+        else if (MCA) umma_commit_mc(&S.empty[stage], 0x3);
         else umma_commit(&S.empty[stage]);
         if (++stage == kStages) {
           stage = 0;
@@ -570,7 +598,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int tile = unit; tile < total; tile += n_units) {
-      const TileInfo ti = decode_tile<PAIR>(S, tile, p.n_tile, n_tiles_n, mblock);
+      const TileInfo ti = decode(tile);
       const bool got = mbar_wait(&S.tfull[acc], acc_phase, abort_flag, lim);
       if (!__all_sync(0xffffffffu, got)) {
         S.abort_flag = 1;
@@ -769,7 +797,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ---------------------------------------------------------------- tear-down
   tc_fence_before();
   __syncthreads();
-  if (PAIR) cluster_sync();   // no MMA, copy or arrival targets either CTA any more
+  if (CL) cluster_sync();   // no MMA, copy or arrival targets either CTA any more
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
@@ -803,11 +831,14 @@ bool encode_3d(EncodeTiledFn enc, CUtensorMap* m, const void* base, uint64_t inn
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Number of CTA pairs that can be resident at once (persistent grid), cached per process.
+// Number of clusters of two CTAs that can be resident at once (persistent grid), cached
+// per process and kernel.
 int max_pairs(const void* fn, size_t smem, int num_sms) {
-  static int cached[2] = {0, 0};
-  const int slot = fn == reinterpret_cast<const void*>(grouped_gemm_kernel<GATE_UP, true>) ? 0 : 1;
-  if (cached[slot]) return cached[slot];
+  static const void* fns[8] = {};
+  static int cached[8] = {};
+  int slot = 0;
+  while (slot < 7 && fns[slot] && fns[slot] != fn) ++slot;
+  if (fns[slot] == fn && cached[slot]) return cached[slot];
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(num_sms & ~1);
   cfg.blockDim = dim3(kThreads);
@@ -824,6 +855,7 @@ int max_pairs(const void* fn, size_t smem, int num_sms) {
     cudaGetLastError();
     n = num_sms / 2;
   }
+  fns[slot] = fn;
   cached[slot] = n;
   return n;
 }
@@ -904,19 +936,30 @@ cudaError_t launch_tc(const ExpertArgs& a, EncodeTiledFn enc, bool* encode_faile
       (Tk + TM - 1) / TM + a.E + (a.has_shared ? (a.T + TM - 1) / TM : 0);
   const long long tiles_bound = m_tiles_bound * n_tiles_n;
   const size_t smem = sizeof(Smem<PAIR>) + 1024;
+  // The down GEMM's single CTAs run as clusters of two that share each A row block when
+  // its reduction is short (K = I <= 2048) and the n-tile count is even.  Same-call A/Bs:
+  // DSV3-shaped prefill (K = 2048) down 2.25 against 2.30 ms (20 steps) and 2.45 against
+  // 2.52 ms (200 steps); but the Switch-shaped down GEMM (K = 8192) 0.683 against
+  // 0.671 ms and the DSV3-shaped gate/up GEMM (K = 7168) 3.91 against 3.76 ms.
+  // Decode-sized batches keep the operand-swapped kernel.
+  constexpr bool kMcaMode = MODE == DOWN && !PAIR;
+  const bool mca = kMcaMode && K <= 2048 && p.swap_rows == 0 && n_tiles_n % 2 == 0 &&
+                   a.num_sms >= 2;
   auto* fn = p.swap_rows > 0 ? grouped_gemm_kernel<MODE, PAIR, !PAIR>
-                             : grouped_gemm_kernel<MODE, PAIR, false>;
+             : (mca ? grouped_gemm_kernel<MODE, PAIR, false, kMcaMode>
+                    : grouped_gemm_kernel<MODE, PAIR, false>);
   cudaError_t e =
       cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  if (!PAIR) {
+  if (!PAIR && !mca) {
     const int grid = (int)(tiles_bound < a.num_sms ? (tiles_bound > 0 ? tiles_bound : 1)
                                                    : a.num_sms);
     fn<<<grid, kThreads, smem, s>>>(mA, mA_sh, mB0, mB1, mB0_sh, mB1_sh, hm, p);
     return cudaGetLastError();
   }
   const int pairs_max = max_pairs(reinterpret_cast<const void*>(fn), smem, a.num_sms);
-  const int pairs = (int)(tiles_bound < pairs_max ? (tiles_bound > 0 ? tiles_bound : 1)
+  const long long units_bound = mca ? tiles_bound / 2 : tiles_bound;
+  const int pairs = (int)(units_bound < pairs_max ? (units_bound > 0 ? units_bound : 1)
                                                   : pairs_max);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * pairs);

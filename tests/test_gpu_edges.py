@@ -203,11 +203,14 @@ def test_status_survives_and_context_reusable(ctx):
     P.check_routing(run, ref)
 
 
-def test_bounded_wait_timeout_is_reported(ctx):
+@pytest.mark.parametrize("H", [128, 512])
+def test_bounded_wait_timeout_is_reported(ctx, H):
     """A barrier that nothing completes (the test hook withholds the first operand load of
     every CTA of the tensor-core kernels): the bounded waits run out, the kernels record
-    MOE_ERR_TIMEOUT, release tensor memory and return; the context keeps working."""
-    cfg = _small(T=64, H=128, I=128, shared=True)
+    MOE_ERR_TIMEOUT, release tensor memory and return; the context keeps working.  With
+    H = 512 the down GEMM runs as clusters of two CTAs, each waiting on stages that the
+    other's multicast also fills."""
+    cfg = _small(T=64, H=H, I=128, shared=True)
     d = make_inputs(cfg, device="cuda")
     layer = MoELayer(cfg, d, ctx=ctx)
     ctx.set_test_hook(B.MOE_TEST_HOOK_WITHHOLD_LOAD, wait_limit_ms=50)

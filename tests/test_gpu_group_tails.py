@@ -3,7 +3,9 @@
 that every tail shape of the tensor-core kernel runs - M = 64 tails with 64-row A boxes,
 full 128-row tiles, multi-tile groups, groups taller than the 2048-row m-block - and every
 output row is compared with the oracle's SwiGLU expert ("LLM Internals §14.2.1" step 5,
-§14.2.2 three matrices) on the same rows."""
+§14.2.2 three matrices) on the same rows.  H = 512 gives the down GEMM two 256-column
+n-tiles, so its tiles run as clusters of two CTAs that multicast the shared A rows; with
+H = 128 they run as plain single CTAs."""
 
 import numpy as np
 import pytest
@@ -19,10 +21,11 @@ pytestmark = pytest.mark.gpu
 SIZES = [1, 16, 17, 63, 64, 65, 127, 128, 129, 255, 256, 257, 2177]
 
 
+@pytest.mark.parametrize("H", [128, 512])
 @pytest.mark.parametrize("shared", [False, True])
-def test_every_row_at_tile_boundaries(shared):
+def test_every_row_at_tile_boundaries(shared, H):
     ctx = B.Context(0)
-    E, H, I, k = len(SIZES), 128, 192, 1
+    E, I, k = len(SIZES), 192, 1
     T = sum(SIZES)
     g = torch.Generator(device="cuda")
     g.manual_seed(7)

@@ -24,6 +24,8 @@
 //           so an item ends with no hand-over between warps.
 #include <string.h>
 
+#include <atomic>
+
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
 
@@ -464,17 +466,29 @@ cudaError_t launch_f8(const Fp8Args& a, EncodeTiledFn enc, bool* encode_failed,
   auto* fn = fp8_gemv_kernel<NMAT, KG>;
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  static int grid = 0;      // one resident wave of CTAs, computed once per process
+  // one resident wave of CTAs, computed once per device (the ordinals past the table are
+  // queried every time)
+  static std::atomic<int> grids[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    dev = -1;
+  }
+  int grid = (dev >= 0 && dev < 64) ? grids[dev].load(std::memory_order_relaxed) : 0;
   if (!grid) {
-    int per_sm = 0, dev = 0, sms = kGridSms;
+    int per_sm = 0, sms = kGridSms;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kF8Threads, smem) !=
             cudaSuccess || per_sm < 1) {
       cudaGetLastError();
       per_sm = 1;
     }
-    if (cudaGetDevice(&dev) == cudaSuccess)
-      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (dev >= 0 && cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
+                        cudaSuccess) {
+      cudaGetLastError();
+      sms = kGridSms;
+    }
     grid = per_sm * (sms > 0 ? sms : kGridSms);
+    if (dev >= 0 && dev < 64) grids[dev].store(grid, std::memory_order_relaxed);
   }
   fn<<<grid, kF8Threads, smem, s>>>(mp, a, lim);
   return cudaGetLastError();

@@ -32,6 +32,8 @@
 // CTA drains what it can of its in-flight copies and MMAs, frees TMEM and returns.
 #include <string.h>
 
+#include <mutex>
+
 #include "moe_internal.h"
 #include "ptx.cuh"
 
@@ -832,13 +834,17 @@ bool encode_3d(EncodeTiledFn enc, CUtensorMap* m, const void* base, uint64_t inn
 }
 
 // Number of clusters of two CTAs that can be resident at once (persistent grid), cached
-// per process and kernel.
+// per kernel and SM count (thread-safe; a device with another SM count is queried anew).
 int max_pairs(const void* fn, size_t smem, int num_sms) {
-  static const void* fns[8] = {};
-  static int cached[8] = {};
-  int slot = 0;
-  while (slot < 7 && fns[slot] && fns[slot] != fn) ++slot;
-  if (fns[slot] == fn && cached[slot]) return cached[slot];
+  static std::mutex mu;
+  static const void* fns[16] = {};
+  static int sms_of[16] = {};
+  static int cached[16] = {};
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < 16; ++i)
+      if (fns[i] == fn && sms_of[i] == num_sms) return cached[i];
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(num_sms & ~1);
   cfg.blockDim = dim3(kThreads);
@@ -855,8 +861,14 @@ int max_pairs(const void* fn, size_t smem, int num_sms) {
     cudaGetLastError();
     n = num_sms / 2;
   }
-  fns[slot] = fn;
-  cached[slot] = n;
+  std::lock_guard<std::mutex> lock(mu);
+  for (int i = 0; i < 16; ++i)
+    if (!fns[i]) {
+      fns[i] = fn;
+      sms_of[i] = num_sms;
+      cached[i] = n;
+      break;
+    }
   return n;
 }
 

@@ -36,7 +36,10 @@ Readings where the pages are silent:
   * group-limited routing scores a group by its k/M largest UNBIASED affinities, and
     its groups are runs of consecutive expert indices;
   * SwiGLU expert: h = SiLU(x W_gate) * (x W_up), y = h W_down, SiLU(z) = z*sigmoid(z),
-    no biases.
+    no biases;
+  * a bf16 layer may store the intermediate h in bf16 between its two projections (it is
+    a GEMM operand like the inputs); `round_bf16` gives that variant of the expert
+    (`h_round`), the default stays exact.
 
 Parity is pinned for every function here (tests/test_oracle_pins.py); none is unpinned.
 """
@@ -315,18 +318,36 @@ def dequantize_fp8_rows(q: np.ndarray, scale: np.ndarray) -> np.ndarray:
 # Step 5: one SwiGLU expert                                  [LI §14.2.1 step 5, §14.2.2]
 # ---------------------------------------------------------------------------
 
+def round_bf16(v: np.ndarray) -> np.ndarray:
+    """The bf16 value nearest to each (finite) v, ties to even, as float64.
+
+    bf16 is the upper half of an fp32 bit pattern, so v is first rounded to fp32 (numpy's
+    correctly rounded conversion) and then the lower 16 bits of that pattern are rounded
+    off: adding 0x7FFF plus the lowest kept bit carries into the kept half exactly when
+    the dropped half exceeds one half ulp, or equals it with the kept half odd.
+    """
+    v32 = np.ascontiguousarray(np.asarray(v, dtype=f64).astype(np.float32))
+    bits = v32.view(np.uint32).astype(np.uint64)
+    bits = (bits + 0x7FFF + ((bits >> 16) & 1)) & 0xFFFF0000
+    return bits.astype(np.uint32).view(np.float32).astype(f64)
+
+
 def swiglu_expert(x: np.ndarray, W_gate: np.ndarray, W_up: np.ndarray,
-                  W_down: np.ndarray) -> np.ndarray:
+                  W_down: np.ndarray,
+                  h_round: Optional[Callable[[np.ndarray], np.ndarray]] = None) -> np.ndarray:
     """y = (SiLU(x W_gate^T) * (x W_up^T)) W_down^T for a batch of rows x[m, H].
 
     Weights are stored output-major: W_gate, W_up [I, H]; W_down [H, I].  The expert is
     the three-matrix SwiGLU of [LI §14.2.2]; [LI §14.2.1 step 5] projects [m, H] to
-    [m, I] and back to H.
+    [m, I] and back to H.  `h_round`, if given, is applied to the [m, I] intermediate
+    before the second projection (e.g. round_bf16 for a layer that stores it in bf16).
     """
     x = np.asarray(x, dtype=f64)
     a = x @ np.asarray(W_gate, dtype=f64).T
     u = x @ np.asarray(W_up, dtype=f64).T
     h = a * sigmoid(a) * u
+    if h_round is not None:
+        h = h_round(h)
     return h @ np.asarray(W_down, dtype=f64).T
 
 
@@ -464,13 +485,15 @@ ExpertFn = Callable[[int], Tuple[np.ndarray, np.ndarray, np.ndarray]]
 
 
 def combine_subset(X, routing: Dict[str, np.ndarray], expert: ExpertFn, tokens,
-                   shared: Optional[Tuple[np.ndarray, np.ndarray, np.ndarray]] = None
+                   shared: Optional[Tuple[np.ndarray, np.ndarray, np.ndarray]] = None,
+                   h_round: Optional[Callable[[np.ndarray], np.ndarray]] = None
                    ) -> np.ndarray:
     """Steps 5-6 for the given tokens: Y[t] = sum over kept j of g_j * E_{idx_j}(x_t)
     plus the shared expert's output  [LI §14.2.1 step 6; KM final weighted sum].
 
     `expert(e)` returns (W_gate[e], W_up[e], W_down[e]); experts are fetched one at a
-    time, and only those that a kept slot of the given tokens uses.
+    time, and only those that a kept slot of the given tokens uses.  `h_round` is passed
+    to every expert (swiglu_expert).
     """
     tokens = np.asarray(tokens, dtype=np.int64)
     X = np.asarray(X)
@@ -487,10 +510,10 @@ def combine_subset(X, routing: Dict[str, np.ndarray], expert: ExpertFn, tokens,
         Wgt, Wup, Wdn = expert(e)
         sel = np.asarray(uses[e], dtype=np.int64)
         sel_t, sel_j = sel[:, 0], sel[:, 1]
-        o = swiglu_expert(X[tokens[sel_t]], Wgt, Wup, Wdn)
+        o = swiglu_expert(X[tokens[sel_t]], Wgt, Wup, Wdn, h_round)
         Y[sel_t] += gate[tokens[sel_t], sel_j][:, None] * o
     if shared is not None:
-        Y += swiglu_expert(X[tokens], *shared)
+        Y += swiglu_expert(X[tokens], *shared, h_round=h_round)
     return Y
 
 

@@ -23,6 +23,11 @@ GAP_EXCLUDE = 1e-6          # rows whose k-th/(k+1)-th key margin is below this 
 # 200x finer than the bf16 resolution of a gate near 0.5.
 GATE_ATOL = 1e-5
 Y_TOL = {"bf16": 2e-2, "f32": 1e-4}   # max-abs error / RMS(Y_oracle)
+# A bf16 layer stores the expert intermediate h in bf16 between its two projections.  On
+# every token the output is held to the same bound against the oracle that rounds h the
+# same way (O.round_bf16): against the exact oracle, that rounding alone takes the worst
+# output of the Switch-shaped layer to 2.1e-2 * RMS(Y) (fp64 elsewhere), so the exact
+# comparison runs on the seeded token samples, as the workloads' recipe states.
 
 
 def to_np(t: torch.Tensor) -> np.ndarray:
@@ -114,6 +119,7 @@ def expert_fetch(d: Dict[str, torch.Tensor]):
 
 def check_output(run: Run, ref: Dict[str, np.ndarray], n_tokens: Optional[int] = None,
                  seed: int = 1) -> Dict[str, float]:
+    """Y of a seeded token sample (every token when n_tokens is None) against the oracle."""
     c, d, L = run.cfg, run.inputs, run.layer
     tokens = token_subset(c.T, n_tokens if n_tokens else c.T, seed).numpy()
     # use tokens whose routing agrees (all of them unless a row was excluded)
@@ -140,6 +146,33 @@ def check_output(run: Run, ref: Dict[str, np.ndarray], n_tokens: Optional[int] =
     tol = Y_TOL[c.dtype] * rms
     assert err <= tol, f"max |dY| = {err:.3e} > {tol:.3e} (RMS {rms:.3e})"
     return {"max_abs_err": err, "rms": rms, "ratio": err / rms, "tokens": int(tokens.size)}
+
+
+def check_output_bf16_h(run: Run, ref: Dict[str, np.ndarray]) -> Dict[str, float]:
+    """Y of every token against the oracle whose experts round h to bf16 (the layer's
+    storage of the intermediate), to Y_TOL["bf16"] * RMS(Y)."""
+    c, d, L = run.cfg, run.inputs, run.layer
+    assert c.dtype == "bf16"
+    idx = to_np(L.idx).astype(np.int64)
+    kept_gpu = to_np(L.row_of_slot).reshape(c.T, c.k) >= 0
+    kept_ref = ref["row_of_slot"].reshape(c.T, c.k) >= 0
+    agree = np.all(idx == ref["idx"], axis=1) & np.all(kept_gpu == kept_ref, axis=1)
+    tokens = np.nonzero(agree)[0]
+    shared = None
+    if c.shared:
+        shared = (to_np(d["Ws_gate"]), to_np(d["Ws_up"]), to_np(d["Ws_down"]))
+    Yref = O.combine_subset(to_np(d["X"]), ref, expert_fetch(d), tokens, shared,
+                            h_round=O.round_bf16)
+    Y = to_np(L.Y[torch.as_tensor(tokens, device=L.Y.device)])
+    live = np.any(Yref != 0.0, axis=1)
+    assert np.all(Y[~live] == 0.0), "a fully dropped token has a non-zero output"
+    if not live.any():
+        return {"bf16_h_ratio": 0.0, "tokens": int(tokens.size)}
+    rms = float(np.sqrt(np.mean(Yref[live] ** 2)))
+    err = float(np.abs(Y - Yref).max())
+    tol = Y_TOL["bf16"] * rms
+    assert err <= tol, f"max |dY| against the bf16-h oracle = {err:.3e} > {tol:.3e}"
+    return {"bf16_h_ratio": err / rms, "tokens": int(tokens.size)}
 
 
 def check_stats(run: Run, ref: Dict[str, np.ndarray]) -> Dict[str, float]:

@@ -1,7 +1,10 @@
 """GPU parity of the whole forward against the fp64 oracle, through the C ABI.
 
-Small cases (several tiles and ragged tails) compare every token; the full-size
-workloads compare the routing of every token and the output of a seeded token sample.
+Small cases (several tiles and ragged tails) and the full-size workloads alike compare the
+routing, dispatch and gates of every token, and the output of every token against the
+oracle that stores the expert intermediate in bf16 as the layer does; the output is also
+compared with the exact oracle on every token of the small cases and on a seeded sample
+of the full-size ones.
 """
 
 import gc
@@ -58,14 +61,21 @@ def test_small_full_parity(cfg):
         out = P.check_output(run, ref)
         st = P.check_stats(run, ref)
         assert out["tokens"] >= cfg.T - info["excluded_rows"]
+        if cfg.dtype == "bf16":
+            out.update(P.check_output_bf16_h(run, ref))
         print(cfg.name, cf, info, out, st)
     _cleanup()
 
 
-# (workload, capacity factor, tokens whose output is compared with the oracle); routing,
-# dispatch and gates are compared on every token
-FULL = [(K.MIXTRAL, None, 256), (K.DSV3_DECODE, None, 64), (K.DSV3_PREFILL, None, 256),
-        (K.SWITCH, 1.0, 256), (K.SWITCH, 1.25, 256)]
+# (workload, capacity factor, seeded token sample compared with the exact oracle to the
+# 2e-2 * RMS(Y) bound); routing, dispatch and gates are compared on every token, and so
+# is Y, to the same bound, against the oracle that stores h in bf16 as the layer does.
+# (Against the exact oracle the bound does not hold for every token of every layer:
+# rounding h to bf16 alone moves the Switch-shaped layer's worst output by 2.1e-2 *
+# RMS(Y).)  The oracle's expert stage over a whole DSV3-shaped batch takes about 15 s on
+# 16 host cores.
+FULL = [(K.MIXTRAL, None, 512), (K.DSV3_DECODE, None, 64), (K.DSV3_PREFILL, None, 512),
+        (K.SWITCH, 1.0, 512), (K.SWITCH, 1.25, 512)]
 
 
 @pytest.mark.parametrize("cfg,cf,n_tok", FULL,
@@ -77,6 +87,9 @@ def test_full_size_parity(cfg, cf, n_tok):
     info = P.check_routing(run, ref)
     P.check_dispatch(run, P.to_np(run.layer.idx).astype(np.int64))
     out = P.check_output(run, ref, n_tokens=n_tok)
+    full = P.check_output_bf16_h(run, ref)
+    assert full["tokens"] >= cfg.T - info["excluded_rows"]
+    out["bf16_h"] = full
     st = P.check_stats(run, ref) if cfg.alpha else {}
     print(cfg.name, cf, info, out, st)
     del run

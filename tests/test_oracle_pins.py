@@ -268,6 +268,33 @@ def test_swiglu_one_hot_orientation():
             assert abs(y[o] - want) < 1e-13
 
 
+def test_round_bf16_matches_torch_and_ties_go_to_even():
+    """The oracle's bf16 rounding against torch's bf16 conversion (round to nearest even),
+    on random values over many binades and on exact halfway cases."""
+    import torch
+    rng = np.random.default_rng(11)
+    v = rng.standard_normal(200000) * np.exp2(rng.integers(-30, 30, 200000))
+    want = torch.from_numpy(v.astype(np.float32)).to(torch.bfloat16).double().numpy()
+    assert np.array_equal(O.round_bf16(v.astype(np.float32)), want)
+    # bf16 keeps 8 significant bits: 1 + 2^-8 lies halfway between 1 and 1 + 2^-7
+    assert O.round_bf16(np.array([1.0 + 2.0 ** -8]))[0] == 1.0              # to even
+    assert O.round_bf16(np.array([1.0 + 3 * 2.0 ** -8]))[0] == 1.0 + 2.0 ** -6  # to even
+    assert O.round_bf16(np.array([1.0 + 2.0 ** -8 + 2.0 ** -20]))[0] == 1.0 + 2.0 ** -7
+    assert O.round_bf16(np.array([-(1.0 + 2.0 ** -8)]))[0] == -1.0
+    assert O.round_bf16(np.array([0.0, 3.0, -0.15625]))[2] == -0.15625   # exact values stay
+
+
+def test_swiglu_rounds_the_intermediate_only_when_asked():
+    """h_round acts on h between the projections: with H = I = 1 the output is
+    w_d * round(silu(w_g x) * (w_u x)); without it the output is exact."""
+    x, wg, wu, wd = np.array([[1.0]]), np.array([[0.7]]), np.array([[1.3]]), np.array([[3.0]])
+    h = _silu(0.7) * 1.3
+    y = O.swiglu_expert(x, wg, wu, wd, h_round=O.round_bf16)[0, 0]
+    assert y == 3.0 * O.round_bf16(np.array([h]))[0]
+    assert O.round_bf16(np.array([h]))[0] != h
+    assert abs(O.swiglu_expert(x, wg, wu, wd)[0, 0] - 3.0 * h) < 1e-14
+
+
 def test_layer_single_expert_is_dense_swiglu():
     """E = 1, k = 1: the gate is 1 and the layer is the one expert."""
     X = np.array([[1.0], [-0.5]])

@@ -33,7 +33,9 @@ def _worker(rank, world, port, out):
 
 def test_max_over_ranks_and_seeds():
     world, port = 2, _free_port()
-    with mp.Manager() as m:
+    # the manager process is spawned too: a fork of a process that already runs threads
+    # (torch's) may deadlock
+    with mp.get_context("spawn").Manager() as m:
         out = m.dict()
         mp.spawn(_worker, args=(world, port, out), nprocs=world, join=True)
         res = dict(out)
